@@ -1,0 +1,326 @@
+"""Benchmark of the batched rejection sampler on one GB300 (or N replicas).
+
+One step = one spec_reject_sample() call over a whole synthetic batch (every kernel
+of the path: row statistics, per-request finalize, and for explicit draft
+probabilities the residual and recovery passes), inputs resident in HBM.
+
+Default workload: the large-batch sweep point B=1024, K=8, V=128256, bf16 target
+logits, explicit fp32 draft probabilities, temperature 0.7 (2.36 GB of logits +
+4.2 GB of draft probabilities per step: larger than L2, so no flush is needed).
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead (a bounded
+sample of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s vs ~8 TB/s peak (1 GB300)"
+UNIT = "draft positions/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_rejection_spec_gb300", "csrc", "spec_reject.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(workload):
+    """DRAM bytes per launch of the row-statistics kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get("rowstats", {})
+    if e.get("source_sha") != source_sha():
+        return None
+    per_unit = e.get("dram_bytes_per_row")
+    return None if per_unit is None else per_unit
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, target_s=8.0):
+    """The oracle as it stands on the host cores, on the first requests of the workload."""
+    import oracle
+    cores = oracle.max_threads()
+    n = 8
+    while True:
+        n = min(n, w["B"])
+        t0 = time.perf_counter()
+        oracle.reject_sample_workload(w, num_requests=n)
+        dt = time.perf_counter() - t0
+        if dt > target_s / 4 or n >= w["B"]:
+            break
+        n = min(w["B"], max(n * 2, int(n * (target_s / 2) / max(dt, 1e-3))))
+    positions = int(w["cu_num_draft"][n])
+    return {"value": positions / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {w['B']} requests ({positions} draft positions), {dt:.2f} s wall"}
+
+
+def run_reference(args, w, meta):
+    """--impl reference: the CPU oracle on bounded samples of the same workload."""
+    import oracle
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    n = 8
+    t0 = time.perf_counter()
+    oracle.reject_sample_workload(w, num_requests=n)
+    dt = time.perf_counter() - t0
+    # each step a bounded sample sized so that the whole run stays within a few minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(min(w["B"], max(8, n * budget / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle.reject_sample_workload(w, num_requests=n)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.reject_sample_workload(w, num_requests=n)
+        times.append(time.perf_counter() - t0)
+    positions = int(w["cu_num_draft"][n])
+    value = positions / statistics.mean(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": meta,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"first {n} of {w['B']} requests per step ({positions} draft positions)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large-1024")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    from speculative_decoding_rejection_spec_gb300 import workloads as W
+    rank, world, local = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return  # the reference arm runs on rank 0 only
+    spec = W.CONFIGS[args.workload]
+    meta = {"workload": f"{args.workload}: B={spec['B']} K={spec['K']} V={spec['V']} {spec['dtype']} logits, "
+                        f"{'explicit fp32 draft probs' if spec['draft'] in ('noisy_q', 'target_q') else 'one-hot drafts'}"
+                        f", temperature {spec['temperature']}",
+            "B_per_gpu": spec["B"], "V": spec["V"], "logits_dtype": spec["dtype"],
+            "l2": "inputs larger than L2 (no flush)", "rng": "numpy PCG64, seeded"}
+    # each rank draws its own batch (independent requests: weak scaling, no data-path collective)
+    w = W.generate(args.workload, seed=spec["seed"] + 1000 * rank)
+    if args.impl == "reference":
+        run_reference(args, w, meta)
+        return
+
+    import torch
+    import __graft_entry__ as G
+    from speculative_decoding_rejection_spec_gb300 import binding
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    G.build()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    d = binding.to_device(w, dev)
+    has_q = d["draft_probs"] is not None
+    dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
+    buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, has_q, dev)
+    nk = binding.num_kernels(has_q)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        binding.sample(**d, buffers=buf)
+    st, bits, _ = binding.last_device_error(buf.workspace)
+    if st != 0:
+        raise SystemExit(f"device input error bits {bits}")
+
+    sampler = ClockSampler(dev.index or 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        binding.sample_profiled(d, buf, ev[i], stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    k1 = [row[0].elapsed_time(row[1]) for row in ev]
+    stage_ms = [statistics.mean(row[i].elapsed_time(row[i + 1]) for row in ev) for i in range(nk)]
+    positions = W.total_drafts(w)
+    value = positions * world / (ms / 1e3)
+
+    # roofline of the dominant kernel (row statistics: every target logit read once)
+    es = 2 if w["dtype"] == "bf16" else 4
+    k1_bytes = w["T"] * w["V"] * es + 4 * (w["T"] - w["B"])
+    k1_s = statistics.mean(k1) / 1e3
+    peak, peak_kind = peaks()
+    achieved = k1_bytes / k1_s / 1e9
+    tr = traffic_for(args.workload)
+    roofline = {"bound": "hbm", "kernel": "rowstats_kernel", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": None if tr is None else int(tr * w["T"]),
+                "algorithmic_bytes_per_launch": k1_bytes, "ms_per_launch": round(1e3 * k1_s, 4),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+    # whole-call algorithmic bytes (logits once + q rows at rejected positions + small vectors)
+    acc = buf.out_num_accepted.cpu().numpy()
+    ks = np.diff(w["cu_num_draft"])
+    rejecting = int(((acc >= 0) & (acc < ks)).sum()) if has_q else 0
+    call_bytes = (w["T"] * w["V"] * es + rejecting * w["V"] * 4 + 8 * (w["T"] - w["B"]) + 12 * w["T"]
+                  + 4 * (2 * w["B"] + 1))
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
+            "hbm_gbs_effective": round(call_bytes / (ms / 1e3) / 1e9, 1),
+            "stage_ms": [round(x, 4) for x in stage_ms], "rows_per_s": w["T"] * world / (ms / 1e3),
+            "roofline": roofline, "gpu_launches": nk * args.steps, "clocks": clocks}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(w, dev, args)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e(w, dev, args):
+    """Same metric through the host-buffer entry point: pinned host inputs copied to the
+    device, the sampler run, the outputs copied back, every step."""
+    import torch
+    from speculative_decoding_rejection_spec_gb300 import binding
+    has_q = w["draft_probs"] is not None
+    dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+        return t
+
+    host = {"logits": pinned(w["logits"]), "draft_ids": pinned(w["draft_ids"]),
+            "cu_num_draft": pinned(w["cu_num_draft"]), "uniforms": pinned(w["uniforms"]),
+            "temperature": pinned(w["temperature"])}
+    if has_q:
+        host["draft_probs"] = pinned(w["draft_probs"])
+    host["out_tokens"] = torch.empty(w["T"], dtype=torch.int32).pin_memory()
+    host["out_num_accepted"] = torch.empty(w["B"], dtype=torch.int32).pin_memory()
+    ptrs = {k: v.data_ptr() for k, v in host.items()}
+    arena = torch.empty(binding.host_arena_size(w["B"], w["T"], w["V"], dt, has_q), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena, stream)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena, stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / steps
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if not k.startswith("out_"))
+    d2h = 4 * (w["T"] + w["B"])
+    from speculative_decoding_rejection_spec_gb300 import workloads as W
+    return {"value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * spec_reject.h -- C ABI of the GB300 (sm_103a) verify-side rejection sampler
+ * for speculative decoding.
+ *
+ * What a call computes (speculative sampling, as defined in "第12章 投机解码：以小博大"
+ * §12.2.1-§12.2.4 and §12.3.2, with the flattened ragged layout of §12.3.5):
+ *
+ *   For request r with k_r = cu_num_draft[r+1] - cu_num_draft[r] drafts
+ *   (0 <= k_r <= 32, the MAX_SPEC_LEN of §12.5.4), its k_r + 1 target rows are
+ *   t_i = cu_num_draft[r] + r + i (i = 0..k_r) and its draft rows are
+ *   d_i = cu_num_draft[r] + i (i < k_r).
+ *     p_i = softmax(target_logits[t_i, :] / temperature[r])   (temperature on the target only)
+ *     q_i = draft_probs[d_i, :], or one-hot at draft_ids[d_i] when draft_probs == NULL
+ *   Sequentially over i: draft x* = draft_ids[d_i] is accepted iff
+ *     uniforms[t_i, 0] * q_i(x*) < p_i(x*)        (probability min(1, p/q))
+ *   and the scan stops at the first rejection j (later drafts are discarded).
+ *   At j < k_r the recovered token is drawn from max(0, p_j - q_j) (one-hot q:
+ *   p_j with x* removed); at j = k_r the bonus token is drawn from p_{k_r}.
+ *   The draw is an inverse CDF in ascending token order with u = uniforms[t_j, 1]:
+ *   the smallest v whose inclusive prefix mass exceeds u times the total.
+ *   temperature[r] <= 0 (or NaN) selects the greedy path: accept iff x* equals
+ *   the lowest-index argmax of the target row; the output at j is that argmax.
+ *
+ * Outputs: out_tokens[t_i] = x*_i for i < j, the sampled token at t_j, -1 after;
+ *          out_num_accepted[r] = j (accepted drafts, the sampled token excluded).
+ *
+ * Conventions of every entry point:
+ *   - Device pointers are device memory owned by the caller; host pointers are
+ *     host memory owned by the caller.  The library allocates nothing and keeps
+ *     no state between calls.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous on that stream unless stated otherwise.
+ *   - Errors the host can see (null pointers, bad sizes or strides, dtype,
+ *     workspace too small, misaligned pointers) return synchronously and launch
+ *     nothing.  Errors that depend on device data (cu_num_draft not starting at
+ *     0, not non-decreasing or not ending at T - B; k_r > 32; a draft id outside
+ *     [0, V)) are recorded in an error word inside the workspace, read with
+ *     spec_reject_last_device_error().  A request with such an error reports
+ *     out_num_accepted = -1 and -1 tokens; a batch whose cu_num_draft is
+ *     inconsistent as a whole reports -1 for every request and writes no tokens.
+ *     No kernel traps or asserts.
+ *   - Identical inputs give bit-identical outputs (no floating-point atomics).
+ */
+#ifndef SPEC_REJECT_H
+#define SPEC_REJECT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spec_status {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,  /* null pointer, bad size / stride / alignment */
+    SPEC_ERR_UNSUPPORTED = 2,  /* vocabulary too large for the chunk tables */
+    SPEC_ERR_WORKSPACE = 3,    /* workspace_bytes below spec_reject_workspace_size() */
+    SPEC_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    SPEC_ERR_DEVICE_INPUT = 5, /* device data was invalid (see the error word) */
+    SPEC_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up */
+} spec_status;
+
+typedef enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Largest vocabulary a call accepts. */
+#define SPEC_REJECT_MAX_VOCAB 1048576
+/* Largest number of drafts per request (MAX_SPEC_LEN). */
+#define SPEC_REJECT_MAX_SPEC_LEN 32
+
+/* Bits of the device error word (first int32 of spec_reject_last_device_error's report). */
+#define SPEC_DEVERR_LAYOUT 1     /* cu_num_draft[0] != 0, cu[B] + B != T, or cu decreasing */
+#define SPEC_DEVERR_SPEC_LEN 2   /* some k_r > 32 */
+#define SPEC_DEVERR_DRAFT_ID 4   /* some draft id outside [0, V) */
+
+/*
+ * Bytes of device workspace spec_reject_sample() needs for a batch of B
+ * requests, T target rows and vocabulary V.  Depends on the logits dtype
+ * (it sets the chunk length) and on whether explicit draft probabilities are
+ * given.  Any pointer alignment is accepted; the size includes slack for
+ * aligning internally.  Returns 0 for invalid sizes.
+ */
+size_t spec_reject_workspace_size(int32_t B, int64_t T, int32_t V, spec_dtype logits_dtype, int has_draft_probs);
+
+/*
+ * The batched rejection sampler (all steps on the GPU, asynchronous on `stream`).
+ *
+ *   target_logits     device, [T, V] rows `logits_row_stride` elements apart
+ *                     (stride >= V, or 0 = every row aliases row 0), fp32 or bf16
+ *                     per `logits_dtype`; element-aligned.  Rows whose start is
+ *                     16-byte aligned stream fastest.  -inf entries are masked
+ *                     tokens; NaN, +inf or an all -inf row give undefined tokens.
+ *   draft_probs       device fp32 [T - B, V] rows `q_row_stride` elements apart
+ *                     (>= V or 0), each row a distribution; or NULL for a
+ *                     deterministic (one-hot) draft.
+ *   draft_ids         device int32 [T - B] (may be NULL when T == B).
+ *   cu_num_draft      device int32 [B + 1]: 0, k_0, k_0 + k_1, ..., T - B.
+ *   uniforms          device fp32 [T, 2] in [0, 1): column 0 the acceptance
+ *                     coin of a verify row, column 1 the sampling draw used at
+ *                     the output row.  All randomness comes from here.
+ *   temperature       device fp32 [B]; <= 0 (or NaN) selects the greedy path.
+ *   out_tokens        device int32 [T].
+ *   out_num_accepted  device int32 [B].
+ *   workspace         device, at least spec_reject_workspace_size() bytes;
+ *                     contents need no initialisation and are overwritten.
+ */
+spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                               int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                               const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                               const float *uniforms, const float *temperature, int32_t *out_tokens,
+                               int32_t *out_num_accepted, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reads the device error word of the last call that used `workspace` (waits for
+ * `stream`).  Returns SPEC_OK when the device data was valid, else
+ * SPEC_ERR_DEVICE_INPUT with *error_bits (SPEC_DEVERR_* bits) and
+ * *first_bad_request (lowest offending request; -1 for a layout error) set.
+ * Either output pointer may be NULL.  SPEC_ERR_CUDA if the copy failed.
+ */
+spec_status spec_reject_last_device_error(const void *workspace, void *stream, int32_t *error_bits,
+                                          int32_t *first_bad_request);
+
+/*
+ * Host-buffer form of spec_reject_sample(): copies the host inputs into a
+ * caller-provided device arena, runs the sampler and copies out_tokens and
+ * out_num_accepted back.  Synchronous: returns after the host outputs are
+ * written (or on the first error).  Host pointers may be pageable or pinned;
+ * pinned memory copies fastest.  Rows are passed with the same strides as the
+ * device form (0 = aliasing is not allowed here: strides must be >= V).
+ * `device_arena` must hold spec_reject_host_arena_size() bytes.
+ */
+size_t spec_reject_host_arena_size(int32_t B, int64_t T, int32_t V, spec_dtype logits_dtype, int has_draft_probs);
+spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                    const float *draft_probs, const int32_t *draft_ids, const int32_t *cu_num_draft,
+                                    int32_t B, const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                    int32_t *out_num_accepted, void *device_arena, size_t arena_bytes,
+                                    void *stream);
+
+/*
+ * Diagnostic form: runs spec_reject_sample() and also writes, per target row,
+ * the row maximum m_t, the softmax normaliser s_t = sum_v exp((l - m_t) / T_r)
+ * (0 on greedy rows) and the lowest-index argmax; per draft row p_i(x*) (0 on
+ * greedy rows); and per request the normalised mass Z of the distribution the
+ * output token was drawn from (1 for a bonus draw, sum max(0, p - q) for an
+ * explicit-q recovery, 1 - p(x*) for a one-hot recovery, 0 on greedy rows).
+ * All debug outputs are device fp32 / int32 arrays; any may be NULL.  Slower
+ * than spec_reject_sample (an extra argmax pass); used to check probabilities.
+ */
+spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                       const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                       const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                       int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
+                                       void *stream, float *row_max, float *row_sum, int32_t *row_argmax,
+                                       float *p_draft, float *z_out);
+
+/*
+ * Measurement form of spec_reject_sample(): identical work, plus cudaEventRecord of
+ * caller-created events (cudaEvent_t handles) on `stream` between the kernels:
+ * stage_events[0] before the row-statistics pass, [1] after it, [2] after the
+ * per-request finalize, and with draft_probs [3] after the residual pass and [4]
+ * after the recovery pass.  Entries beyond num_events, or NULL entries, are skipped.
+ * The pages have no counterpart: this exists to time each kernel on its own stream.
+ */
+spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                        int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                        const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                        const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                        int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
+                                        void *stream, void *const *stage_events, int num_events);
+
+/* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 4 with). */
+int spec_reject_num_kernels(int has_draft_probs);
+
+/* Static description of a status code. */
+const char *spec_reject_status_string(spec_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int spec_reject_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_REJECT_H */

@@ -184,8 +184,8 @@ static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u, doubl
  *   dbg_z[B]          per request: normalised residual mass at the output row (1 for the
  *                     bonus, 0 for greedy)
  * Every dbg_* pointer may be NULL.  nthreads <= 0 uses the OpenMP default.
- * Returns 0, or 1 when the batch as a whole is inconsistent (cu[0] != 0 or cu[B] + B != T),
- * in which case every request is reported invalid.
+ * Returns 0, or 1 when the batch as a whole is inconsistent (cu[0] != 0, cu[B] + B != T or
+ * cu decreasing), in which case every request is reported invalid and no token is written.
  */
 int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_t V, int64_t logits_row_stride,
                          const float *draft_probs, int64_t q_row_stride, const int32_t *draft_ids,
@@ -196,7 +196,12 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
 {
     logit_rows L = {target_logits, dtype, T, V, logits_row_stride};
     const int64_t num_draft_rows = T - B;
+    /* The flattened layout itself is broken when cu does not start at 0, does not
+     * end at T - B, or decreases: then no request's rows are known. */
     int global_bad = (B < 0 || V < 1 || cu_num_draft[0] != 0 || (int64_t)cu_num_draft[B] + B != T);
+    for (int32_t req = 0; !global_bad && req < B; ++req)
+        if (cu_num_draft[req + 1] < cu_num_draft[req])
+            global_bad = 1;
 
 #ifdef _OPENMP
     if (nthreads > 0)
@@ -222,8 +227,9 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 if (draft_ids[db + i] < 0 || draft_ids[db + i] >= V)
                     bad = 1;
             if (bad) {
+                /* Too many drafts or a draft id outside [0, V): this request only. */
                 out_num_accepted[req] = -1;
-                if (!global_bad && k >= 0 && k <= ORACLE_MAX_SPEC_LEN && tb >= 0 && tb + k + 1 <= T)
+                if (!global_bad)
                     for (int64_t i = 0; i <= k; ++i)
                         out_tokens[tb + i] = -1;
                 if (out_flags)

@@ -1,0 +1,265 @@
+"""Thin ctypes binding of ``libspecreject.so`` (declared in ``include/spec_reject.h``).
+
+Argument marshalling only: every step of the sampler runs in the library's CUDA
+kernels.  Tensors must already live on the GPU (the ``*_host`` form takes host
+arrays and does its own copies inside the library).  There is no CPU fallback:
+if the library is missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libspecreject.so")
+
+F32, BF16 = 0, 1
+MAX_SPEC_LEN = 32
+DEVERR_LAYOUT, DEVERR_SPEC_LEN, DEVERR_DRAFT_ID = 1, 2, 4
+
+EXPORTED = [
+    "spec_reject_workspace_size", "spec_reject_sample", "spec_reject_last_device_error",
+    "spec_reject_host_arena_size", "spec_reject_sample_host", "spec_reject_debug_rowstats",
+    "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
+]
+
+_lib = None
+
+
+class SpecRejectError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY):
+        raise RuntimeError(f"{LIBRARY} is missing: build it with __graft_entry__.build() "
+                           "(the sampler has no CPU fallback)")
+    lib = ctypes.CDLL(LIBRARY)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.spec_reject_workspace_size.restype = sz
+    lib.spec_reject_workspace_size.argtypes = [i32, i64, i32, ctypes.c_int, ctypes.c_int]
+    sample_args = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, sz, P]
+    lib.spec_reject_sample.restype = ctypes.c_int
+    lib.spec_reject_sample.argtypes = sample_args
+    lib.spec_reject_debug_rowstats.restype = ctypes.c_int
+    lib.spec_reject_debug_rowstats.argtypes = sample_args + [P, P, P, P, P]
+    lib.spec_reject_last_device_error.restype = ctypes.c_int
+    lib.spec_reject_last_device_error.argtypes = [P, P, P, P]
+    lib.spec_reject_host_arena_size.restype = sz
+    lib.spec_reject_host_arena_size.argtypes = [i32, i64, i32, ctypes.c_int, ctypes.c_int]
+    lib.spec_reject_sample_host.restype = ctypes.c_int
+    lib.spec_reject_sample_host.argtypes = [P, ctypes.c_int, i64, i32, P, P, P, i32, P, P, P, P, P, sz, P]
+    lib.spec_reject_status_string.restype = ctypes.c_char_p
+    lib.spec_reject_status_string.argtypes = [ctypes.c_int]
+    lib.spec_reject_version.restype = ctypes.c_int
+    lib.spec_reject_sample_profiled.restype = ctypes.c_int
+    lib.spec_reject_sample_profiled.argtypes = sample_args + [P, ctypes.c_int]
+    lib.spec_reject_num_kernels.restype = ctypes.c_int
+    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().spec_reject_status_string(int(status)).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"target logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def workspace_size(B: int, T: int, V: int, dtype_code: int, has_draft_probs: bool) -> int:
+    n = load().spec_reject_workspace_size(int(B), int(T), int(V), int(dtype_code), int(bool(has_draft_probs)))
+    if n == 0:
+        raise ValueError("invalid sizes for spec_reject_workspace_size")
+    return int(n)
+
+
+def host_arena_size(B: int, T: int, V: int, dtype_code: int, has_draft_probs: bool) -> int:
+    n = load().spec_reject_host_arena_size(int(B), int(T), int(V), int(dtype_code), int(bool(has_draft_probs)))
+    if n == 0:
+        raise ValueError("invalid sizes for spec_reject_host_arena_size")
+    return int(n)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _row_stride(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit stride along the vocabulary")
+    return int(t.stride(0)) if t.shape[0] > 1 else int(t.shape[1])
+
+
+@dataclass
+class Buffers:
+    """Device buffers of one call, reusable across calls of the same shape."""
+    out_tokens: object
+    out_num_accepted: object
+    workspace: object
+
+
+def make_buffers(B: int, T: int, V: int, dtype_code: int, has_draft_probs: bool, device=None) -> Buffers:
+    import torch
+    dev = device if device is not None else torch.device("cuda")
+    return Buffers(out_tokens=torch.empty(T, dtype=torch.int32, device=dev),
+                   out_num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                   workspace=torch.empty(workspace_size(B, T, V, dtype_code, has_draft_probs), dtype=torch.uint8,
+                                         device=dev))
+
+
+def sample(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *,
+           buffers: Buffers | None = None, stream=None, debug: dict | None = None):
+    """Run the rejection sampler on device tensors; returns (out_tokens [T], out_num_accepted [B]).
+
+    target_logits: float32 / bfloat16 [T, V]; draft_probs: float32 [T - B, V] or None;
+    draft_ids int32 [T - B]; cu_num_draft int32 [B + 1]; uniforms float32 [T, 2];
+    temperature float32 [B].  With ``debug`` (a dict), the diagnostic entry point also
+    fills debug['row_max'], ['row_sum'], ['row_argmax'], ['p_draft'], ['z'] (device tensors).
+    """
+    import torch
+    lib = load()
+    T, V = int(target_logits.shape[0]), int(target_logits.shape[1])
+    B = int(cu_num_draft.shape[0]) - 1
+    dt = _dtype_code(target_logits)
+    if buffers is None:
+        buffers = make_buffers(B, T, V, dt, draft_probs is not None, target_logits.device)
+    for name, t, want in (("draft_ids", draft_ids, torch.int32), ("cu_num_draft", cu_num_draft, torch.int32),
+                          ("uniforms", uniforms, torch.float32), ("temperature", temperature, torch.float32)):
+        if t.dtype != want or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {want} tensor")
+    qs = 0
+    if draft_probs is not None:
+        if draft_probs.dtype != torch.float32:
+            raise TypeError("draft_probs must be float32")
+        qs = _row_stride(draft_probs)
+    args = [_ptr(target_logits), dt, T, V, _row_stride(target_logits), _ptr(draft_probs), qs, _ptr(draft_ids),
+            _ptr(cu_num_draft), B, _ptr(uniforms), _ptr(temperature), _ptr(buffers.out_tokens),
+            _ptr(buffers.out_num_accepted), _ptr(buffers.workspace), int(buffers.workspace.numel()),
+            _stream(stream)]
+    if debug is None:
+        st = lib.spec_reject_sample(*args)
+        what = "spec_reject_sample"
+    else:
+        dev = target_logits.device
+        debug.update(row_max=torch.full((T,), float("nan"), device=dev),
+                     row_sum=torch.full((T,), float("nan"), device=dev),
+                     row_argmax=torch.full((T,), -1, dtype=torch.int32, device=dev),
+                     p_draft=torch.full((max(T - B, 0),), float("nan"), device=dev),
+                     z=torch.full((B,), float("nan"), device=dev))
+        st = lib.spec_reject_debug_rowstats(*args, _ptr(debug["row_max"]), _ptr(debug["row_sum"]),
+                                            _ptr(debug["row_argmax"]), _ptr(debug["p_draft"]), _ptr(debug["z"]))
+        what = "spec_reject_debug_rowstats"
+    if st != 0:
+        raise SpecRejectError(st, what)
+    return buffers.out_tokens, buffers.out_num_accepted
+
+
+def sample_profiled(d: dict, buffers: Buffers, events: list, stream=None):
+    """``sample`` plus CUDA events recorded between the kernels (see spec_reject_sample_profiled).
+
+    ``events`` are torch.cuda.Event(enable_timing=True) objects that have been recorded once
+    (so that their handles exist).
+    """
+    lib = load()
+    t = d["target_logits"]
+    T, V = int(t.shape[0]), int(t.shape[1])
+    B = int(d["cu_num_draft"].shape[0]) - 1
+    q = d.get("draft_probs")
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    st = lib.spec_reject_sample_profiled(
+        _ptr(t), _dtype_code(t), T, V, _row_stride(t), _ptr(q), 0 if q is None else _row_stride(q),
+        _ptr(d["draft_ids"]), _ptr(d["cu_num_draft"]), B, _ptr(d["uniforms"]), _ptr(d["temperature"]),
+        _ptr(buffers.out_tokens), _ptr(buffers.out_num_accepted), _ptr(buffers.workspace),
+        int(buffers.workspace.numel()), _stream(stream), handles, len(events))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_sample_profiled")
+
+
+def num_kernels(has_draft_probs: bool) -> int:
+    return int(load().spec_reject_num_kernels(int(bool(has_draft_probs))))
+
+
+def last_device_error(workspace, stream=None):
+    """(status, error_bits, first_bad_request) of the last call that used ``workspace`` (synchronises)."""
+    bits = ctypes.c_int32(0)
+    first = ctypes.c_int32(0)
+    st = load().spec_reject_last_device_error(_ptr(workspace), _stream(stream), ctypes.byref(bits),
+                                              ctypes.byref(first))
+    if st not in (0, 5):
+        raise SpecRejectError(st, "spec_reject_last_device_error")
+    return int(st), int(bits.value), int(first.value)
+
+
+def sample_host(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.ndarray, uniforms: np.ndarray,
+                temperature: np.ndarray, draft_probs: np.ndarray | None, arena, *, out_tokens: np.ndarray | None = None,
+                out_num_accepted: np.ndarray | None = None, stream=None):
+    """Host-buffer entry point: host arrays in, host arrays out; copies happen inside the library.
+
+    ``logits`` is float32 or uint16 (bf16 bits) [T, V], C-contiguous (pinned memory copies fastest);
+    ``arena`` a device tensor of at least ``host_arena_size`` bytes.
+    """
+    T, V = logits.shape
+    B = cu_num_draft.shape[0] - 1
+    dt = BF16 if logits.dtype == np.uint16 else F32
+    for a in (logits, draft_ids, cu_num_draft, uniforms, temperature) + (() if draft_probs is None else (draft_probs,)):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("host arrays must be C-contiguous")
+    if out_tokens is None:
+        out_tokens = np.empty(T, np.int32)
+    if out_num_accepted is None:
+        out_num_accepted = np.empty(B, np.int32)
+    hp = lambda a: None if a is None else ctypes.c_void_p(a.ctypes.data)
+    st = load().spec_reject_sample_host(hp(logits), dt, T, V, hp(draft_probs), hp(draft_ids), hp(cu_num_draft), B,
+                                        hp(uniforms), hp(temperature), hp(out_tokens), hp(out_num_accepted),
+                                        _ptr(arena), int(arena.numel()), _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_sample_host")
+    return out_tokens, out_num_accepted
+
+
+def sample_host_ptrs(ptrs: dict, T: int, V: int, B: int, dtype_code: int, arena, stream=None):
+    """Same as ``sample_host`` but with raw host addresses (e.g. of pinned torch tensors)."""
+    st = load().spec_reject_sample_host(ptrs["logits"], dtype_code, T, V, ptrs.get("draft_probs"), ptrs["draft_ids"],
+                                        ptrs["cu_num_draft"], B, ptrs["uniforms"], ptrs["temperature"],
+                                        ptrs["out_tokens"], ptrs["out_num_accepted"], _ptr(arena),
+                                        int(arena.numel()), _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_sample_host")
+
+
+def to_device(w: dict, device="cuda"):
+    """Copy a synthetic workload (host numpy arrays) to device tensors for ``sample``."""
+    import torch
+    dev = torch.device(device)
+    if w["dtype"] == "bf16":
+        logits = torch.from_numpy(w["logits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        logits = torch.from_numpy(w["logits"]).to(dev)
+    q = None if w.get("draft_probs") is None else torch.from_numpy(w["draft_probs"]).to(dev)
+    return dict(target_logits=logits, draft_probs=q,
+                draft_ids=torch.from_numpy(w["draft_ids"]).to(dev),
+                cu_num_draft=torch.from_numpy(w["cu_num_draft"]).to(dev),
+                uniforms=torch.from_numpy(w["uniforms"]).to(dev),
+                temperature=torch.from_numpy(w["temperature"]).to(dev))

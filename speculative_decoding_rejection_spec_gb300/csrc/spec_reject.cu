@@ -1,0 +1,1454 @@
+// spec_reject.cu -- batched verify-side rejection sampler for speculative decoding,
+// hand-written for GB300 (sm_103a).  Implements the C ABI of include/spec_reject.h.
+//
+// The method (speculative sampling, "第12章 投机解码：以小博大" §12.2.1-§12.2.4, §12.3.2):
+// per request, accept draft x* with probability min(1, p/q) in order, stop at the first
+// rejection, draw the recovered token from max(0, p - q) there (one-hot q: p without x*,
+// §12.9), or the bonus token from p after the last draft; at temperature 0 compare with
+// the argmax instead.
+//
+// Structure on the GPU (all steps are kernels of this file; nothing runs on the host):
+//
+//   K1 rowstats   one streaming pass over every target row, split into 8 KB chunks
+//                 (4096 bf16 / 2048 fp32 logits).  Each warp owns a contiguous range of
+//                 (row, chunk) units and reduces each chunk to a partial:
+//                   sampling rows: (m_c, s_c) with m_c the chunk max and
+//                                  s_c = sum_v 2^(l_v * c - fl(m_c * c)), c = log2(e) / T_r,
+//                                  the draft token x* of a verify row left out;
+//                   greedy rows:   (max, lowest index of the max).
+//                 128-bit loads that do not allocate in L1, 8 in flight per lane.  Block 0
+//                 also validates the ragged layout and initialises the error word.
+//   K2 finalize   one warp per request.  Lane i combines the chunk partials of verify row i
+//                 (online max / rescaled sum), adds x* back, forms p(x*) and takes the
+//                 acceptance decision u * q(x*) < p(x*) (or x* == argmax); a ballot gives the
+//                 first rejection j.  For the bonus and one-hot recoveries it then locates
+//                 the output token: a warp scan over the chunk masses finds the chunk that
+//                 holds u * Z, a three-level warp descent (32 segments -> 32 sub-segments ->
+//                 one element) finds the token inside it.  Explicit-q recoveries are left to
+//                 K3 / K4.
+//   K3 residual   explicit q only: streams target row j and draft row j of each rejecting
+//                 request in chunks, reducing sum max(0, p - q) per chunk.
+//   K4 recover    explicit q only: one warp per rejecting request locates the recovered
+//                 token from K3's chunk masses, as K2 does.
+//
+// Every reduction has a fixed order (warp butterflies, sequential chunk combines), so
+// identical inputs give identical outputs; there are no floating-point atomics.  No kernel
+// waits on another block, so nothing can hang.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <limits.h>
+#include <math.h>
+
+#include "spec_reject.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnitBytes = 8192;  // bytes of logits per (row, chunk) unit
+constexpr int kUnroll = 8;        // 16-byte vectors in flight per lane
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Layout of the workspace (all offsets 256-byte aligned).  The error word comes first so
+// that spec_reject_last_device_error() finds it without knowing the call's sizes.
+struct Plan {
+    int chunk;    // logits per chunk
+    int nchunks;  // chunks per row
+    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool make_plan(int32_t B, int64_t T, int32_t V, spec_dtype dt, int has_q, Plan *pl)
+{
+    if (B < 0 || T < 0 || V < 1 || V > SPEC_REJECT_MAX_VOCAB || (dt != SPEC_F32 && dt != SPEC_BF16))
+        return false;
+    const int es = dt == SPEC_BF16 ? 2 : 4;
+    pl->chunk = kUnitBytes / es;
+    pl->nchunks = (V + pl->chunk - 1) / pl->chunk;
+    size_t o = 0;
+    pl->off_err = o;
+    o = align256(o + 4 * sizeof(int32_t));
+    pl->off_part = o;
+    o = align256(o + sizeof(float2) * (size_t)T * (size_t)pl->nchunks);
+    pl->off_rstate = o;
+    o = align256(o + sizeof(int32_t) * (size_t)(B + 1));
+    pl->off_rstat = o;
+    o = align256(o + sizeof(float2) * (size_t)(B + 1));
+    pl->off_rpart = o;
+    o = align256(o + (has_q ? sizeof(float) * (size_t)B * (size_t)pl->nchunks : 0));
+    pl->total = o + 256;  // slack for aligning the caller's pointer
+    return true;
+}
+
+struct Params {
+    const void *logits;
+    int64_t T;
+    int32_t V;
+    int64_t lstride;  // elements
+    const float *q;
+    int64_t qstride;  // elements
+    const int32_t *ids;
+    const int32_t *cu;
+    int32_t B;
+    const float *uni;
+    const float *temp;
+    int32_t *out_tokens;
+    int32_t *out_acc;
+    // workspace
+    float2 *part;     // [T * nchunks] chunk partials
+    int32_t *err;     // [0] SPEC_DEVERR_* bits, [1] first bad request (INT_MAX = none)
+    int32_t *rstate;  // [B] output position j of a pending explicit-q recovery, else -1
+    float2 *rstat;    // [B] (M, S) of that output row
+    float *rpart;     // [B * nchunks] residual chunk masses
+    int chunk, nchunks;
+    // diagnostics (all may be null)
+    float *dbg_pdraft;
+    float *dbg_z;
+};
+
+// ---------------------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------------------
+
+template <int DT> struct Elem;
+template <> struct Elem<0> {  // fp32
+    static constexpr int kVec = 4;
+    static constexpr int kSize = 4;
+};
+template <> struct Elem<1> {  // bf16
+    static constexpr int kVec = 8;
+    static constexpr int kSize = 2;
+};
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Streaming 16-byte load through the non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <int DT> __device__ __forceinline__ void unpack(const uint4 &w, float *x);
+template <> __device__ __forceinline__ void unpack<0>(const uint4 &w, float *x)
+{
+    x[0] = __uint_as_float(w.x);
+    x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z);
+    x[3] = __uint_as_float(w.w);
+}
+template <> __device__ __forceinline__ void unpack<1>(const uint4 &w, float *x)
+{
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xffff0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xffff0000u);
+    x[4] = __uint_as_float(w.z << 16);
+    x[5] = __uint_as_float(w.z & 0xffff0000u);
+    x[6] = __uint_as_float(w.w << 16);
+    x[7] = __uint_as_float(w.w & 0xffff0000u);
+}
+
+// A 16-byte vector with element `rel` replaced by -inf (fp32 0xff800000, bf16 0xff80).
+template <int DT> __device__ __forceinline__ uint4 mask_elem(uint4 w, int rel);
+template <> __device__ __forceinline__ uint4 mask_elem<0>(uint4 w, int rel)
+{
+    w.x = rel == 0 ? 0xff800000u : w.x;
+    w.y = rel == 1 ? 0xff800000u : w.y;
+    w.z = rel == 2 ? 0xff800000u : w.z;
+    w.w = rel == 3 ? 0xff800000u : w.w;
+    return w;
+}
+template <> __device__ __forceinline__ uint4 mask_elem<1>(uint4 w, int rel)
+{
+    const uint32_t lo = 0x0000ff80u, hi = 0xff800000u;
+    w.x = rel == 0 ? (w.x & 0xffff0000u) | lo : rel == 1 ? (w.x & 0x0000ffffu) | hi : w.x;
+    w.y = rel == 2 ? (w.y & 0xffff0000u) | lo : rel == 3 ? (w.y & 0x0000ffffu) | hi : w.y;
+    w.z = rel == 4 ? (w.z & 0xffff0000u) | lo : rel == 5 ? (w.z & 0x0000ffffu) | hi : w.z;
+    w.w = rel == 6 ? (w.w & 0xffff0000u) | lo : rel == 7 ? (w.w & 0x0000ffffu) | hi : w.w;
+    return w;
+}
+
+template <int DT> __device__ __forceinline__ uint4 neg_inf_vec();
+template <> __device__ __forceinline__ uint4 neg_inf_vec<0>() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+template <> __device__ __forceinline__ uint4 neg_inf_vec<1>() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+
+template <int DT> __device__ __forceinline__ float load1(const char *row, int64_t v);
+template <> __device__ __forceinline__ float load1<0>(const char *row, int64_t v)
+{
+    return __ldg(reinterpret_cast<const float *>(row) + v);
+}
+template <> __device__ __forceinline__ float load1<1>(const char *row, int64_t v)
+{
+    const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(row) + v);
+    return __uint_as_float(uint32_t(b) << 16);
+}
+
+template <int DT> __device__ __forceinline__ const char *row_ptr(const Params &P, int64_t t)
+{
+    return reinterpret_cast<const char *>(P.logits) + t * P.lstride * Elem<DT>::kSize;
+}
+
+// ---------------------------------------------------------------------------------------
+// Warp reductions (fixed butterfly order: deterministic)
+// ---------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Inclusive prefix sum over lanes (Kogge-Stone, fixed order).
+__device__ __forceinline__ float warp_incl_scan(float v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += n;
+    }
+    return v;
+}
+
+// Largest value, lowest index on ties.
+__device__ __forceinline__ void warp_argmax(float &best, int &idx)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float b2 = __shfl_xor_sync(kFull, best, o);
+        const int i2 = __shfl_xor_sync(kFull, idx, o);
+        if (b2 > best || (b2 == best && i2 < idx)) {
+            best = b2;
+            idx = i2;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K1: row statistics
+// ---------------------------------------------------------------------------------------
+
+// Running softmax statistics of one lane: max m (raw logit), reference M = fl(m * c) and
+// s = sum 2^(l * c - M).
+struct SoftAcc {
+    float m = -INFINITY, M = -INFINITY, s = 0.f;
+    __device__ __forceinline__ void rebase(float bm, float c)
+    {
+        if (bm > m) {
+            const float Mn = bm * c;
+            s = (m == -INFINITY) ? 0.f : s * ex2(M - Mn);
+            m = bm;
+            M = Mn;
+        }
+    }
+};
+
+struct ArgAcc {
+    float best = -INFINITY;
+    int idx = INT_MAX;
+    __device__ __forceinline__ void add(float x, int v)
+    {
+        if (x > best) {
+            best = x;
+            idx = v;
+        }
+    }
+};
+
+// Block 0 of K1: check the ragged layout, initialise the error word.
+__device__ void validate_layout(const Params &P)
+{
+    __shared__ int s_first;
+    if (threadIdx.x == 0)
+        s_first = INT_MAX;
+    __syncthreads();
+    int layout_bad = 0, len_bad = 0;
+    for (int r = threadIdx.x; r < P.B; r += blockDim.x) {
+        const int k = P.cu[r + 1] - P.cu[r];
+        if (k < 0)
+            layout_bad = 1;
+        if (k > SPEC_REJECT_MAX_SPEC_LEN) {
+            len_bad = 1;
+            atomicMin(&s_first, r);
+        }
+    }
+    if (threadIdx.x == 0 && (P.cu[0] != 0 || (int64_t)P.cu[P.B] + P.B != P.T))
+        layout_bad = 1;
+    layout_bad = __syncthreads_or(layout_bad);
+    len_bad = __syncthreads_or(len_bad);
+    if (threadIdx.x == 0) {
+        P.err[0] = (layout_bad ? SPEC_DEVERR_LAYOUT : 0) | (len_bad ? SPEC_DEVERR_SPEC_LEN : 0);
+        P.err[1] = layout_bad ? -1 : s_first;
+    }
+}
+
+// Request that owns target row t (rows are request-major; cu[r] + r is increasing for a
+// valid layout; for an invalid one any in-range answer is fine, K2 reports the error).
+__device__ __forceinline__ int find_request(const Params &P, int64_t t)
+{
+    int lo = 0, hi = P.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)__ldg(P.cu + mid) + mid <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Bounds of one (row, chunk) unit: 16-byte aligned body [vlo, vlo + nvec * VEC) and
+// scalar head [lo, vlo) and tail [vhi, hi), each shorter than one vector.
+struct UnitRange {
+    int64_t lo, hi, vlo, nvec, vhi;
+};
+
+template <int DT> __device__ __forceinline__ UnitRange unit_range(const Params &P, const char *row, int c)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    constexpr int ES = Elem<DT>::kSize;
+    UnitRange R;
+    R.lo = (int64_t)c * P.chunk;
+    R.hi = min((int64_t)P.V, R.lo + P.chunk);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row + R.lo * ES);
+    R.vlo = min(R.hi, R.lo + (int64_t)(((16 - (a & 15)) & 15) / ES));
+    R.nvec = (R.hi - R.vlo) / VEC;
+    R.vhi = R.vlo + R.nvec * VEC;
+    return R;
+}
+
+// Largest of the elements of a vector (bf16: packed max on the raw pairs).
+template <int DT> __device__ __forceinline__ float vec_max(const uint4 &w);
+template <> __device__ __forceinline__ float vec_max<0>(const uint4 &w)
+{
+    return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+template <> __device__ __forceinline__ float vec_max<1>(const uint4 &w)
+{
+    uint32_t a, b, m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(w.x), "r"(w.y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(w.z), "r"(w.w));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+}
+
+template <int DT>
+__device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, float cs, int xs, int lane);
+template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int64_t t, int c, int lane);
+
+template <int DT>
+__device__ __forceinline__ void rowstats_unit(const Params &P, int64_t t, int c, bool greedy, float cs, int xs,
+                                              int lane)
+{
+    if (greedy)
+        argmax_unit<DT>(P, t, c, lane);
+    else
+        softmax_unit<DT>(P, t, c, cs, xs, lane);
+}
+
+template <int DT>
+__device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, float cs, int xs, int lane)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    constexpr int ES = Elem<DT>::kSize;
+    const char *row = row_ptr<DT>(P, t);
+    const UnitRange R = unit_range<DT>(P, row, c);
+    const int64_t lo = R.lo, hi = R.hi, vlo = R.vlo, nvec = R.nvec, vhi = R.vhi;
+    const char *vbase = row + vlo * ES;
+    {
+        SoftAcc acc;
+        float sacc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            sacc[e] = 0.f;
+        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * kUnroll) {
+            uint4 raw[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t vi = b0 + u * 32 + lane;
+                if (vi < nvec) {
+                    raw[u] = ld_stream(vbase + vi * 16);
+                    const int rel = xs - (int)(vlo + vi * VEC);
+                    if ((unsigned)rel < (unsigned)VEC)  // the draft token: leave it out
+                        raw[u] = mask_elem<DT>(raw[u], rel);
+                } else {
+                    raw[u] = neg_inf_vec<DT>();
+                }
+            }
+            float bm = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                bm = fmaxf(bm, vec_max<DT>(raw[u]));
+            if (bm > acc.m) {
+                // fold the per-slot sums into the lane sum before moving the reference
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    s += sacc[e];
+                    sacc[e] = 0.f;
+                }
+                acc.s += s;
+                acc.rebase(bm, cs);
+            }
+            if (acc.m > -INFINITY) {  // nothing but -inf so far: no mass, and M is not finite
+                const float M = acc.M;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    float x[VEC];
+                    unpack<DT>(raw[u], x);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        sacc[e] += ex2(fmaf(x[e], cs, -M));
+                }
+            }
+        }
+        {
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                s += sacc[e];
+            acc.s += s;
+        }
+        // scalar head and tail (fewer than VEC elements each)
+        float xh = -INFINITY, xt = -INFINITY;
+        if (lane < vlo - lo) {
+            const int64_t v = lo + lane;
+            xh = (v == xs) ? -INFINITY : load1<DT>(row, v);
+        }
+        if (lane < hi - vhi) {
+            const int64_t v = vhi + lane;
+            xt = (v == xs) ? -INFINITY : load1<DT>(row, v);
+        }
+        const float bm = fmaxf(xh, xt);
+        if (bm > -INFINITY) {
+            acc.rebase(bm, cs);
+            acc.s += ex2(fmaf(xh, cs, -acc.M)) + ex2(fmaf(xt, cs, -acc.M));
+        }
+        // warp combine
+        const float mw = warp_max(acc.m);
+        const float Mw = mw * cs;
+        const float sl = (acc.m == -INFINITY) ? 0.f : acc.s * ex2(acc.M - Mw);
+        const float sw = warp_sum(sl);
+        if (lane == 0)
+            P.part[t * P.nchunks + c] = make_float2(mw, mw == -INFINITY ? 0.f : sw);
+    }
+}
+
+template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int64_t t, int c, int lane)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    constexpr int ES = Elem<DT>::kSize;
+    const char *row = row_ptr<DT>(P, t);
+    const UnitRange R = unit_range<DT>(P, row, c);
+    const int64_t lo = R.lo, hi = R.hi, vlo = R.vlo, nvec = R.nvec, vhi = R.vhi;
+    const char *vbase = row + vlo * ES;
+    {
+        ArgAcc acc;
+        if (lane < vlo - lo)
+            acc.add(load1<DT>(row, lo + lane), (int)(lo + lane));
+        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * kUnroll) {
+            uint4 raw[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t vi = b0 + u * 32 + lane;
+                if (vi < nvec)
+                    raw[u] = ld_stream(vbase + vi * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t vi = b0 + u * 32 + lane;
+                if (vi < nvec) {
+                    float x[VEC];
+                    unpack<DT>(raw[u], x);
+                    const int v0 = (int)(vlo + vi * VEC);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        acc.add(x[e], v0 + e);
+                }
+            }
+        }
+        if (lane < hi - vhi)
+            acc.add(load1<DT>(row, vhi + lane), (int)(vhi + lane));
+        warp_argmax(acc.best, acc.idx);
+        if (lane == 0)
+            P.part[t * P.nchunks + c] = make_float2(acc.best, __int_as_float(acc.idx));
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) rowstats_kernel(Params P, int force_argmax)
+{
+    if (blockIdx.x == 0)
+        validate_layout(P);
+    if (P.B == 0)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int64_t nunits = P.T * (int64_t)P.nchunks;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t per = (nunits + nw - 1) / nw;
+    const int64_t u0 = gw * per;
+    const int64_t u1 = min(nunits, u0 + per);
+    int64_t cached_t = -1;
+    bool greedy = true;
+    float cs = 0.f;
+    int xs = -1;
+    for (int64_t u = u0; u < u1; ++u) {
+        const int64_t t = u / P.nchunks;
+        const int c = (int)(u - t * P.nchunks);
+        if (t != cached_t) {
+            cached_t = t;
+            const int r = find_request(P, t);
+            const int64_t i = t - ((int64_t)__ldg(P.cu + r) + r);
+            const int k = __ldg(P.cu + r + 1) - __ldg(P.cu + r);
+            const int64_t d = t - r;
+            const float temp = __ldg(P.temp + r);
+            greedy = force_argmax || !(temp > 0.f);
+            cs = greedy ? 0.f : kLog2e / temp;
+            xs = (!greedy && i >= 0 && i < k && d >= 0 && d < P.T - P.B) ? __ldg(P.ids + d) : -1;
+        }
+        rowstats_unit<DT>(P, t, c, greedy, cs, xs, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Chunk combines (used by K2 / K4)
+// ---------------------------------------------------------------------------------------
+
+// Sequential combine of one row's softmax partials by a single lane: M = max fl(m_c * c),
+// S = sum s_c 2^(fl(m_c * c) - M).
+__device__ __forceinline__ void lane_combine_soft(const Params &P, int64_t t, float cs, float &M, float &S)
+{
+    M = -INFINITY;
+    S = 0.f;
+    const float2 *pp = P.part + t * P.nchunks;
+    for (int c = 0; c < P.nchunks; ++c) {
+        const float2 pc = pp[c];
+        if (pc.x == -INFINITY)
+            continue;
+        const float Mc = pc.x * cs;
+        if (Mc > M) {
+            S = (M == -INFINITY) ? pc.y : S * ex2(M - Mc) + pc.y;
+            M = Mc;
+        } else {
+            S += pc.y * ex2(Mc - M);
+        }
+    }
+}
+
+__device__ __forceinline__ int lane_combine_argmax(const Params &P, int64_t t, float *best_out)
+{
+    float best = -INFINITY;
+    int idx = INT_MAX;
+    const float2 *pp = P.part + t * P.nchunks;
+    for (int c = 0; c < P.nchunks; ++c) {
+        const float2 pc = pp[c];
+        const int i = __float_as_int(pc.y);
+        if (pc.x > best || (pc.x == best && i < idx)) {
+            best = pc.x;
+            idx = i;
+        }
+    }
+    if (best_out)
+        *best_out = best;
+    return idx == INT_MAX ? 0 : idx;
+}
+
+// Warp combine of one row's softmax partials (lanes over chunks).
+__device__ __forceinline__ void warp_combine_soft(const Params &P, int64_t t, float cs, int lane, float &M, float &S)
+{
+    const float2 *pp = P.part + t * P.nchunks;
+    float m = -INFINITY;
+    for (int c = lane; c < P.nchunks; c += 32) {
+        const float x = pp[c].x;
+        m = fmaxf(m, x);
+    }
+    m = warp_max(m);
+    M = m * cs;
+    float s = 0.f;
+    if (m > -INFINITY) {
+        for (int c = lane; c < P.nchunks; c += 32) {
+            const float2 pc = pp[c];
+            if (pc.x != -INFINITY)
+                s += pc.y * ex2(pc.x * cs - M);
+        }
+    }
+    S = warp_sum(s);
+}
+
+__device__ __forceinline__ int warp_combine_argmax(const Params &P, int64_t t, int lane)
+{
+    const float2 *pp = P.part + t * P.nchunks;
+    float best = -INFINITY;
+    int idx = INT_MAX;
+    for (int c = lane; c < P.nchunks; c += 32) {
+        const float2 pc = pp[c];
+        const int i = __float_as_int(pc.y);
+        if (pc.x > best || (pc.x == best && i < idx)) {
+            best = pc.x;
+            idx = i;
+        }
+    }
+    warp_argmax(best, idx);
+    return idx == INT_MAX ? 0 : idx;
+}
+
+// ---------------------------------------------------------------------------------------
+// Inverse-CDF locate: chunk scan + three-level warp descent inside the chunk
+// ---------------------------------------------------------------------------------------
+
+// Mass of the target distribution in units of 2^M: w(v) = 2^(l_v c - M), x* optionally left out.
+template <int DT> struct TargetMass {
+    const char *row;
+    float cs, M;
+    int64_t excl;
+    __device__ __forceinline__ float one(int64_t v) const
+    {
+        return v == excl ? 0.f : ex2(fmaf(load1<DT>(row, v), cs, -M));
+    }
+    // Sum of masses of elements [v0, v1); vector loads where the row is 16-byte aligned.
+    __device__ __forceinline__ float range(int64_t v0, int64_t v1) const
+    {
+        constexpr int VEC = Elem<DT>::kVec;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t v = v0;
+        const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0);
+        if (aligned) {
+            for (; v + VEC <= v1; v += VEC) {
+                float x[VEC];
+                unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e)
+                    s[e & 3] += (v + e == excl) ? 0.f : ex2(fmaf(x[e], cs, -M));
+            }
+        }
+        for (; v < v1; ++v)
+            s[v & 3] += one(v);
+        return (s[0] + s[1]) + (s[2] + s[3]);
+    }
+};
+
+// Explicit-q residual mass r(v) = max(0, 2^(l_v c - M) / S - q(v)) in probability units.
+template <int DT> struct ResidualMass {
+    const char *row;
+    const float *qrow;
+    float cs, M, inv_s;
+    __device__ __forceinline__ float one(int64_t v) const
+    {
+        return fmaxf(0.f, ex2(fmaf(load1<DT>(row, v), cs, -M)) * inv_s - __ldg(qrow + v));
+    }
+    __device__ __forceinline__ float range(int64_t v0, int64_t v1) const
+    {
+        constexpr int VEC = Elem<DT>::kVec;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t v = v0;
+        const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0) &&
+                             ((reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0);
+        if (aligned) {
+            for (; v + VEC <= v1; v += VEC) {
+                float x[VEC];
+                unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
+#pragma unroll
+                for (int h = 0; h < VEC / 4; ++h) {
+                    const float4 q4 = __ldg(reinterpret_cast<const float4 *>(qrow + v) + h);
+                    s[0] += fmaxf(0.f, ex2(fmaf(x[4 * h + 0], cs, -M)) * inv_s - q4.x);
+                    s[1] += fmaxf(0.f, ex2(fmaf(x[4 * h + 1], cs, -M)) * inv_s - q4.y);
+                    s[2] += fmaxf(0.f, ex2(fmaf(x[4 * h + 2], cs, -M)) * inv_s - q4.z);
+                    s[3] += fmaxf(0.f, ex2(fmaf(x[4 * h + 3], cs, -M)) * inv_s - q4.w);
+                }
+            }
+        }
+        for (; v < v1; ++v)
+            s[v & 3] += one(v);
+        return (s[0] + s[1]) + (s[2] + s[3]);
+    }
+};
+
+// Smallest v in [lo, hi) whose inclusive prefix mass exceeds theta (masses given by F).
+// Three levels: 32 lane segments, 32 sub-segments of the chosen segment, then the
+// elements of the chosen sub-segment in order.  When rounding leaves theta beyond the
+// range's total, returns the last element with positive mass (or hi - 1).
+template <class F>
+__device__ int64_t warp_find(const F &f, int64_t lo, int64_t hi, float theta, int lane)
+{
+    for (int level = 0; level < 2; ++level) {
+        const int64_t n = hi - lo;
+        if (n <= 32)
+            break;
+        int64_t seg = (n + 31) / 32;
+        if (level == 0)
+            seg = (seg + 7) & ~int64_t(7);  // keep segment starts vector aligned
+        const int64_t s0 = min(hi, lo + lane * seg), s1 = min(hi, s0 + seg);
+        const float tot = f.range(s0, s1);
+        const float incl = warp_incl_scan(tot, lane);
+        const unsigned hit = __ballot_sync(kFull, incl > theta);
+        int L;
+        if (hit) {
+            L = __ffs(hit) - 1;
+        } else {
+            const unsigned pos = __ballot_sync(kFull, tot > 0.f);
+            if (!pos)
+                return hi - 1;
+            L = 31 - __clz(pos);
+            theta = INFINITY;  // take the last positive element of that segment
+        }
+        const float excl = __shfl_sync(kFull, incl - tot, L);
+        if (theta != INFINITY)
+            theta -= excl;
+        lo = min(hi, lo + L * seg);
+        hi = min(hi, lo + seg);
+    }
+    // final level: at most 32 elements, one per lane
+    const int64_t v = lo + lane;
+    const float w = (v < hi) ? f.one(v) : 0.f;
+    const float incl = warp_incl_scan(w, lane);
+    const unsigned hit = __ballot_sync(kFull, v < hi && incl > theta);
+    if (hit)
+        return lo + (__ffs(hit) - 1);
+    const unsigned pos = __ballot_sync(kFull, w > 0.f);
+    return pos ? lo + (31 - __clz(pos)) : hi - 1;
+}
+
+// Masses of the chunks of row t relative to 2^M (K1 partials), with an optional extra
+// mass added to one chunk (x* back in when sampling p itself on a verify row).
+struct ChunkMassFromPartials {
+    const float2 *pp;
+    float cs, M;
+    int extra_chunk;
+    float extra;
+    __device__ __forceinline__ float operator()(int c) const
+    {
+        const float2 pc = pp[c];
+        float m = (pc.x == -INFINITY) ? 0.f : pc.y * ex2(pc.x * cs - M);
+        return c == extra_chunk ? m + extra : m;
+    }
+};
+
+struct ChunkMassFromArray {
+    const float *z;
+    __device__ __forceinline__ float operator()(int c) const { return z[c]; }
+};
+
+// Warp scan over the chunk masses: total Z, then the chunk holding u * Z and the
+// remaining threshold inside it.  Both passes use the same scan, so they agree bit for bit.
+template <class CM>
+__device__ __forceinline__ float chunk_total(const CM &cm, int nchunks, int lane)
+{
+    float carry = 0.f;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        const float m = (c0 + lane < nchunks) ? cm(c0 + lane) : 0.f;
+        const float incl = warp_incl_scan(m, lane);
+        carry += __shfl_sync(kFull, incl, 31);
+    }
+    return carry;
+}
+
+template <class CM>
+__device__ __forceinline__ int chunk_locate(const CM &cm, int nchunks, float theta, int lane, float &theta_in)
+{
+    float carry = 0.f;
+    int last_pos = -1;
+    float last_mass = 0.f;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        const float m = (c0 + lane < nchunks) ? cm(c0 + lane) : 0.f;
+        const float incl = warp_incl_scan(m, lane) + carry;
+        const unsigned hit = __ballot_sync(kFull, incl > theta);
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            theta_in = theta - __shfl_sync(kFull, incl - m, L);
+            return c0 + L;
+        }
+        const unsigned pos = __ballot_sync(kFull, m > 0.f);
+        if (pos) {
+            const int L = 31 - __clz(pos);
+            last_pos = c0 + L;
+            last_mass = __shfl_sync(kFull, m, L);
+        }
+        carry = __shfl_sync(kFull, incl, 31);
+    }
+    // rounding left theta at or beyond the total: last chunk with mass, its last element
+    theta_in = INFINITY;
+    (void)last_mass;
+    return last_pos < 0 ? nchunks - 1 : last_pos;
+}
+
+// ---------------------------------------------------------------------------------------
+// K2: per-request finalize
+// ---------------------------------------------------------------------------------------
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
+{
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (r >= P.B)
+        return;
+    const int errbits = P.err[0];
+    if (errbits & SPEC_DEVERR_LAYOUT) {
+        if (lane == 0) {
+            P.out_acc[r] = -1;
+            if (P.rstate)
+                P.rstate[r] = -1;
+            if (P.dbg_z)
+                P.dbg_z[r] = 0.f;
+        }
+        return;
+    }
+    const int cu0 = P.cu[r];
+    const int k = P.cu[r + 1] - cu0;
+    const int64_t tb = (int64_t)cu0 + r;
+    const int64_t db = cu0;
+    const bool too_long = k > SPEC_REJECT_MAX_SPEC_LEN;
+    int xs = -1;
+    if (!too_long && lane < k)
+        xs = P.ids[db + lane];
+    const unsigned badid = __ballot_sync(kFull, !too_long && lane < k && (xs < 0 || xs >= P.V));
+    if (too_long || badid) {
+        for (int64_t i = lane; i <= k; i += 32)
+            P.out_tokens[tb + i] = -1;
+        if (lane == 0) {
+            P.out_acc[r] = -1;
+            if (P.rstate)
+                P.rstate[r] = -1;
+            if (P.dbg_z)
+                P.dbg_z[r] = 0.f;
+            atomicOr(P.err, too_long ? SPEC_DEVERR_SPEC_LEN : SPEC_DEVERR_DRAFT_ID);
+            atomicMin(P.err + 1, r);
+        }
+        return;
+    }
+
+    const float temp = P.temp[r];
+    const bool greedy = !(temp > 0.f);
+    const float cs = greedy ? 0.f : kLog2e / temp;
+
+    // Acceptance decision of draft row `lane`.
+    bool accept = true;
+    int am = 0;
+    float Mi = -INFINITY, Si = 0.f, wstar = 0.f;
+    if (lane < k) {
+        const int64_t t = tb + lane;
+        if (greedy) {
+            am = lane_combine_argmax(P, t, nullptr);
+            accept = (xs == am);
+        } else {
+            lane_combine_soft(P, t, cs, Mi, Si);
+            const float ls = load1<DT>(row_ptr<DT>(P, t), xs);
+            const float ys = ls * cs;
+            if (ys > Mi) {
+                Si = (Mi == -INFINITY) ? 0.f : Si * ex2(Mi - ys);
+                Mi = ys;
+            }
+            const float e = fmaf(ls, cs, -Mi);
+            wstar = ex2(e);
+            Si += wstar;
+            const float qs = P.q ? __ldg(P.q + (db + lane) * P.qstride + xs) : 1.f;
+            const float us = P.uni[2 * t];
+            const double lhs = (double)us * (double)qs;  // exact
+            const float ps = wstar / Si;
+            if (ps > 1e-30f)
+                accept = lhs < (double)ps;
+            else  // below fp32's normal range: form p(x*) in double
+                accept = lhs < exp2((double)e) / (double)Si;
+            if (P.dbg_pdraft)
+                P.dbg_pdraft[db + lane] = ps;
+        }
+    }
+    const unsigned rej = __ballot_sync(kFull, lane < k && !accept);
+    const int j = rej ? __ffs(rej) - 1 : k;
+    const int64_t tj = tb + j;
+
+    int token = -1;
+    bool pending = false;
+    float zdbg = 0.f;
+    if (greedy) {
+        token = (j < k) ? __shfl_sync(kFull, am, j) : warp_combine_argmax(P, tj, lane);
+    } else {
+        const float us = P.uni[2 * tj + 1];
+        const char *row = row_ptr<DT>(P, tj);
+        if (j == k) {  // bonus: draw from p
+            float M, S;
+            warp_combine_soft(P, tj, cs, lane, M, S);
+            ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, M, -1, 0.f};
+            const float Z = chunk_total(cm, P.nchunks, lane);
+            float th;
+            const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
+            TargetMass<DT> f{row, cs, M, -1};
+            token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
+            zdbg = 1.f;
+        } else {
+            const float Mj = __shfl_sync(kFull, Mi, j);
+            const float Sj = __shfl_sync(kFull, Si, j);
+            const int xj = __shfl_sync(kFull, xs, j);
+            if (!P.q) {  // one-hot draft: residual = p without x*
+                const float wj = __shfl_sync(kFull, wstar, j);
+                ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, Mj, -1, 0.f};
+                float Z = chunk_total(cm, P.nchunks, lane);
+                int64_t excl = xj;
+                if (!(Z > 0.f)) {  // empty residual: draw from p itself
+                    cm.extra_chunk = xj / P.chunk;
+                    cm.extra = wj;
+                    Z = chunk_total(cm, P.nchunks, lane);
+                    excl = -1;
+                } else {
+                    zdbg = Z / Sj;
+                }
+                float th;
+                const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
+                TargetMass<DT> f{row, cs, Mj, excl};
+                token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
+                                       lane);
+            } else {  // explicit q: K3 / K4 finish this request
+                pending = true;
+                if (lane == 0)
+                    P.rstat[r] = make_float2(Mj, Sj);
+            }
+        }
+    }
+    if (lane == 0) {
+        P.out_acc[r] = j;
+        if (P.rstate)
+            P.rstate[r] = pending ? j : -1;
+        if (P.dbg_z && !pending)
+            P.dbg_z[r] = zdbg;
+    }
+    for (int i = lane; i <= k; i += 32) {
+        if (i == j && pending)
+            continue;
+        P.out_tokens[tb + i] = (i < j) ? xs : (i == j ? token : -1);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K3: explicit-q residual chunk masses for rejecting requests
+// ---------------------------------------------------------------------------------------
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) residual_kernel(Params P)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nunits = (int64_t)P.B * P.nchunks;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t per = (nunits + nw - 1) / nw;
+    const int64_t u0 = gw * per;
+    const int64_t u1 = min(nunits, u0 + per);
+    for (int64_t u = u0; u < u1; ++u) {
+        const int r = (int)(u / P.nchunks);
+        const int c = (int)(u - (int64_t)r * P.nchunks);
+        const int j = P.rstate[r];
+        if (j < 0)
+            continue;
+        const int cu0 = P.cu[r];
+        const int64_t t = (int64_t)cu0 + r + j;
+        const int64_t d = (int64_t)cu0 + j;
+        const float2 st = P.rstat[r];
+        const float cs = kLog2e / P.temp[r];
+        ResidualMass<DT> f{row_ptr<DT>(P, t), P.q + d * P.qstride, cs, st.x, 1.f / st.y};
+        const int64_t lo = (int64_t)c * P.chunk;
+        const int64_t hi = min((int64_t)P.V, lo + P.chunk);
+        // lane-strided 8-element groups keep the loads coalesced
+        float s = 0.f;
+        const int64_t n8 = (hi - lo + 7) / 8;
+        for (int64_t g = lane; g < n8; g += 32)
+            s += f.range(lo + g * 8, min(hi, lo + g * 8 + 8));
+        s = warp_sum(s);
+        if (lane == 0)
+            P.rpart[(int64_t)r * P.nchunks + c] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K4: explicit-q recovered token
+// ---------------------------------------------------------------------------------------
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) recover_kernel(Params P)
+{
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (r >= P.B)
+        return;
+    const int j = P.rstate[r];
+    if (j < 0)
+        return;
+    const int cu0 = P.cu[r];
+    const int64_t t = (int64_t)cu0 + r + j;
+    const int64_t d = (int64_t)cu0 + j;
+    const float2 st = P.rstat[r];
+    const float cs = kLog2e / P.temp[r];
+    const float us = P.uni[2 * t + 1];
+    const char *row = row_ptr<DT>(P, t);
+    ChunkMassFromArray cmz{P.rpart + (int64_t)r * P.nchunks};
+    const float Z = chunk_total(cmz, P.nchunks, lane);
+    int token;
+    if (Z > 0.f) {
+        float th;
+        const int c = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
+        ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y};
+        token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
+    } else {  // empty residual: draw from p itself (x* back in)
+        const int xs = P.ids[d];
+        const float wj = ex2(fmaf(load1<DT>(row, xs), cs, -st.x));
+        ChunkMassFromPartials cm{P.part + t * P.nchunks, cs, st.x, xs / P.chunk, wj};
+        const float Zp = chunk_total(cm, P.nchunks, lane);
+        float th;
+        const int c = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
+        TargetMass<DT> f{row, cs, st.x, -1};
+        token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
+    }
+    if (lane == 0) {
+        P.out_tokens[t] = token;
+        if (P.dbg_z)
+            P.dbg_z[r] = Z > 0.f ? Z : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Diagnostics: per-row statistics from K1's partials
+// ---------------------------------------------------------------------------------------
+
+// One warp per row: m_t and s_t = sum exp((l - m_t) / T_r) (sampling rows, x* included).
+template <int DT>
+__global__ void __launch_bounds__(kThreads) debug_soft_kernel(Params P, float *row_max, float *row_sum)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= P.T || P.B == 0 || (P.err[0] & SPEC_DEVERR_LAYOUT))
+        return;
+    const int r = find_request(P, t);
+    const float temp = P.temp[r];
+    if (!(temp > 0.f))
+        return;  // greedy rows: filled from the argmax pass
+    const float cs = kLog2e / temp;
+    const int64_t i = t - ((int64_t)P.cu[r] + r);
+    const int k = P.cu[r + 1] - P.cu[r];
+    const int xs = (i < k) ? P.ids[t - r] : -1;
+    float M, S;
+    warp_combine_soft(P, t, cs, lane, M, S);
+    float m = -INFINITY;
+    for (int c = lane; c < P.nchunks; c += 32)
+        m = fmaxf(m, P.part[t * P.nchunks + c].x);
+    m = warp_max(m);
+    if (xs >= 0 && xs < P.V) {
+        const float ls = load1<DT>(row_ptr<DT>(P, t), xs);
+        m = fmaxf(m, ls);
+        const float ys = ls * cs;
+        if (ys > M) {
+            S = (M == -INFINITY) ? 0.f : S * ex2(M - ys);
+            M = ys;
+        }
+        S += ex2(fmaf(ls, cs, -M));
+    }
+    if (lane == 0) {
+        if (row_max)
+            row_max[t] = m;
+        if (row_sum)  // S is relative to 2^M; rescale to exp(-m / T)
+            row_sum[t] = (float)((double)S * exp2((double)M - (double)m * (double)cs));
+    }
+}
+
+// One warp per row after an argmax pass: lowest-index argmax (and the max on greedy rows).
+__global__ void __launch_bounds__(kThreads) debug_argmax_kernel(Params P, float *row_max, float *row_sum,
+                                                                int32_t *row_argmax)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= P.T || P.B == 0 || (P.err[0] & SPEC_DEVERR_LAYOUT))
+        return;
+    const int idx = warp_combine_argmax(P, t, lane);
+    if (lane == 0) {
+        if (row_argmax)
+            row_argmax[t] = idx;
+        const int r = find_request(P, t);
+        if (!(P.temp[r] > 0.f)) {
+            float best;
+            lane_combine_argmax(P, t, &best);
+            if (row_max)
+                row_max[t] = best;
+            if (row_sum)
+                row_sum[t] = 0.f;
+            const int64_t i = t - ((int64_t)P.cu[r] + r);
+            if (P.dbg_pdraft && i < P.cu[r + 1] - P.cu[r])
+                P.dbg_pdraft[t - r] = 0.f;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------
+
+struct DeviceInfo {
+    int sms = 0;
+    int blocks_rowstats[2] = {0, 0};
+    int blocks_residual[2] = {0, 0};
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];  // per-device launch-shape cache (SM count, occupancy)
+
+template <int DT> cudaError_t fill_info(DeviceInfo &di)
+{
+    cudaError_t e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_rowstats[DT], rowstats_kernel<DT>, kThreads, 0)))
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT>, kThreads, 0);
+}
+
+cudaError_t device_info(DeviceInfo **out)
+{
+    int dev;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    DeviceInfo &di = g_dev[dev];
+    if (di.sms == 0) {
+        DeviceInfo tmp;
+        if ((e = cudaDeviceGetAttribute(&tmp.sms, cudaDevAttrMultiProcessorCount, dev)))
+            return e;
+        if ((e = fill_info<0>(tmp)) || (e = fill_info<1>(tmp)))
+            return e;
+        di = tmp;
+    }
+    *out = &di;
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Blocks for a persistent launch: enough to fill every SM at full occupancy, no more
+// than there is work for, at least one.
+int64_t clamp_grid(int64_t full, int64_t needed)
+{
+    const int64_t g = needed < full ? needed : full;
+    return g < 1 ? 1 : g;
+}
+
+spec_status check_args(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t lstride, const float *q,
+                       int64_t qstride, const int32_t *ids, const int32_t *cu, int32_t B, const float *uni,
+                       const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws)
+{
+    if (dt != SPEC_F32 && dt != SPEC_BF16)
+        return SPEC_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || V < 1 || T < B)
+        return SPEC_ERR_INVALID_ARG;
+    if (V > SPEC_REJECT_MAX_VOCAB)
+        return SPEC_ERR_UNSUPPORTED;
+    if (lstride != 0 && lstride < V)
+        return SPEC_ERR_INVALID_ARG;
+    if (q && qstride != 0 && qstride < V)
+        return SPEC_ERR_INVALID_ARG;
+    if (!cu || !ws || (T > 0 && (!logits || !uni || !out_tokens)) || (B > 0 && (!temp || !out_acc)) ||
+        (T > B && !ids))
+        return SPEC_ERR_INVALID_ARG;
+    const size_t es = dt == SPEC_BF16 ? 2 : 4;
+    if (!aligned(logits, es) || !aligned(q, 4) || !aligned(ids, 4) || !aligned(cu, 4) || !aligned(uni, 4) ||
+        !aligned(temp, 4) || !aligned(out_tokens, 4) || !aligned(out_acc, 4))
+        return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
+
+spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t lstride, const float *q,
+                int64_t qstride, const int32_t *ids, const int32_t *cu, int32_t B, const float *uni,
+                const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
+                cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
+                cudaEvent_t *ev = nullptr, int nev = 0)
+{
+    spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
+    if (st != SPEC_OK)
+        return st;
+    Plan pl;
+    if (!make_plan(B, T, V, dt, q != nullptr, &pl))
+        return SPEC_ERR_INVALID_ARG;
+    if (ws_bytes < pl.total)
+        return SPEC_ERR_WORKSPACE;
+    DeviceInfo *di;
+    if (device_info(&di) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    Params P;
+    P.logits = logits;
+    P.T = T;
+    P.V = V;
+    P.lstride = lstride;
+    P.q = q;
+    P.qstride = qstride;
+    P.ids = ids;
+    P.cu = cu;
+    P.B = B;
+    P.uni = uni;
+    P.temp = temp;
+    P.out_tokens = out_tokens;
+    P.out_acc = out_acc;
+    P.part = reinterpret_cast<float2 *>(base + pl.off_part);
+    P.err = reinterpret_cast<int32_t *>(base + pl.off_err);
+    P.rstate = q ? reinterpret_cast<int32_t *>(base + pl.off_rstate) : nullptr;
+    P.rstat = reinterpret_cast<float2 *>(base + pl.off_rstat);
+    P.rpart = q ? reinterpret_cast<float *>(base + pl.off_rpart) : nullptr;
+    P.chunk = pl.chunk;
+    P.nchunks = pl.nchunks;
+    P.dbg_pdraft = dbg_pd;
+    P.dbg_z = dbg_z;
+
+    const int DT = dt == SPEC_BF16 ? 1 : 0;
+    const int64_t units = T * (int64_t)pl.nchunks;
+    const int64_t full = (int64_t)di->sms * (di->blocks_rowstats[DT] > 0 ? di->blocks_rowstats[DT] : 1);
+    const int gridA = (int)clamp_grid(full, (units + kWarps - 1) / kWarps);
+    const int gridB = (int)((B + kWarps - 1) / kWarps);
+    const bool debug = dbg_m || dbg_s || dbg_am || dbg_pd || dbg_z;
+
+    // stage events: [0] before K1, [1] after K1, [2] after K2, [3] after K3, [4] after K4
+    int evi = 0;
+    auto mark = [&]() {
+        if (evi < nev && ev[evi])
+            cudaEventRecord(ev[evi], stream);
+        ++evi;
+    };
+    mark();
+    if (DT)
+        rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, 0);
+    else
+        rowstats_kernel<0><<<gridA, kThreads, 0, stream>>>(P, 0);
+    mark();
+    if (debug && T > 0 && (dbg_m || dbg_s)) {
+        const int g = (int)((T + kWarps - 1) / kWarps);
+        if (DT)
+            debug_soft_kernel<1><<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s);
+        else
+            debug_soft_kernel<0><<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s);
+    }
+    if (B > 0) {
+        if (DT)
+            finalize_kernel<1><<<gridB, kThreads, 0, stream>>>(P);
+        else
+            finalize_kernel<0><<<gridB, kThreads, 0, stream>>>(P);
+        mark();
+        if (q) {
+            const int64_t runits = (int64_t)B * pl.nchunks;
+            const int64_t rfull = (int64_t)di->sms * (di->blocks_residual[DT] > 0 ? di->blocks_residual[DT] : 1);
+            const int gridC = (int)clamp_grid(rfull, (runits + kWarps - 1) / kWarps);
+            if (DT)
+                residual_kernel<1><<<gridC, kThreads, 0, stream>>>(P);
+            else
+                residual_kernel<0><<<gridC, kThreads, 0, stream>>>(P);
+            mark();
+            if (DT)
+                recover_kernel<1><<<gridB, kThreads, 0, stream>>>(P);
+            else
+                recover_kernel<0><<<gridB, kThreads, 0, stream>>>(P);
+            mark();
+        }
+    }
+    if (debug && T > 0 && B > 0 && (dbg_am || dbg_m || dbg_s || dbg_pd)) {
+        // argmax of every row (the sampling path does not need it), then per-row combine
+        if (DT)
+            rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, 1);
+        else
+            rowstats_kernel<0><<<gridA, kThreads, 0, stream>>>(P, 1);
+        const int g = (int)((T + kWarps - 1) / kWarps);
+        debug_argmax_kernel<<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s, dbg_am);
+    }
+    if (cudaGetLastError() != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------------------
+
+extern "C" {
+
+size_t spec_reject_workspace_size(int32_t B, int64_t T, int32_t V, spec_dtype logits_dtype, int has_draft_probs)
+{
+    Plan pl;
+    if (!make_plan(B, T, V, logits_dtype, has_draft_probs, &pl))
+        return 0;
+    return pl.total;
+}
+
+spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                               int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                               const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                               const float *uniforms, const float *temperature, int32_t *out_tokens,
+                               int32_t *out_num_accepted, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
+               cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                       const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                       const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                       int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
+                                       void *stream, float *row_max, float *row_sum, int32_t *row_argmax,
+                                       float *p_draft, float *z_out)
+{
+    return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
+               cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(stream), row_max, row_sum, row_argmax, p_draft, z_out);
+}
+
+spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                        int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                        const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                        const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                        int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
+                                        void *stream, void *const *stage_events, int num_events)
+{
+    return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
+               cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, nullptr, nullptr,
+               reinterpret_cast<cudaEvent_t *>(const_cast<void **>(stage_events)), num_events);
+}
+
+spec_status spec_reject_last_device_error(const void *workspace, void *stream, int32_t *error_bits,
+                                          int32_t *first_bad_request)
+{
+    if (!workspace)
+        return SPEC_ERR_INVALID_ARG;
+    const char *base =
+        reinterpret_cast<const char *>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
+    int32_t word[2] = {0, INT_MAX};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(word, base, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (error_bits)
+        *error_bits = word[0];
+    if (first_bad_request)
+        *first_bad_request = (word[0] & SPEC_DEVERR_LAYOUT) || word[1] == INT_MAX ? -1 : word[1];
+    return word[0] ? SPEC_ERR_DEVICE_INPUT : SPEC_OK;
+}
+
+size_t spec_reject_host_arena_size(int32_t B, int64_t T, int32_t V, spec_dtype logits_dtype, int has_draft_probs)
+{
+    Plan pl;
+    if (!make_plan(B, T, V, logits_dtype, has_draft_probs, &pl))
+        return 0;
+    const size_t es = logits_dtype == SPEC_BF16 ? 2 : 4;
+    size_t o = 0;
+    o = align256(o + es * (size_t)T * (size_t)V);                                       // logits
+    o = align256(o + (has_draft_probs ? 4 * (size_t)(T - B) * (size_t)V : 0));          // draft probs
+    o = align256(o + 4 * (size_t)(T - B));                                              // draft ids
+    o = align256(o + 4 * (size_t)(B + 1));                                              // cu
+    o = align256(o + 8 * (size_t)T);                                                    // uniforms
+    o = align256(o + 4 * (size_t)B);                                                    // temperature
+    o = align256(o + 4 * (size_t)T);                                                    // out tokens
+    o = align256(o + 4 * (size_t)B);                                                    // out accepted
+    return o + pl.total + 256;
+}
+
+spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                    const float *draft_probs, const int32_t *draft_ids, const int32_t *cu_num_draft,
+                                    int32_t B, const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                    int32_t *out_num_accepted, void *device_arena, size_t arena_bytes, void *stream)
+{
+    if (!device_arena || !cu_num_draft || B < 0 || T < B || V < 1 || (T > 0 && (!target_logits || !uniforms ||
+        !out_tokens)) || (B > 0 && (!temperature || !out_num_accepted)) || (T > B && !draft_ids))
+        return SPEC_ERR_INVALID_ARG;
+    const size_t need = spec_reject_host_arena_size(B, T, V, logits_dtype, draft_probs != nullptr);
+    if (need == 0)
+        return SPEC_ERR_INVALID_ARG;
+    if (arena_bytes < need)
+        return SPEC_ERR_WORKSPACE;
+    const size_t es = logits_dtype == SPEC_BF16 ? 2 : 4;
+    const int has_q = draft_probs != nullptr;
+    char *a = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(device_arena) + 255) & ~uintptr_t(255));
+    size_t o = 0;
+    char *d_logits = a + o;
+    o = align256(o + es * (size_t)T * (size_t)V);
+    float *d_q = reinterpret_cast<float *>(a + o);
+    o = align256(o + (has_q ? 4 * (size_t)(T - B) * (size_t)V : 0));
+    int32_t *d_ids = reinterpret_cast<int32_t *>(a + o);
+    o = align256(o + 4 * (size_t)(T - B));
+    int32_t *d_cu = reinterpret_cast<int32_t *>(a + o);
+    o = align256(o + 4 * (size_t)(B + 1));
+    float *d_uni = reinterpret_cast<float *>(a + o);
+    o = align256(o + 8 * (size_t)T);
+    float *d_temp = reinterpret_cast<float *>(a + o);
+    o = align256(o + 4 * (size_t)B);
+    int32_t *d_tok = reinterpret_cast<int32_t *>(a + o);
+    o = align256(o + 4 * (size_t)T);
+    int32_t *d_acc = reinterpret_cast<int32_t *>(a + o);
+    o = align256(o + 4 * (size_t)B);
+    char *d_ws = a + o;
+    const size_t ws_bytes = arena_bytes - (size_t)(d_ws - reinterpret_cast<char *>(device_arena));
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // one cudaMemcpyAsync per buffer
+    const struct {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    } in[] = {
+        {d_logits, target_logits, es * (size_t)T * (size_t)V},
+        {d_q, draft_probs, has_q ? 4 * (size_t)(T - B) * (size_t)V : 0},
+        {d_ids, draft_ids, 4 * (size_t)(T - B)},
+        {d_cu, cu_num_draft, 4 * (size_t)(B + 1)},
+        {d_uni, uniforms, 8 * (size_t)T},
+        {d_temp, temperature, 4 * (size_t)B},
+    };
+    for (const auto &c : in)
+        if (c.bytes && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+    spec_status st = spec_reject_sample(d_logits, logits_dtype, T, V, V, has_q ? d_q : nullptr, V, d_ids, d_cu, B,
+                                        d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, stream);
+    if (st != SPEC_OK)
+        return st;
+    if ((T && cudaMemcpyAsync(out_tokens, d_tok, 4 * (size_t)T, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+        (B && cudaMemcpyAsync(out_num_accepted, d_acc, 4 * (size_t)B, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+const char *spec_reject_status_string(spec_status status)
+{
+    switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument (null pointer, size, stride or alignment)";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size";
+    case SPEC_ERR_WORKSPACE: return "workspace too small";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_DEVICE_INPUT: return "invalid device input (see the device error word)";
+    case SPEC_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int spec_reject_version(void) { return 100; }
+
+int spec_reject_num_kernels(int has_draft_probs) { return has_draft_probs ? 4 : 2; }
+
+}  // extern "C"

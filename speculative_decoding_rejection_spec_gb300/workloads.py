@@ -104,6 +104,7 @@ def generate(spec: dict | str, seed: int | None = None, threads: int | None = No
     name = spec if isinstance(spec, str) else spec.get("name", "custom")
     spec = dict(CONFIGS[spec]) if isinstance(spec, str) else dict(spec)
     spec.update(overrides)
+    name = spec.get("name", name)
     seed = int(spec.get("seed", 0) if seed is None else seed)
     B, V = int(spec["B"]), int(spec["V"])
     ks = _draft_counts(spec, seed)

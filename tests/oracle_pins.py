@@ -481,6 +481,10 @@ def check_invalid_inputs(impl=None):
                                None, impl=impl)
     if res.status != 1 or not (res.num_accepted == -1).all():
         return False, "T != cu[B] + B not reported"
+    res = oracle.reject_sample(l, ids, np.array([0, 3, 1, 36], np.int32), rng.random((T, 2), dtype=np.float32),
+                               np.ones(B, np.float32), None, impl=impl)
+    if res.status != 1 or not (res.num_accepted == -1).all() or (res.tokens != -2).any():
+        return False, "decreasing cu not reported as a layout error"
     return True, "ok"
 
 

@@ -1,0 +1,110 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path, run the oracle, compare.
+
+Comparison rule: accepted counts and tokens must match the oracle exactly on every
+request the oracle does not flag.  A request is flagged when one of its decisions
+came within the oracle's near-boundary band (acceptance within 1e-5 relative of
+u * q(x*) = p(x*); the sampling threshold within 1e-5 * Z of a CDF boundary, or
+within 2e-6 absolute on an explicit-q residual row), when its residual was empty, or
+when a row it visited was not finite.  Flagged requests are counted, never excused
+silently: the tests bound how many there may be.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+import oracle
+from speculative_decoding_rejection_spec_gb300 import binding
+
+
+@dataclass
+class Compared:
+    n: int
+    flagged: int
+    mismatched: int        # unflagged requests that differ (must be 0)
+    mismatched_flagged: int
+    detail: str
+
+
+def dtype_code(w):
+    return binding.BF16 if w["dtype"] == "bf16" else binding.F32
+
+
+def run_gpu(w, debug=False, device_tensors=None, buffers=None):
+    import torch
+    d = device_tensors or binding.to_device(w)
+    buf = buffers or binding.make_buffers(w["B"], w["T"], w["V"], dtype_code(w), d["draft_probs"] is not None)
+    dbg = {} if debug else None
+    tok, acc = binding.sample(**d, buffers=buf, debug=dbg)
+    st, bits, first = binding.last_device_error(buf.workspace)
+    torch.cuda.synchronize()
+    out = dict(tokens=tok.cpu().numpy().copy(), acc=acc.cpu().numpy().copy(), status=st, bits=bits, first=first)
+    if debug:
+        out.update({k: v.cpu().numpy() for k, v in dbg.items()})
+    return out
+
+
+def compare(w, gpu, ref) -> Compared:
+    cu = w["cu_num_draft"]
+    B = w["B"]
+    flagged = (ref.flags & (oracle.NEAR_ANY | oracle.NONFINITE)) != 0
+    mism = 0
+    mism_f = 0
+    first = ""
+    for r in range(B):
+        lo, hi = int(cu[r]) + r, int(cu[r + 1]) + r + 1
+        same = gpu["acc"][r] == ref.num_accepted[r] and np.array_equal(gpu["tokens"][lo:hi], ref.tokens[lo:hi])
+        if not same:
+            if flagged[r]:
+                mism_f += 1
+            else:
+                mism += 1
+                if not first:
+                    first = (f"request {r}: gpu acc {gpu['acc'][r]} tokens {gpu['tokens'][lo:hi].tolist()} | "
+                             f"oracle acc {ref.num_accepted[r]} tokens {ref.tokens[lo:hi].tolist()} "
+                             f"flags {ref.flags[r]}")
+    return Compared(n=B, flagged=int(flagged.sum()), mismatched=mism, mismatched_flagged=mism_f, detail=first)
+
+
+def assert_parity(w, gpu=None, ref=None, max_flag_frac=0.02):
+    gpu = gpu if gpu is not None else run_gpu(w)
+    ref = ref if ref is not None else oracle.reject_sample_workload(w)
+    c = compare(w, gpu, ref)
+    assert c.mismatched == 0, f"{w['name']}: {c.mismatched} unflagged mismatches; first: {c.detail}"
+    assert c.flagged <= max(1, int(max_flag_frac * c.n)), f"{w['name']}: {c.flagged} of {c.n} requests flagged"
+    return c, gpu, ref
+
+
+def assert_rowstats(w, gpu, ref):
+    """Per-row probabilities from the diagnostic entry point against the oracle (1e-5 relative)."""
+    B, T = w["B"], w["T"]
+    cu = w["cu_num_draft"]
+    valid_req = ref.num_accepted >= 0
+    rows = np.concatenate([np.arange(cu[r] + r, cu[r + 1] + r + 1) for r in range(B) if valid_req[r]]
+                          ) if valid_req.any() else np.zeros(0, int)
+    finite = np.isfinite(ref.row_max[rows])
+    rows = rows[finite]
+    assert np.array_equal(gpu["row_max"][rows].astype(np.float64), ref.row_max[rows]), "row max"
+    assert np.array_equal(gpu["row_argmax"][rows], ref.row_argmax[rows]), "row argmax"
+    s_ref = ref.row_sum[rows]
+    s_gpu = gpu["row_sum"][rows].astype(np.float64)
+    pos = s_ref > 0
+    rel = np.abs(s_gpu[pos] / s_ref[pos] - 1)
+    assert (rel <= 1e-5).all(), f"row sum: max rel err {rel.max():.3g}"
+    assert (s_gpu[~pos] == 0).all()
+    drows = np.concatenate([np.arange(cu[r], cu[r + 1]) for r in range(B) if valid_req[r]]
+                           ) if valid_req.any() else np.zeros(0, int)
+    if drows.size:
+        p_ref = ref.p_draft[drows]
+        p_gpu = gpu["p_draft"][drows].astype(np.float64)
+        err = np.abs(p_gpu - p_ref)
+        ok = err <= 1e-5 * p_ref + 1e-37
+        assert ok.all(), f"p(x*): worst {np.max(err / np.maximum(p_ref, 1e-300)):.3g} rel"
+    same_j = valid_req & (gpu["acc"] == ref.num_accepted)  # Z belongs to the output row j
+    zr = ref.z[same_j]
+    zg = gpu["z"][same_j].astype(np.float64)
+    explicit = w.get("draft_probs") is not None
+    tol = 1e-5 * zr + (2e-6 if explicit else 0.0)
+    bad = np.abs(zg - zr) > tol
+    assert not bad.any(), f"Z: gpu {zg[bad][:4]} oracle {zr[bad][:4]}"

@@ -1,0 +1,85 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its
+host-side checks reject bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as G
+from speculative_decoding_rejection_spec_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_reject.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    G.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_reject_\w+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert set(binding.EXPORTED) <= set(names), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert binding.status_string(st)
+    assert binding.status_string(3) == "workspace too small"
+    assert lib.spec_reject_version() >= 100
+
+
+def test_workspace_size_monotone_and_rejects_bad_sizes(lib):
+    small = binding.workspace_size(4, 16, 1000, binding.F32, True)
+    big = binding.workspace_size(1024, 9216, 128256, binding.BF16, True)
+    assert 0 < small < big
+    assert binding.workspace_size(1024, 9216, 128256, binding.BF16, False) <= big
+    for bad in [(-1, 4, 10), (1, -1, 10), (1, 1, 0), (1, 1, 2 ** 21)]:
+        assert lib.spec_reject_workspace_size(bad[0], bad[1], bad[2], 0, 0) == 0
+
+
+def _call(lib, **kw):
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: the host checks fail first
+    args = dict(logits=fake, dtype=0, T=8, V=100, stride=100, q=None, qstride=0, ids=fake, cu=fake, B=2,
+                uni=fake, temp=fake, tok=fake, acc=fake, ws=fake, wsb=1 << 20, stream=None)
+    args.update(kw)
+    return lib.spec_reject_sample(args["logits"], args["dtype"], args["T"], args["V"], args["stride"], args["q"],
+                                  args["qstride"], args["ids"], args["cu"], args["B"], args["uni"], args["temp"],
+                                  args["tok"], args["acc"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(logits=None), 1), (dict(cu=None), 1), (dict(ws=None), 1), (dict(ids=None), 1), (dict(uni=None), 1),
+    (dict(temp=None), 1), (dict(tok=None), 1), (dict(acc=None), 1),
+    (dict(dtype=7), 1), (dict(V=0), 1), (dict(T=1, B=2), 1), (dict(B=-1), 1), (dict(stride=50), 1),
+    (dict(q=ctypes.c_void_p(4096), qstride=10), 1), (dict(V=2 ** 21, stride=2 ** 21), 2),
+    (dict(logits=ctypes.c_void_p(4098)), 1), (dict(cu=ctypes.c_void_p(4098)), 1),
+    (dict(wsb=16), 3),
+])
+def test_host_checks(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_host_entry_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    st = lib.spec_reject_sample_host(fake, 0, 8, 100, None, fake, fake, 2, fake, fake, fake, fake, fake, 16, None)
+    assert st == 3
+    st = lib.spec_reject_sample_host(fake, 0, 8, 100, None, fake, None, 2, fake, fake, fake, fake, fake, 1 << 30,
+                                     None)
+    assert st == 1
+    assert lib.spec_reject_last_device_error(None, None, None, None) == 1

@@ -1,0 +1,260 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_rejection_spec_gb300 import binding, workloads as W
+
+import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    import __graft_entry__ as G
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    G.build()
+    binding.load()
+
+
+# ---------------------------------------------------------------------------- the five workloads
+
+SMALL = ["tiny", "greedy", "probabilistic", "deterministic", "large-128"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_config_parity_and_rowstats(name):
+    w = W.generate(name)
+    ref = oracle.reject_sample_workload(w, debug=True)
+    gpu = PT.run_gpu(w, debug=True)
+    assert gpu["status"] == 0, gpu
+    c, _, _ = PT.assert_parity(w, gpu, ref)
+    PT.assert_rowstats(w, gpu, ref)
+    if name == "greedy":
+        assert c.flagged == 0  # every greedy decision is an exact comparison
+
+
+@pytest.mark.parametrize("name", ["large-512", "large-1024"])
+def test_full_size_parity(name):
+    """Full-size large-batch workloads, in the launch configuration the benchmark times."""
+    w = W.generate(name)
+    gpu = PT.run_gpu(w)
+    assert gpu["status"] == 0
+    PT.assert_parity(w, gpu, oracle.reject_sample_workload(w))
+
+
+def test_production_entry_matches_diagnostic_entry():
+    w = W.generate("probabilistic", B=8)
+    a = PT.run_gpu(w)
+    b = PT.run_gpu(w, debug=True)
+    assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["acc"], b["acc"])
+
+
+def test_deterministic_repeat():
+    w = W.generate("large-128")
+    d = binding.to_device(w)
+    a = PT.run_gpu(w, device_tensors=d)
+    b = PT.run_gpu(w, device_tensors=d)
+    assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["acc"], b["acc"])
+
+
+# ---------------------------------------------------------------------------- edge cases
+
+def _mixed_k(B, seed):
+    rng = np.random.default_rng(seed)
+    k = rng.integers(0, 33, size=B)
+    k[:4] = [0, 32, 0, 32]
+    return k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("draft", ["noisy_q", "target_mix"])
+def test_ragged_k_zero_and_max_odd_vocab(dtype, draft):
+    """k in 0..32 (k = 0 and k = 32 present), V = 5003 (odd: misaligned rows, vector tails)."""
+    w = W.generate(dict(B=24, K=_mixed_k(24, 5), V=5003, dtype=dtype, sigma=1.0, temperature=1.0, draft=draft,
+                        q_sigma=0.3, p_match=0.9, seed=21), name=f"ragged-{dtype}-{draft}")
+    ref = oracle.reject_sample_workload(w, debug=True)
+    gpu = PT.run_gpu(w, debug=True)
+    PT.assert_parity(w, gpu, ref, max_flag_frac=0.1)
+    PT.assert_rowstats(w, gpu, ref)
+
+
+@pytest.mark.parametrize("V", [1, 7, 1001, 4096, 4097, 12289])
+def test_vocab_edges(V):
+    """Vocabularies from 1 to several chunks with ragged tails, both dtypes, both draft kinds."""
+    for dtype in ("f32", "bf16"):
+        for draft in ("noisy_q", "uniform"):
+            w = W.generate(dict(B=6, K=3, V=V, dtype=dtype, sigma=1.5, temperature=0.9, draft=draft, seed=V),
+                           name=f"V{V}-{dtype}-{draft}")
+            ref = oracle.reject_sample_workload(w, debug=True)
+            gpu = PT.run_gpu(w, debug=True)
+            PT.assert_parity(w, gpu, ref, max_flag_frac=0.5)
+            PT.assert_rowstats(w, gpu, ref)
+
+
+def test_q_equals_p_accepts_everything():
+    w = W.generate(dict(B=32, K=6, V=3000, dtype="f32", sigma=2.0, temperature=0.8, draft="target_q", seed=31),
+                   name="q=p")
+    w["uniforms"][:, 0] *= np.float32(0.999)  # fp32 rounding of q vs p cannot flip a decision
+    c, gpu, ref = PT.assert_parity(w)
+    assert (gpu["acc"] == 6).all()
+
+
+def test_disjoint_supports_reject_at_zero():
+    w = W.generate(dict(B=16, K=4, V=2048, dtype="f32", sigma=2.0, temperature=1.0, draft="noisy_q", seed=41),
+                   name="disjoint")
+    w["logits"][:, 1::2] = -np.inf
+    q = np.random.default_rng(3).random(w["draft_probs"].shape)
+    q[:, 0::2] = 0
+    w["draft_probs"][:] = (q / q.sum(axis=1, keepdims=True)).astype(np.float32)
+    w["draft_ids"][:] = np.random.default_rng(4).integers(0, 1024, size=w["draft_ids"].shape) * 2 + 1
+    c, gpu, ref = PT.assert_parity(w)
+    assert (gpu["acc"] == 0).all()
+    assert (gpu["tokens"].reshape(16, 5)[:, 0] % 2 == 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_one_hot_target_and_masked_logits(dtype):
+    w = W.generate(dict(B=20, K=5, V=3001, dtype=dtype, sigma=2.0, temperature=1.0, draft="uniform", seed=51),
+                   name="masked")
+    neg = np.float32(-np.inf)
+    rng = np.random.default_rng(5)
+    lg = W.logits_as_f32(w).copy()
+    lg[rng.random(lg.shape) < 0.3] = neg          # 30 % masked tokens
+    hot_rows = rng.random(lg.shape[0]) < 0.3       # some rows one-hot
+    hot = rng.integers(0, 3001, size=lg.shape[0])
+    lg[hot_rows] = neg
+    lg[hot_rows, hot[hot_rows]] = 0.0
+    # half of the drafts of one-hot rows hit the hot token
+    rows = np.arange(w["T"])
+    req = np.repeat(np.arange(w["B"]), 6)
+    drow = rows - req
+    isd = (rows - (w["cu_num_draft"][req] + req)) < 5
+    sel = isd & hot_rows & (rng.random(w["T"]) < 0.5)
+    w["draft_ids"][drow[sel]] = hot[sel]
+    w["logits"][:] = W.f32_to_bf16_bits(lg) if dtype == "bf16" else lg
+    ref = oracle.reject_sample_workload(w, debug=True)
+    gpu = PT.run_gpu(w, debug=True)
+    PT.assert_parity(w, gpu, ref)
+    PT.assert_rowstats(w, gpu, ref)
+
+
+def test_mixed_greedy_and_sampled_explicit_q():
+    temps = np.where(np.arange(40) % 2 == 0, -1.0, 0.7)
+    temps[::5] = 0.0
+    w = W.generate(dict(B=40, K="ragged", K_max=8, V=7000, dtype="bf16", sigma=2.5, temperature=temps,
+                        draft="noisy_q", q_sigma=0.5, seed=61), name="mixed")
+    ref = oracle.reject_sample_workload(w, debug=True)
+    gpu = PT.run_gpu(w, debug=True)
+    PT.assert_parity(w, gpu, ref)
+    PT.assert_rowstats(w, gpu, ref)
+
+
+def test_greedy_bf16_ties_lowest_index():
+    w = W.generate(dict(B=64, K=5, V=9000, dtype="bf16", sigma=1.0, temperature=0.0, draft="argmax_mix",
+                        p_match=0.8, seed=71), name="ties")
+    lg = np.round(W.logits_as_f32(w) * 2) / 2  # coarse values: many ties at the maximum
+    w["logits"][:] = W.f32_to_bf16_bits(lg.astype(np.float32))
+    am = np.argmax(lg, axis=1)
+    rows = np.arange(w["T"])
+    req = np.repeat(np.arange(w["B"]), 6)
+    isd = (rows - (w["cu_num_draft"][req] + req)) < 5
+    w["draft_ids"][:] = am[isd]
+    ref = oracle.reject_sample_workload(w, debug=True)
+    gpu = PT.run_gpu(w, debug=True)
+    c, _, _ = PT.assert_parity(w, gpu, ref)
+    assert c.flagged == 0
+    assert (gpu["acc"] == 5).all()
+    PT.assert_rowstats(w, gpu, ref)
+
+
+def test_zero_uniforms():
+    w = W.generate(dict(B=16, K=4, V=3000, dtype="f32", sigma=2.0, temperature=1.0, draft="noisy_q", seed=81),
+                   name="u0")
+    w["uniforms"][::3] = 0.0
+    PT.assert_parity(w, max_flag_frac=0.2)
+
+
+def test_strided_logits_rows():
+    """Rows further apart than V (a padded or sliced logits buffer)."""
+    import torch
+    w = W.generate(dict(B=8, K=4, V=1001, dtype="bf16", sigma=2.0, temperature=0.9, draft="noisy_q", seed=91),
+                   name="strided")
+    d = binding.to_device(w)
+    big = torch.zeros((w["T"], 1024 + 40), dtype=torch.bfloat16, device="cuda")
+    big[:, 8:8 + 1001] = d["target_logits"]
+    d["target_logits"] = big[:, 8:8 + 1001]
+    qbig = torch.zeros((w["T"] - w["B"], 1100), dtype=torch.float32, device="cuda")
+    qbig[:, 3:3 + 1001] = d["draft_probs"]
+    d["draft_probs"] = qbig[:, 3:3 + 1001]
+    gpu = PT.run_gpu(w, device_tensors=d)
+    PT.assert_parity(w, gpu)
+
+
+def test_single_request_and_empty_batch():
+    import torch
+    w = W.generate(dict(B=1, K=7, V=2000, dtype="f32", sigma=2.0, temperature=1.0, draft="noisy_q", seed=101),
+                   name="single")
+    PT.assert_parity(w)
+    # B = 0, T = 0: nothing to do, no device error
+    z = torch.zeros(0, device="cuda")
+    e = binding.make_buffers(0, 0, 10, binding.F32, False)
+    tok, acc = binding.sample(torch.zeros((0, 10), device="cuda"), torch.zeros(0, dtype=torch.int32, device="cuda"),
+                              torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros((0, 2), device="cuda"),
+                              z, buffers=e)
+    assert binding.last_device_error(e.workspace)[0] == 0
+
+
+# ---------------------------------------------------------------------------- invalid device input
+
+def _run_raw(w):
+    d = binding.to_device(w)
+    buf = binding.make_buffers(w["B"], w["T"], w["V"], PT.dtype_code(w), d["draft_probs"] is not None)
+    tok, acc = binding.sample(**d, buffers=buf)
+    st, bits, first = binding.last_device_error(buf.workspace)
+    return tok.cpu().numpy(), acc.cpu().numpy(), st, bits, first
+
+
+def test_device_errors_per_request():
+    w = W.generate(dict(B=5, K=[2, 33, 3, 1, 4], V=500, dtype="f32", sigma=1.0, temperature=1.0, draft="noisy_q",
+                        seed=111), name="bad")
+    w["draft_ids"][w["cu_num_draft"][3]] = 500  # request 3: id out of range
+    ref = oracle.reject_sample_workload(w)
+    tok, acc, st, bits, first = _run_raw(w)
+    assert st == 5 and bits == (binding.DEVERR_SPEC_LEN | binding.DEVERR_DRAFT_ID) and first == 1
+    assert acc[1] == -1 and acc[3] == -1 and (ref.num_accepted[[1, 3]] == -1).all()
+    assert np.array_equal(tok, ref.tokens) and np.array_equal(acc, ref.num_accepted)
+
+
+@pytest.mark.parametrize("which", ["cu0", "decreasing", "total"])
+def test_device_errors_layout(which):
+    w = W.generate(dict(B=4, K=3, V=300, dtype="f32", sigma=1.0, temperature=1.0, draft="uniform", seed=121),
+                   name="layout")
+    if which == "cu0":
+        w["cu_num_draft"][0] = 1
+    elif which == "decreasing":
+        w["cu_num_draft"][2] = 1
+    else:
+        w["cu_num_draft"][-1] -= 1
+    tok, acc, st, bits, first = _run_raw(w)
+    assert st == 5 and bits & binding.DEVERR_LAYOUT and first == -1
+    assert (acc == -1).all()
+    ref = oracle.reject_sample_workload(w)
+    assert ref.status == 1 and (ref.num_accepted == -1).all()
+
+
+# ---------------------------------------------------------------------------- host-buffer entry point
+
+def test_host_entry_matches_device_entry():
+    import torch
+    for name in ("tiny", "greedy"):
+        w = W.generate(name)
+        dev = PT.run_gpu(w)
+        arena = torch.empty(binding.host_arena_size(w["B"], w["T"], w["V"], PT.dtype_code(w),
+                                                    w["draft_probs"] is not None), dtype=torch.uint8, device="cuda")
+        tok, acc = binding.sample_host(w["logits"], w["draft_ids"], w["cu_num_draft"], w["uniforms"],
+                                       w["temperature"], w["draft_probs"], arena)
+        assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
