@@ -72,7 +72,7 @@ class Oracle:
             P, ctypes.c_int64, P, P, ctypes.c_int32,  # q, q stride, draft ids, cu, B
             P, P,  # uniforms, temperature
             P, P, P,  # out tokens, out accepted, out flags
-            P, P, P, P, P,  # dbg row max / sum / argmax, p draft, z
+            P, P, P, P, P, P,  # dbg row max / sum / argmax, p draft, z, margins
             ctypes.c_int,  # nthreads
         ]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -111,6 +111,7 @@ class OracleResult:
     row_argmax: np.ndarray | None = None
     p_draft: np.ndarray | None = None
     z: np.ndarray | None = None
+    margin: np.ndarray | None = None  # [B, 2]: acceptance margin (relative), sampling margin / Z
 
 
 def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.ndarray, uniforms: np.ndarray,
@@ -157,13 +158,15 @@ def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.nd
     dbg = {}
     if debug:
         dbg = dict(row_max=np.full(T, np.nan), row_sum=np.full(T, np.nan), row_argmax=np.full(T, -1, np.int32),
-                   p_draft=np.full(max(T - B, 0), np.nan), z=np.full(B, np.nan))
+                   p_draft=np.full(max(T - B, 0), np.nan), z=np.full(B, np.nan),
+                   margin=np.full((max(B, 0), 2), np.inf))
     if ids.size == 0:
         ids = np.zeros(1, dtype=np.int32)
     status = (impl or _load()).lib.oracle_reject_sample(
         _ptr(logits), dcode, T, V, stride, _ptr(q), qs, _ptr(ids), _ptr(cu), B, _ptr(u), _ptr(temp),
         _ptr(tokens), _ptr(acc), _ptr(flags), _ptr(dbg.get("row_max")), _ptr(dbg.get("row_sum")),
-        _ptr(dbg.get("row_argmax")), _ptr(dbg.get("p_draft")), _ptr(dbg.get("z")), int(nthreads))
+        _ptr(dbg.get("row_argmax")), _ptr(dbg.get("p_draft")), _ptr(dbg.get("z")), _ptr(dbg.get("margin")),
+        int(nthreads))
     return OracleResult(tokens=tokens, num_accepted=acc, flags=flags, status=int(status), **dbg)
 
 

@@ -183,6 +183,10 @@ static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u, doubl
  *   dbg_p_draft[T-B]  per draft row: p(x*) (0 on greedy rows or bad ids)
  *   dbg_z[B]          per request: normalised residual mass at the output row (1 for the
  *                     bonus, 0 for greedy)
+ *   dbg_margin[2*B]   per request: [0] the smallest relative acceptance margin
+ *                     |u*q* - p*| / max(p*, u*q*) over the visited positions, [1] the
+ *                     sampling margin (distance from theta to the nearest boundary of
+ *                     the chosen interval) divided by Z; +inf where not applicable
  * Every dbg_* pointer may be NULL.  nthreads <= 0 uses the OpenMP default.
  * Returns 0, or 1 when the batch as a whole is inconsistent (cu[0] != 0, cu[B] + B != T or
  * cu decreasing), in which case every request is reported invalid and no token is written.
@@ -192,7 +196,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                          const int32_t *cu_num_draft, int32_t B, const float *uniforms, const float *temperature,
                          int32_t *out_tokens, int32_t *out_num_accepted, uint32_t *out_flags, double *dbg_row_max,
                          double *dbg_row_sum, int32_t *dbg_row_argmax, double *dbg_p_draft, double *dbg_z,
-                         int nthreads)
+                         double *dbg_margin, int nthreads)
 {
     logit_rows L = {target_logits, dtype, T, V, logits_row_stride};
     const int64_t num_draft_rows = T - B;
@@ -243,6 +247,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
             const int greedy = !(temp > 0.0);
             int64_t j = k; /* output position: first rejection, or k for the bonus */
             int nonfinite = 0;
+            double margin_accept = INFINITY, margin_sample = INFINITY;
 
             /* Acceptance test, sequential over the drafts, stopping at the first rejection. */
             for (int64_t i = 0; i < k; ++i) {
@@ -264,6 +269,8 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 const double big = lhs > rhs ? lhs : rhs;
                 if (fabs(lhs - rhs) <= REL_BAND * big)
                     flags |= OF_NEAR_ACCEPT;
+                if (big > 0.0 && fabs(lhs - rhs) / big < margin_accept)
+                    margin_accept = fabs(lhs - rhs) / big;
                 if (!(lhs < rhs)) {
                     j = i;
                     break;
@@ -308,6 +315,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 if (Z > 0.0) {
                     zr = Z;
                     token = inverse_cdf(r, V, Z, us, &margin);
+                    margin_sample = margin / Z;
                     if (margin <= REL_BAND * Z)
                         flags |= OF_NEAR_SAMPLE;
                     if (explicit_residual && margin <= ABS_BAND)
@@ -318,6 +326,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                     for (int32_t v = 0; v < V; ++v)
                         Zp += p[v];
                     token = inverse_cdf(p, V, Zp, us, &margin);
+                    margin_sample = margin / Zp;
                     if (margin <= REL_BAND * Zp)
                         flags |= OF_NEAR_SAMPLE;
                 }
@@ -335,6 +344,10 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 out_flags[req] = flags;
             if (dbg_z)
                 dbg_z[req] = greedy ? 0.0 : zr;
+            if (dbg_margin) {
+                dbg_margin[2 * req] = margin_accept;
+                dbg_margin[2 * req + 1] = margin_sample;
+            }
         }
 
         /* Per-row statistics for every row (debug outputs only). */

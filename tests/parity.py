@@ -6,7 +6,10 @@ came within the oracle's near-boundary band (acceptance within 1e-5 relative of
 u * q(x*) = p(x*); the sampling threshold within 1e-5 * Z of a CDF boundary, or
 within 2e-6 absolute on an explicit-q residual row), when its residual was empty, or
 when a row it visited was not finite.  Flagged requests are counted, never excused
-silently: the tests bound how many there may be.
+silently.  How many are flagged depends on the workload (with V = 151936 most of the
+mass sits in tokens narrower than 1e-5), so the tests bound what matters: how many
+flagged requests actually differ, and how close to a boundary each of them was (the
+oracle's margins; the fp32 path's error is far below the band).
 """
 from __future__ import annotations
 
@@ -25,6 +28,7 @@ class Compared:
     mismatched: int        # unflagged requests that differ (must be 0)
     mismatched_flagged: int
     detail: str
+    worst_margin: float    # largest oracle margin among mismatched requests (0 if none)
 
 
 def dtype_code(w):
@@ -52,10 +56,16 @@ def compare(w, gpu, ref) -> Compared:
     mism = 0
     mism_f = 0
     first = ""
+    worst = 0.0
     for r in range(B):
         lo, hi = int(cu[r]) + r, int(cu[r + 1]) + r + 1
         same = gpu["acc"][r] == ref.num_accepted[r] and np.array_equal(gpu["tokens"][lo:hi], ref.tokens[lo:hi])
         if not same:
+            if ref.margin is not None:
+                m_acc, m_smp = float(ref.margin[r, 0]), float(ref.margin[r, 1])
+                if w.get("draft_probs") is not None and 0 <= ref.num_accepted[r] < cu[r + 1] - cu[r]:
+                    m_smp *= float(ref.z[r])  # explicit-q residual: the fp32 error is absolute, not relative to Z
+                worst = max(worst, min(m_acc, m_smp))
             if flagged[r]:
                 mism_f += 1
             else:
@@ -64,15 +74,25 @@ def compare(w, gpu, ref) -> Compared:
                     first = (f"request {r}: gpu acc {gpu['acc'][r]} tokens {gpu['tokens'][lo:hi].tolist()} | "
                              f"oracle acc {ref.num_accepted[r]} tokens {ref.tokens[lo:hi].tolist()} "
                              f"flags {ref.flags[r]}")
-    return Compared(n=B, flagged=int(flagged.sum()), mismatched=mism, mismatched_flagged=mism_f, detail=first)
+    return Compared(n=B, flagged=int(flagged.sum()), mismatched=mism, mismatched_flagged=mism_f, detail=first,
+                    worst_margin=worst)
 
 
-def assert_parity(w, gpu=None, ref=None, max_flag_frac=0.02):
+# Largest relative margin at which the fp32 path may still decide differently from the
+# fp64 oracle: well inside the 1e-5 band, several times the path's worst fp32 error.
+MISMATCH_MARGIN = 2e-6
+
+
+def assert_parity(w, gpu=None, ref=None, max_mismatch_frac=0.01):
     gpu = gpu if gpu is not None else run_gpu(w)
-    ref = ref if ref is not None else oracle.reject_sample_workload(w)
+    ref = ref if ref is not None else oracle.reject_sample_workload(w, debug=True)
     c = compare(w, gpu, ref)
-    assert c.mismatched == 0, f"{w['name']}: {c.mismatched} unflagged mismatches; first: {c.detail}"
-    assert c.flagged <= max(1, int(max_flag_frac * c.n)), f"{w['name']}: {c.flagged} of {c.n} requests flagged"
+    msg = (f"{w['name']}: {c.n} requests, {c.flagged} flagged, {c.mismatched_flagged} flagged mismatches, "
+           f"worst margin {c.worst_margin:.3g}")
+    print(msg)
+    assert c.mismatched == 0, f"{msg}; {c.mismatched} UNFLAGGED mismatches; first: {c.detail}"
+    assert c.mismatched_flagged <= max(2, int(max_mismatch_frac * c.n)), msg
+    assert c.worst_margin <= MISMATCH_MARGIN, msg
     return c, gpu, ref
 
 
