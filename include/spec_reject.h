@@ -169,6 +169,36 @@ spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype lo
                                         int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
                                         void *stream, void *const *stage_events, int num_events);
 
+/*
+ * spec_reject_sample() for callers that cannot allocate device memory: for example a
+ * plugin inside a host inference engine that is handed only its inputs and outputs, or
+ * a serving loop that must not call cudaMalloc between steps (it can synchronise the
+ * device and stall the other streams).  The pages have no counterpart; this is a
+ * deployment convenience.
+ *
+ * Same arguments and results as spec_reject_sample(), without the workspace: the
+ * scratch is a fixed array of SPEC_REJECT_NOALLOC_SCRATCH_BYTES in device memory that
+ * every GPU loading this library holds until the process exits.  A batch whose
+ * spec_reject_workspace_size() exceeds that returns SPEC_ERR_WORKSPACE and launches
+ * nothing (for V = 128256 bf16 logits with draft probabilities and K = 8 that is
+ * 3432 requests, 30888 target rows).  The call allocates nothing.
+ *
+ * The first call on a device (the current device) looks up the array's device address;
+ * make that first call before any stream capture.  Every call shares the one array and
+ * leaves its contents behind: calls that can overlap on the GPU (different streams, or
+ * different host threads on one device) race and must be serialised by the caller.
+ *
+ * device_error_word: optional device int32[2] that receives the device error word of
+ * this call ([0] SPEC_DEVERR_* bits, [1] first bad request or INT32_MAX), copied on
+ * `stream` after the kernels; NULL to skip.
+ */
+#define SPEC_REJECT_NOALLOC_SCRATCH_BYTES (8u << 20)
+spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                       const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                       const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                       int32_t *out_num_accepted, int32_t *device_error_word, void *stream);
+
 /* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 4 with). */
 int spec_reject_num_kernels(int has_draft_probs);
 

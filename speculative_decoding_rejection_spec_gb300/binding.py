@@ -24,6 +24,7 @@ EXPORTED = [
     "spec_reject_workspace_size", "spec_reject_sample", "spec_reject_last_device_error",
     "spec_reject_host_arena_size", "spec_reject_sample_host", "spec_reject_debug_rowstats",
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
+    "spec_reject_sample_noalloc",
 ]
 
 _lib = None
@@ -63,6 +64,8 @@ def load():
     lib.spec_reject_version.restype = ctypes.c_int
     lib.spec_reject_sample_profiled.restype = ctypes.c_int
     lib.spec_reject_sample_profiled.argtypes = sample_args + [P, ctypes.c_int]
+    lib.spec_reject_sample_noalloc.restype = ctypes.c_int
+    lib.spec_reject_sample_noalloc.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int]
     _lib = lib
@@ -195,6 +198,26 @@ def sample_profiled(d: dict, buffers: Buffers, events: list, stream=None):
         int(buffers.workspace.numel()), _stream(stream), handles, len(events))
     if st != 0:
         raise SpecRejectError(st, "spec_reject_sample_profiled")
+
+
+def sample_noalloc(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *,
+                   out_tokens, out_num_accepted, device_error_word=None, stream=None):
+    """``sample`` without a workspace: the library's fixed device scratch array is used.
+
+    For callers that cannot allocate device memory.  The caller still provides the
+    outputs (and optionally a device int32[2] for the error word).  Calls that overlap
+    on the GPU share the one scratch array and race.
+    """
+    T, V = int(target_logits.shape[0]), int(target_logits.shape[1])
+    B = int(cu_num_draft.shape[0]) - 1
+    q = draft_probs
+    st = load().spec_reject_sample_noalloc(
+        _ptr(target_logits), _dtype_code(target_logits), T, V, _row_stride(target_logits), _ptr(q),
+        0 if q is None else _row_stride(q), _ptr(draft_ids), _ptr(cu_num_draft), B, _ptr(uniforms),
+        _ptr(temperature), _ptr(out_tokens), _ptr(out_num_accepted), _ptr(device_error_word), _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_sample_noalloc")
+    return out_tokens, out_num_accepted
 
 
 def num_kernels(has_draft_probs: bool) -> int:

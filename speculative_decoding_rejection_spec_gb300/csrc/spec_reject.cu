@@ -1433,6 +1433,53 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     return SPEC_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------------------
+
+// Scratch for spec_reject_sample_noalloc(): a fixed device array instead of a caller
+// workspace.  Every GPU that loads this library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_REJECT_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on each device.  In host code the symbol is only a
+// host-side stand-in, so the address comes from cudaGetSymbolAddress, once per device.
+static void *g_noalloc_addr[kMaxDevices];
+
+spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                       const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                       const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                       int32_t *out_num_accepted, int32_t *device_error_word, void *stream)
+{
+    const size_t need = spec_reject_workspace_size(B, T, V, logits_dtype, draft_probs != nullptr);
+    if (need == 0)
+        return SPEC_ERR_INVALID_ARG;
+    if (need > SPEC_REJECT_NOALLOC_SCRATCH_BYTES)
+        return SPEC_ERR_WORKSPACE;  // batch too large for the fixed scratch array
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return SPEC_ERR_CUDA;
+    if (!g_noalloc_addr[dev]) {  // first call on this device (current device): look the address up
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
+            return SPEC_ERR_CUDA;
+        g_noalloc_addr[dev] = addr;
+    }
+    // Nothing in the scratch has to start at zero: the row-statistics kernel writes the
+    // error word first and every other region is written before it is read.
+    const spec_status st = spec_reject_sample(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs,
+                                              q_row_stride, draft_ids, cu_num_draft, B, uniforms, temperature,
+                                              out_tokens, out_num_accepted, g_noalloc_addr[dev],
+                                              SPEC_REJECT_NOALLOC_SCRATCH_BYTES, stream);
+    if (st != SPEC_OK || !device_error_word)
+        return st;
+    // the error word sits at the start of the (256-byte aligned) scratch
+    if (cudaMemcpyAsync(device_error_word, g_noalloc_addr[dev], 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
 const char *spec_reject_status_string(spec_status status)
 {
     switch (status) {
