@@ -72,6 +72,7 @@ typedef enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_DEVERR_LAYOUT 1     /* cu_num_draft[0] != 0, cu[B] + B != T, or cu decreasing */
 #define SPEC_DEVERR_SPEC_LEN 2   /* some k_r > 32 */
 #define SPEC_DEVERR_DRAFT_ID 4   /* some draft id outside [0, V) */
+#define SPEC_DEVERR_TIMEOUT 8    /* a bounded wait inside a kernel gave up (results invalid) */
 
 /*
  * Bytes of device workspace spec_reject_sample() needs for a batch of B

@@ -46,8 +46,19 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnitBytes = 8192;  // bytes of logits per (row, chunk) unit
-constexpr int kUnroll = 8;        // 16-byte vectors in flight per lane
+#ifndef SPEC_UNIT_BYTES
+#define SPEC_UNIT_BYTES 8192
+#endif
+#ifndef SPEC_LDG_UNROLL
+#define SPEC_LDG_UNROLL 4       // 16-byte vectors in flight per lane (register-staged K1)
+#endif
+#ifndef SPEC_LDG_MIN_BLOCKS
+#define SPEC_LDG_MIN_BLOCKS 3   // blocks of 256 per SM the register-staged K1 must fit
+#endif
+#ifndef SPEC_TMA_MIN_BLOCKS
+#define SPEC_TMA_MIN_BLOCKS 2   // blocks per SM of the TMA K1 (each with its own ring)
+#endif
+constexpr int kUnitBytes = SPEC_UNIT_BYTES;  // bytes of logits per (row, chunk) unit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -158,26 +169,6 @@ template <> __device__ __forceinline__ void unpack<1>(const uint4 &w, float *x)
     x[5] = __uint_as_float(w.z & 0xffff0000u);
     x[6] = __uint_as_float(w.w << 16);
     x[7] = __uint_as_float(w.w & 0xffff0000u);
-}
-
-// A 16-byte vector with element `rel` replaced by -inf (fp32 0xff800000, bf16 0xff80).
-template <int DT> __device__ __forceinline__ uint4 mask_elem(uint4 w, int rel);
-template <> __device__ __forceinline__ uint4 mask_elem<0>(uint4 w, int rel)
-{
-    w.x = rel == 0 ? 0xff800000u : w.x;
-    w.y = rel == 1 ? 0xff800000u : w.y;
-    w.z = rel == 2 ? 0xff800000u : w.z;
-    w.w = rel == 3 ? 0xff800000u : w.w;
-    return w;
-}
-template <> __device__ __forceinline__ uint4 mask_elem<1>(uint4 w, int rel)
-{
-    const uint32_t lo = 0x0000ff80u, hi = 0xff800000u;
-    w.x = rel == 0 ? (w.x & 0xffff0000u) | lo : rel == 1 ? (w.x & 0x0000ffffu) | hi : w.x;
-    w.y = rel == 2 ? (w.y & 0xffff0000u) | lo : rel == 3 ? (w.y & 0x0000ffffu) | hi : w.y;
-    w.z = rel == 4 ? (w.z & 0xffff0000u) | lo : rel == 5 ? (w.z & 0x0000ffffu) | hi : w.z;
-    w.w = rel == 6 ? (w.w & 0xffff0000u) | lo : rel == 7 ? (w.w & 0x0000ffffu) | hi : w.w;
-    return w;
 }
 
 template <int DT> __device__ __forceinline__ uint4 neg_inf_vec();
@@ -354,52 +345,36 @@ template <> __device__ __forceinline__ float vec_max<1>(const uint4 &w)
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
 }
 
-template <int DT>
-__device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, float cs, int xs, int lane);
-template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int64_t t, int c, int lane);
+// Source of the 16-byte vectors of a unit body: streaming loads from global memory.
+struct GlobalVec {
+    static constexpr int kUnroll = SPEC_LDG_UNROLL;  // vectors in flight per lane
+    const char *base;
+    __device__ __forceinline__ uint4 operator()(int64_t vi) const { return ld_stream(base + vi * 16); }
+};
 
-template <int DT>
-__device__ __forceinline__ void rowstats_unit(const Params &P, int64_t t, int c, bool greedy, float cs, int xs,
-                                              int lane)
-{
-    if (greedy)
-        argmax_unit<DT>(P, t, c, lane);
-    else
-        softmax_unit<DT>(P, t, c, cs, xs, lane);
-}
-
-template <int DT>
-__device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, float cs, int xs, int lane)
+// Softmax partial of one unit: body vectors from `src`, head / tail scalars from `row`.
+template <int DT, class SRC>
+__device__ __forceinline__ void softmax_body(const Params &P, int64_t t, int c, float cs, int lane, const SRC &src,
+                                             const UnitRange &R, const char *row)
 {
     constexpr int VEC = Elem<DT>::kVec;
-    constexpr int ES = Elem<DT>::kSize;
-    const char *row = row_ptr<DT>(P, t);
-    const UnitRange R = unit_range<DT>(P, row, c);
     const int64_t lo = R.lo, hi = R.hi, vlo = R.vlo, nvec = R.nvec, vhi = R.vhi;
-    const char *vbase = row + vlo * ES;
     {
         SoftAcc acc;
         float sacc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
             sacc[e] = 0.f;
-        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * kUnroll) {
-            uint4 raw[kUnroll];
+        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * SRC::kUnroll) {
+            uint4 raw[SRC::kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < SRC::kUnroll; ++u) {
                 const int64_t vi = b0 + u * 32 + lane;
-                if (vi < nvec) {
-                    raw[u] = ld_stream(vbase + vi * 16);
-                    const int rel = xs - (int)(vlo + vi * VEC);
-                    if ((unsigned)rel < (unsigned)VEC)  // the draft token: leave it out
-                        raw[u] = mask_elem<DT>(raw[u], rel);
-                } else {
-                    raw[u] = neg_inf_vec<DT>();
-                }
+                raw[u] = (vi < nvec) ? src(vi) : neg_inf_vec<DT>();
             }
             float bm = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
+            for (int u = 0; u < SRC::kUnroll; ++u)
                 bm = fmaxf(bm, vec_max<DT>(raw[u]));
             if (bm > acc.m) {
                 // fold the per-slot sums into the lane sum before moving the reference
@@ -415,7 +390,7 @@ __device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, flo
             if (acc.m > -INFINITY) {  // nothing but -inf so far: no mass, and M is not finite
                 const float M = acc.M;
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
+                for (int u = 0; u < SRC::kUnroll; ++u) {
                     float x[VEC];
                     unpack<DT>(raw[u], x);
 #pragma unroll
@@ -433,14 +408,10 @@ __device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, flo
         }
         // scalar head and tail (fewer than VEC elements each)
         float xh = -INFINITY, xt = -INFINITY;
-        if (lane < vlo - lo) {
-            const int64_t v = lo + lane;
-            xh = (v == xs) ? -INFINITY : load1<DT>(row, v);
-        }
-        if (lane < hi - vhi) {
-            const int64_t v = vhi + lane;
-            xt = (v == xs) ? -INFINITY : load1<DT>(row, v);
-        }
+        if (lane < vlo - lo)
+            xh = load1<DT>(row, lo + lane);
+        if (lane < hi - vhi)
+            xt = load1<DT>(row, vhi + lane);
         const float bm = fmaxf(xh, xt);
         if (bm > -INFINITY) {
             acc.rebase(bm, cs);
@@ -456,28 +427,27 @@ __device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, flo
     }
 }
 
-template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int64_t t, int c, int lane)
+// Argmax partial of one unit (greedy rows).
+template <int DT, class SRC>
+__device__ __forceinline__ void argmax_body(const Params &P, int64_t t, int c, int lane, const SRC &src,
+                                            const UnitRange &R, const char *row)
 {
     constexpr int VEC = Elem<DT>::kVec;
-    constexpr int ES = Elem<DT>::kSize;
-    const char *row = row_ptr<DT>(P, t);
-    const UnitRange R = unit_range<DT>(P, row, c);
     const int64_t lo = R.lo, hi = R.hi, vlo = R.vlo, nvec = R.nvec, vhi = R.vhi;
-    const char *vbase = row + vlo * ES;
     {
         ArgAcc acc;
         if (lane < vlo - lo)
             acc.add(load1<DT>(row, lo + lane), (int)(lo + lane));
-        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * kUnroll) {
-            uint4 raw[kUnroll];
+        for (int64_t b0 = 0; b0 < nvec; b0 += 32 * SRC::kUnroll) {
+            uint4 raw[SRC::kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < SRC::kUnroll; ++u) {
                 const int64_t vi = b0 + u * 32 + lane;
                 if (vi < nvec)
-                    raw[u] = ld_stream(vbase + vi * 16);
+                    raw[u] = src(vi);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < SRC::kUnroll; ++u) {
                 const int64_t vi = b0 + u * 32 + lane;
                 if (vi < nvec) {
                     float x[VEC];
@@ -497,8 +467,46 @@ template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int6
     }
 }
 
+template <int DT> __device__ __noinline__ void softmax_unit(const Params &P, int64_t t, int c, float cs, int lane)
+{
+    const char *row = row_ptr<DT>(P, t);
+    const UnitRange R = unit_range<DT>(P, row, c);
+    softmax_body<DT>(P, t, c, cs, lane, GlobalVec{row + R.vlo * Elem<DT>::kSize}, R, row);
+}
+
+template <int DT> __device__ __noinline__ void argmax_unit(const Params &P, int64_t t, int c, int lane)
+{
+    const char *row = row_ptr<DT>(P, t);
+    const UnitRange R = unit_range<DT>(P, row, c);
+    argmax_body<DT>(P, t, c, lane, GlobalVec{row + R.vlo * Elem<DT>::kSize}, R, row);
+}
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads) rowstats_kernel(Params P, int force_argmax)
+__device__ __forceinline__ void rowstats_unit(const Params &P, int64_t t, int c, bool greedy, float cs, int lane)
+{
+    if (greedy)
+        argmax_unit<DT>(P, t, c, lane);
+    else
+        softmax_unit<DT>(P, t, c, cs, lane);
+}
+
+// Per-row parameters a unit needs: greedy or not, and c = log2(e) / T_r.
+struct RowInfo {
+    int64_t t = -1;
+    bool greedy = true;
+    float cs = 0.f;
+};
+
+__device__ __forceinline__ void row_info(const Params &P, int64_t t, int force_argmax, RowInfo &ri)
+{
+    ri.t = t;
+    const float temp = __ldg(P.temp + find_request(P, t));
+    ri.greedy = force_argmax || !(temp > 0.f);
+    ri.cs = ri.greedy ? 0.f : kLog2e / temp;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, SPEC_LDG_MIN_BLOCKS) rowstats_kernel(Params P, int force_argmax)
 {
     if (blockIdx.x == 0)
         validate_layout(P);
@@ -511,25 +519,276 @@ __global__ void __launch_bounds__(kThreads) rowstats_kernel(Params P, int force_
     const int64_t per = (nunits + nw - 1) / nw;
     const int64_t u0 = gw * per;
     const int64_t u1 = min(nunits, u0 + per);
-    int64_t cached_t = -1;
-    bool greedy = true;
-    float cs = 0.f;
-    int xs = -1;
+    RowInfo ri;
     for (int64_t u = u0; u < u1; ++u) {
         const int64_t t = u / P.nchunks;
         const int c = (int)(u - t * P.nchunks);
-        if (t != cached_t) {
-            cached_t = t;
-            const int r = find_request(P, t);
-            const int64_t i = t - ((int64_t)__ldg(P.cu + r) + r);
-            const int k = __ldg(P.cu + r + 1) - __ldg(P.cu + r);
-            const int64_t d = t - r;
-            const float temp = __ldg(P.temp + r);
-            greedy = force_argmax || !(temp > 0.f);
-            cs = greedy ? 0.f : kLog2e / temp;
-            xs = (!greedy && i >= 0 && i < k && d >= 0 && d < P.T - P.B) ? __ldg(P.ids + d) : -1;
+        if (t != ri.t)
+            row_info(P, t, force_argmax, ri);
+        rowstats_unit<DT>(P, t, c, ri.greedy, ri.cs, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// K1 with a TMA ring: bulk copies into shared memory, decoupling bytes in flight from registers
+// ---------------------------------------------------------------------------------------
+
+#ifndef SPEC_TMA_STAGES
+#define SPEC_TMA_STAGES 12     // 12 x 8 KB per block, two blocks: 192 KB of logits in flight per SM
+#endif
+#ifndef SPEC_TMA_CONSUMERS
+#define SPEC_TMA_CONSUMERS 6   // consumer warps per block; one more warp issues the copies
+#endif
+constexpr int kTmaStages = SPEC_TMA_STAGES;
+constexpr int kTmaConsumers = SPEC_TMA_CONSUMERS;
+// A parity wait names the right phase only if the stage's previous phase has completed.
+// With the stage count a multiple of the consumer count, round r - 1 of a stage went to
+// the same consumer warp, which therefore saw it complete before it waits for round r.
+static_assert(kTmaStages % kTmaConsumers == 0, "stages must be a multiple of consumer warps");
+constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up (far above any real wait)
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, at most kWaitLimit polls.  On
+// giving up it sets SPEC_DEVERR_TIMEOUT in the error word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    atomicOr(err, SPEC_DEVERR_TIMEOUT);
+    return false;
+}
+
+// One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), its
+// completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+constexpr int kVecPerLane = kUnitBytes / 16 / 32;  // 16-byte vectors of a unit held by each lane
+
+// Softmax partial of a unit held in registers: v[k] is body vector k * 32 + lane (slots
+// past the body hold -inf), the scalar tail comes from global memory.
+template <int DT>
+__device__ __forceinline__ void softmax_regs(const Params &P, int64_t t, int c, float cs, int lane,
+                                             const uint4 (&v)[kVecPerLane], const UnitRange &R, const char *row)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    float xt = -INFINITY;
+    if (lane < R.hi - R.vhi)
+        xt = load1<DT>(row, R.vhi + lane);
+    float m = xt;
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k)
+        m = fmaxf(m, vec_max<DT>(v[k]));
+    const float M = m * cs;
+    float s = 0.f;
+    if (m > -INFINITY) {
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            acc[e] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+            float x[VEC];
+            unpack<DT>(v[k], x);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                acc[e] += ex2(fmaf(x[e], cs, -M));
         }
-        rowstats_unit<DT>(P, t, c, greedy, cs, xs, lane);
+        acc[0] += ex2(fmaf(xt, cs, -M));
+#pragma unroll
+        for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e)
+                acc[e] += acc[e + w];
+        s = acc[0];
+    }
+    const float mw = warp_max(m);
+    const float Mw = mw * cs;
+    const float sl = (m == -INFINITY) ? 0.f : s * ex2(M - Mw);
+    const float sw = warp_sum(sl);
+    if (lane == 0)
+        P.part[t * P.nchunks + c] = make_float2(mw, mw == -INFINITY ? 0.f : sw);
+}
+
+template <int DT>
+__device__ __forceinline__ void argmax_regs(const Params &P, int64_t t, int c, int lane, const uint4 (&v)[kVecPerLane],
+                                            const UnitRange &R, const char *row)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    ArgAcc acc;
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+        const int64_t vi = (int64_t)k * 32 + lane;
+        if (vi < R.nvec) {
+            float x[VEC];
+            unpack<DT>(v[k], x);
+            const int v0 = (int)(R.vlo + vi * VEC);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                acc.add(x[e], v0 + e);
+        }
+    }
+    if (lane < R.hi - R.vhi)
+        acc.add(load1<DT>(row, R.vhi + lane), (int)(R.vhi + lane));
+    warp_argmax(acc.best, acc.idx);
+    if (lane == 0)
+        P.part[t * P.nchunks + c] = make_float2(acc.best, __int_as_float(acc.idx));
+}
+
+// What the producer tells the consumer of a stage about its unit.
+struct StageInfo {
+    int64_t t;  // target row
+    int c;      // chunk of the row
+    float cs;   // log2(e) / T_r, or 0 on greedy rows
+    int greedy;
+};
+
+// Rows must start on 16-byte boundaries (the host checks base and stride).  Units are
+// split contiguously over the blocks; within a block, unit i goes through stage i % S and
+// is reduced by consumer warp i % kTmaConsumers, which copies the stage into registers and
+// hands it back to the producer before reducing it.  The producer walks the units in order,
+// so it follows rows and requests incrementally and passes each stage's row parameters on
+// in shared memory (published by the same mbarrier phase as the data).
+template <int DT>
+__global__ void __launch_bounds__(kTmaThreads, SPEC_TMA_MIN_BLOCKS) rowstats_tma_kernel(Params P, int force_argmax)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    constexpr int ES = Elem<DT>::kSize;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kTmaStages];
+    __shared__ __align__(8) uint64_t empty[kTmaStages];
+    __shared__ StageInfo info[kTmaStages];
+
+    if (blockIdx.x == 0)
+        validate_layout(P);
+    if (P.B == 0)
+        return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const int64_t nunits = P.T * (int64_t)P.nchunks;
+    const int64_t per = (nunits + gridDim.x - 1) / gridDim.x;
+    const int64_t u0 = (int64_t)blockIdx.x * per;
+    const int64_t n = max((int64_t)0, min(nunits, u0 + per) - u0);
+
+    if (warp == kTmaConsumers) {  // producer
+        if (lane != 0)
+            return;
+        int64_t issued = 0;
+        int64_t t = u0 / P.nchunks;
+        int c = (int)(u0 - t * P.nchunks);
+        int r = n > 0 ? find_request(P, t) : 0;
+        int64_t r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;  // first row after request r
+        float cs = 0.f;
+        int greedy = 1;
+        int64_t info_t = -1;
+        for (int64_t i = 0; i < n; ++i) {
+            const int s = (int)(i % kTmaStages);
+            const uint32_t round = (uint32_t)(i / kTmaStages);
+            if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1, P.err))
+                break;
+            if (t != info_t) {
+                info_t = t;
+                while (t >= r_end && r < P.B - 1) {  // next request (rows are request-major)
+                    ++r;
+                    r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;
+                }
+                const float temp = __ldg(P.temp + r);
+                greedy = force_argmax || !(temp > 0.f);
+                cs = greedy ? 0.f : kLog2e / temp;
+            }
+            info[s] = StageInfo{t, c, cs, greedy};
+            const int64_t lo = (int64_t)c * P.chunk;
+            const int64_t hi = min((int64_t)P.V, lo + P.chunk);
+            const uint32_t bytes = (uint32_t)((hi - lo) * ES) & ~15u;
+            mbar_arrive_expect_tx(&full[s], bytes);
+            if (bytes)
+                bulk_g2s(ring + (size_t)s * kUnitBytes, row_ptr<DT>(P, t) + lo * ES, bytes, &full[s]);
+            ++issued;
+            if (++c == P.nchunks) {
+                c = 0;
+                ++t;
+            }
+        }
+        if (issued < n) {  // gave up: let the copies still in flight land before the block exits
+            for (int64_t i = max((int64_t)0, issued - kTmaStages); i < issued; ++i)
+                mbar_wait(&full[i % kTmaStages], (uint32_t)(i / kTmaStages) & 1, P.err);
+        }
+        return;
+    }
+
+    for (int64_t i = warp; i < n; i += kTmaConsumers) {
+        const int s = (int)(i % kTmaStages);
+        const bool ok = __all_sync(kFull, mbar_wait(&full[s], (uint32_t)(i / kTmaStages) & 1, P.err));
+        if (!ok)
+            break;
+        const StageInfo si = info[s];
+        const int64_t t = si.t;
+        const int c = si.c;
+        const char *row = row_ptr<DT>(P, t);
+        UnitRange R;
+        R.lo = (int64_t)c * P.chunk;
+        R.hi = min((int64_t)P.V, R.lo + P.chunk);
+        R.vlo = R.lo;
+        R.nvec = ((R.hi - R.lo) * ES) / 16;
+        R.vhi = R.vlo + R.nvec * VEC;
+        const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (size_t)s * kUnitBytes);
+        uint4 v[kVecPerLane];
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+            const int vi = k * 32 + lane;
+            v[k] = (vi < R.nvec) ? stage[vi] : neg_inf_vec<DT>();
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);  // the stage is in registers: hand it back at once
+        if (si.greedy)
+            argmax_regs<DT>(P, t, c, lane, v, R, row);
+        else
+            softmax_regs<DT>(P, t, c, si.cs, lane, v, R, row);
     }
 }
 
@@ -644,9 +903,10 @@ template <int DT> struct TargetMass {
                     s[e & 3] += (v + e == excl) ? 0.f : ex2(fmaf(x[e], cs, -M));
             }
         }
+        float tail = 0.f;
         for (; v < v1; ++v)
-            s[v & 3] += one(v);
-        return (s[0] + s[1]) + (s[2] + s[3]);
+            tail += one(v);
+        return ((s[0] + s[1]) + (s[2] + s[3])) + tail;
     }
 };
 
@@ -680,9 +940,10 @@ template <int DT> struct ResidualMass {
                 }
             }
         }
+        float tail = 0.f;
         for (; v < v1; ++v)
-            s[v & 3] += one(v);
-        return (s[0] + s[1]) + (s[2] + s[3]);
+            tail += one(v);
+        return ((s[0] + s[1]) + (s[2] + s[3])) + tail;
     }
 };
 
@@ -731,20 +992,29 @@ __device__ int64_t warp_find(const F &f, int64_t lo, int64_t hi, float theta, in
     return pos ? lo + (31 - __clz(pos)) : hi - 1;
 }
 
-// Masses of the chunks of row t relative to 2^M (K1 partials), with an optional extra
-// mass added to one chunk (x* back in when sampling p itself on a verify row).
+// Masses of the chunks of row t relative to 2^M (K1 partials), one chunk optionally
+// replaced by a mass computed separately (the chunk of x* without x*).
 struct ChunkMassFromPartials {
     const float2 *pp;
     float cs, M;
-    int extra_chunk;
-    float extra;
+    int override_chunk;
+    float override_mass;
     __device__ __forceinline__ float operator()(int c) const
     {
+        if (c == override_chunk)
+            return override_mass;
         const float2 pc = pp[c];
-        float m = (pc.x == -INFINITY) ? 0.f : pc.y * ex2(pc.x * cs - M);
-        return c == extra_chunk ? m + extra : m;
+        return (pc.x == -INFINITY) ? 0.f : pc.y * ex2(pc.x * cs - M);
     }
 };
+
+// Total mass of [lo, hi) by the warp: 32 contiguous, vector-aligned segments, one per lane.
+template <class F> __device__ __forceinline__ float warp_range_mass(const F &f, int64_t lo, int64_t hi, int lane)
+{
+    const int64_t seg = (((hi - lo + 31) / 32) + 7) & ~int64_t(7);
+    const int64_t s0 = min(hi, lo + lane * seg), s1 = min(hi, s0 + seg);
+    return warp_sum(f.range(s0, s1));
+}
 
 struct ChunkMassFromArray {
     const float *z;
@@ -854,16 +1124,9 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             am = lane_combine_argmax(P, t, nullptr);
             accept = (xs == am);
         } else {
-            lane_combine_soft(P, t, cs, Mi, Si);
-            const float ls = load1<DT>(row_ptr<DT>(P, t), xs);
-            const float ys = ls * cs;
-            if (ys > Mi) {
-                Si = (Mi == -INFINITY) ? 0.f : Si * ex2(Mi - ys);
-                Mi = ys;
-            }
-            const float e = fmaf(ls, cs, -Mi);
+            lane_combine_soft(P, t, cs, Mi, Si);  // every token, x* included
+            const float e = fmaf(load1<DT>(row_ptr<DT>(P, t), xs), cs, -Mi);
             wstar = ex2(e);
-            Si += wstar;
             const float qs = P.q ? __ldg(P.q + (db + lane) * P.qstride + xs) : 1.f;
             const float us = P.uni[2 * t];
             const double lhs = (double)us * (double)qs;  // exact
@@ -903,13 +1166,16 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             const float Sj = __shfl_sync(kFull, Si, j);
             const int xj = __shfl_sync(kFull, xs, j);
             if (!P.q) {  // one-hot draft: residual = p without x*
-                const float wj = __shfl_sync(kFull, wstar, j);
-                ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, Mj, -1, 0.f};
+                // the chunk holding x*, summed again without it (no cancellation)
+                const int cx = xj / P.chunk;
+                TargetMass<DT> fx{row, cs, Mj, xj};
+                const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
+                                                 min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
+                ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, Mj, cx, mx};
                 float Z = chunk_total(cm, P.nchunks, lane);
                 int64_t excl = xj;
                 if (!(Z > 0.f)) {  // empty residual: draw from p itself
-                    cm.extra_chunk = xj / P.chunk;
-                    cm.extra = wj;
+                    cm.override_chunk = -1;
                     Z = chunk_total(cm, P.nchunks, lane);
                     excl = -1;
                 } else {
@@ -1009,10 +1275,8 @@ __global__ void __launch_bounds__(kThreads) recover_kernel(Params P)
         const int c = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
         ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y};
         token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
-    } else {  // empty residual: draw from p itself (x* back in)
-        const int xs = P.ids[d];
-        const float wj = ex2(fmaf(load1<DT>(row, xs), cs, -st.x));
-        ChunkMassFromPartials cm{P.part + t * P.nchunks, cs, st.x, xs / P.chunk, wj};
+    } else {  // empty residual: draw from p itself
+        ChunkMassFromPartials cm{P.part + t * P.nchunks, cs, st.x, -1, 0.f};
         const float Zp = chunk_total(cm, P.nchunks, lane);
         float th;
         const int c = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
@@ -1043,25 +1307,12 @@ __global__ void __launch_bounds__(kThreads) debug_soft_kernel(Params P, float *r
     if (!(temp > 0.f))
         return;  // greedy rows: filled from the argmax pass
     const float cs = kLog2e / temp;
-    const int64_t i = t - ((int64_t)P.cu[r] + r);
-    const int k = P.cu[r + 1] - P.cu[r];
-    const int xs = (i < k) ? P.ids[t - r] : -1;
     float M, S;
     warp_combine_soft(P, t, cs, lane, M, S);
     float m = -INFINITY;
     for (int c = lane; c < P.nchunks; c += 32)
         m = fmaxf(m, P.part[t * P.nchunks + c].x);
     m = warp_max(m);
-    if (xs >= 0 && xs < P.V) {
-        const float ls = load1<DT>(row_ptr<DT>(P, t), xs);
-        m = fmaxf(m, ls);
-        const float ys = ls * cs;
-        if (ys > M) {
-            S = (M == -INFINITY) ? 0.f : S * ex2(M - ys);
-            M = ys;
-        }
-        S += ex2(fmaf(ls, cs, -M));
-    }
     if (lane == 0) {
         if (row_max)
             row_max[t] = m;
@@ -1105,7 +1356,10 @@ struct DeviceInfo {
     int sms = 0;
     int blocks_rowstats[2] = {0, 0};
     int blocks_residual[2] = {0, 0};
+    int blocks_tma[2] = {0, 0};
 };
+
+constexpr size_t kTmaSmem = (size_t)kTmaStages * kUnitBytes;
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];  // per-device launch-shape cache (SM count, occupancy)
@@ -1114,6 +1368,11 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
 {
     cudaError_t e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_rowstats[DT], rowstats_kernel<DT>, kThreads, 0)))
+        return e;
+    if ((e = cudaFuncSetAttribute(rowstats_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem)))
+        return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_tma[DT], rowstats_tma_kernel<DT>, kTmaThreads,
+                                                           kTmaSmem)))
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT>, kThreads, 0);
 }
@@ -1171,6 +1430,28 @@ spec_status check_args(const void *logits, spec_dtype dt, int64_t T, int32_t V, 
         !aligned(temp, 4) || !aligned(out_tokens, 4) || !aligned(out_acc, 4))
         return SPEC_ERR_INVALID_ARG;
     return SPEC_OK;
+}
+
+// K1: the TMA ring when every row starts on a 16-byte boundary (the common case), the
+// register-staged kernel otherwise.
+void launch_rowstats(int DT, const Params &P, const DeviceInfo &di, int64_t T, int nchunks, const void *logits,
+                     int64_t lstride, int gridA, cudaStream_t stream, int force_argmax)
+{
+    const size_t es = DT ? 2 : 4;
+    const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * es) % 16 == 0;
+    if (rows_aligned && di.blocks_tma[DT] > 0) {
+        const int64_t units = T * (int64_t)nchunks;
+        const int grid = (int)clamp_grid((int64_t)di.sms * di.blocks_tma[DT], (units + 3) / 4);
+        if (DT)
+            rowstats_tma_kernel<1><<<grid, kTmaThreads, kTmaSmem, stream>>>(P, force_argmax);
+        else
+            rowstats_tma_kernel<0><<<grid, kTmaThreads, kTmaSmem, stream>>>(P, force_argmax);
+    } else {
+        if (DT)
+            rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, force_argmax);
+        else
+            rowstats_kernel<0><<<gridA, kThreads, 0, stream>>>(P, force_argmax);
+    }
 }
 
 spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t lstride, const float *q,
@@ -1231,10 +1512,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         ++evi;
     };
     mark();
-    if (DT)
-        rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, 0);
-    else
-        rowstats_kernel<0><<<gridA, kThreads, 0, stream>>>(P, 0);
+    launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
     mark();
     if (debug && T > 0 && (dbg_m || dbg_s)) {
         const int g = (int)((T + kWarps - 1) / kWarps);
@@ -1267,10 +1545,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     }
     if (debug && T > 0 && B > 0 && (dbg_am || dbg_m || dbg_s || dbg_pd)) {
         // argmax of every row (the sampling path does not need it), then per-row combine
-        if (DT)
-            rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, 1);
-        else
-            rowstats_kernel<0><<<gridA, kThreads, 0, stream>>>(P, 1);
+        launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 1);
         const int g = (int)((T + kWarps - 1) / kWarps);
         debug_argmax_kernel<<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s, dbg_am);
     }

@@ -46,6 +46,24 @@ def test_full_size_parity(name):
     PT.assert_parity(w, gpu, oracle.reject_sample_workload(w, debug=True))
 
 
+@pytest.mark.parametrize("name", ["greedy", "probabilistic", "deterministic", "large-128"])
+def test_config_parity_unaligned_rows(name):
+    """The same workloads with the logits one element off a 16-byte boundary, which sends the
+    row-statistics pass through its register-staged kernel instead of the TMA ring."""
+    import torch
+    w = W.generate(name)
+    d = binding.to_device(w)
+    t = d["target_logits"]
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    view = buf[1:1 + t.numel()].view(t.shape)
+    view.copy_(t)
+    assert view.data_ptr() % 16 != 0
+    d["target_logits"] = view
+    gpu = PT.run_gpu(w, device_tensors=d)
+    assert gpu["status"] == 0
+    PT.assert_parity(w, gpu, oracle.reject_sample_workload(w, debug=True))
+
+
 def test_production_entry_matches_diagnostic_entry():
     w = W.generate("probabilistic", B=8)
     a = PT.run_gpu(w)
