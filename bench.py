@@ -68,7 +68,7 @@ def traffic_for(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -83,7 +83,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -91,7 +91,6 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -167,8 +166,8 @@ def run_reference(args, w, meta):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large-1024")
     ap.add_argument("--no-e2e", action="store_true")
@@ -253,7 +252,8 @@ def main():
     peak, peak_kind = peaks()
     achieved = k1_bytes / k1_s / 1e9
     tr = traffic_for(args.workload)
-    roofline = {"bound": "hbm", "kernel": "rowstats_kernel", "achieved": round(achieved, 1), "peak": peak,
+    roofline = {"bound": "hbm", "kernel": "row statistics (K1: rowstats_tma_kernel for aligned rows)",
+                "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": None if tr is None else int(tr * w["T"]),
                 "algorithmic_bytes_per_launch": k1_bytes, "ms_per_launch": round(1e3 * k1_s, 4),
