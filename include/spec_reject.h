@@ -159,8 +159,7 @@ spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype log
  * Measurement form of spec_reject_sample(): identical work, plus cudaEventRecord of
  * caller-created events (cudaEvent_t handles) on `stream` between the kernels:
  * stage_events[0] before the row-statistics pass, [1] after it, [2] after the
- * per-request finalize, and with draft_probs [3] after the residual pass and [4]
- * after the recovery pass.  Entries beyond num_events, or NULL entries, are skipped.
+ * per-request finalize, and with draft_probs [3] after the residual / recovery pass.  Entries beyond num_events, or NULL entries, are skipped.
  * The pages have no counterpart: this exists to time each kernel on its own stream.
  */
 spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
@@ -200,7 +199,7 @@ spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype log
                                        const float *uniforms, const float *temperature, int32_t *out_tokens,
                                        int32_t *out_num_accepted, int32_t *device_error_word, void *stream);
 
-/* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 4 with). */
+/* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 3 with). */
 int spec_reject_num_kernels(int has_draft_probs);
 
 /* Static description of a status code. */

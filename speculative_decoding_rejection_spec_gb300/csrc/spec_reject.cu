@@ -26,10 +26,10 @@
 //                 holds u * Z, a three-level warp descent (32 segments -> 32 sub-segments ->
 //                 one element) finds the token inside it.  Explicit-q recoveries are left to
 //                 K3 / K4.
-//   K3 residual   explicit q only: streams target row j and draft row j of each rejecting
-//                 request in chunks, reducing sum max(0, p - q) per chunk.
-//   K4 recover    explicit q only: one warp per rejecting request locates the recovered
-//                 token from K3's chunk masses, as K2 does.
+//   K3 residual   explicit q only: warps stream (request, chunk) units of target row j and
+//                 draft row j of each rejecting request, reducing sum max(0, p - q) per
+//                 chunk; the warp that completes a request's last chunk (a per-request
+//                 counter) locates the recovered token as K2 does.
 //
 // Every reduction has a fixed order (warp butterflies, sequential chunk combines), so
 // identical inputs give identical outputs; there are no floating-point atomics.  No kernel
@@ -55,9 +55,6 @@ constexpr int kWarps = kThreads / 32;
 #ifndef SPEC_LDG_MIN_BLOCKS
 #define SPEC_LDG_MIN_BLOCKS 3   // blocks of 256 per SM the register-staged K1 must fit
 #endif
-#ifndef SPEC_TMA_MIN_BLOCKS
-#define SPEC_TMA_MIN_BLOCKS 2   // blocks per SM of the TMA K1 (each with its own ring)
-#endif
 constexpr int kUnitBytes = SPEC_UNIT_BYTES;  // bytes of logits per (row, chunk) unit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -67,7 +64,7 @@ constexpr unsigned kFull = 0xffffffffu;
 struct Plan {
     int chunk;    // logits per chunk
     int nchunks;  // chunks per row
-    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, total;
+    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, off_rcnt, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -90,6 +87,8 @@ bool make_plan(int32_t B, int64_t T, int32_t V, spec_dtype dt, int has_q, Plan *
     o = align256(o + sizeof(float2) * (size_t)(B + 1));
     pl->off_rpart = o;
     o = align256(o + (has_q ? sizeof(float) * (size_t)B * (size_t)pl->nchunks : 0));
+    pl->off_rcnt = o;
+    o = align256(o + (has_q ? sizeof(int32_t) * (size_t)B : 0));
     pl->total = o + 256;  // slack for aligning the caller's pointer
     return true;
 }
@@ -114,6 +113,7 @@ struct Params {
     int32_t *rstate;  // [B] output position j of a pending explicit-q recovery, else -1
     float2 *rstat;    // [B] (M, S) of that output row
     float *rpart;     // [B * nchunks] residual chunk masses
+    int32_t *rcnt;    // [B] residual chunks done (zeroed by K2, counted up by K3)
     int chunk, nchunks;
     // diagnostics (all may be null)
     float *dbg_pdraft;
@@ -530,22 +530,9 @@ __global__ void __launch_bounds__(kThreads, SPEC_LDG_MIN_BLOCKS) rowstats_kernel
 }
 
 // ---------------------------------------------------------------------------------------
-// K1 with a TMA ring: bulk copies into shared memory, decoupling bytes in flight from registers
+// mbarrier and bulk-copy helpers (TMA)
 // ---------------------------------------------------------------------------------------
 
-#ifndef SPEC_TMA_STAGES
-#define SPEC_TMA_STAGES 12     // 12 x 8 KB per block, two blocks: 192 KB of logits in flight per SM
-#endif
-#ifndef SPEC_TMA_CONSUMERS
-#define SPEC_TMA_CONSUMERS 6   // consumer warps per block; one more warp issues the copies
-#endif
-constexpr int kTmaStages = SPEC_TMA_STAGES;
-constexpr int kTmaConsumers = SPEC_TMA_CONSUMERS;
-// A parity wait names the right phase only if the stage's previous phase has completed.
-// With the stage count a multiple of the consumer count, round r - 1 of a stage went to
-// the same consumer warp, which therefore saw it complete before it waits for round r.
-static_assert(kTmaStages % kTmaConsumers == 0, "stages must be a multiple of consumer warps");
-constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait gives up (far above any real wait)
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -561,11 +548,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
@@ -671,111 +653,98 @@ __device__ __forceinline__ void argmax_regs(const Params &P, int64_t t, int c, i
         P.part[t * P.nchunks + c] = make_float2(acc.best, __int_as_float(acc.idx));
 }
 
-// What the producer tells the consumer of a stage about its unit.
-struct StageInfo {
-    int64_t t;  // target row
-    int c;      // chunk of the row
-    float cs;   // log2(e) / T_r, or 0 on greedy rows
-    int greedy;
-};
+// ---------------------------------------------------------------------------------------
+// K1 with warp-private TMA pipelines
+// ---------------------------------------------------------------------------------------
+//
+// Each warp streams its own contiguous range of units through its own ring of kWrStages
+// shared-memory slots: lane 0 keeps kWrStages bulk copies in flight ahead of the warp, the
+// warp copies a landed unit into registers, lane 0 immediately reuses the slot for the unit
+// kWrStages further on, and the warp reduces the unit from registers.  No warp ever waits
+// for another, and a slot's mbarrier is only waited on by the warp that refills it, one
+// phase at a time, so every parity wait is unambiguous.
 
-// Rows must start on 16-byte boundaries (the host checks base and stride).  Units are
-// split contiguously over the blocks; within a block, unit i goes through stage i % S and
-// is reduced by consumer warp i % kTmaConsumers, which copies the stage into registers and
-// hands it back to the producer before reducing it.  The producer walks the units in order,
-// so it follows rows and requests incrementally and passes each stage's row parameters on
-// in shared memory (published by the same mbarrier phase as the data).
+#ifndef SPEC_WR_WARPS
+#define SPEC_WR_WARPS 4       // warps per block
+#endif
+#ifndef SPEC_WR_STAGES
+#define SPEC_WR_STAGES 3      // slots per warp
+#endif
+#ifndef SPEC_WR_MIN_BLOCKS
+#define SPEC_WR_MIN_BLOCKS 2  // 2 blocks x 4 warps x 3 slots x 8 KB = 192 KB of logits in flight per SM
+#endif
+constexpr int kWrWarps = SPEC_WR_WARPS;
+constexpr int kWrStages = SPEC_WR_STAGES;
+constexpr int kWrThreads = kWrWarps * 32;
+
 template <int DT>
-__global__ void __launch_bounds__(kTmaThreads, SPEC_TMA_MIN_BLOCKS) rowstats_tma_kernel(Params P, int force_argmax)
+__global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_kernel(Params P, int force_argmax)
 {
     constexpr int VEC = Elem<DT>::kVec;
     constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full[kTmaStages];
-    __shared__ __align__(8) uint64_t empty[kTmaStages];
-    __shared__ StageInfo info[kTmaStages];
+    __shared__ __align__(8) uint64_t full[kWrWarps * kWrStages];
 
     if (blockIdx.x == 0)
         validate_layout(P);
     if (P.B == 0)
         return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kTmaStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_fence_init();
-    }
+    if (threadIdx.x < kWrWarps * kWrStages)
+        mbar_init(&full[threadIdx.x], 1);
+    mbar_fence_init();
     __syncthreads();
 
     const int64_t nunits = P.T * (int64_t)P.nchunks;
-    const int64_t per = (nunits + gridDim.x - 1) / gridDim.x;
-    const int64_t u0 = (int64_t)blockIdx.x * per;
+    const int64_t nw = (int64_t)gridDim.x * kWrWarps;
+    const int64_t per = (nunits + nw - 1) / nw;
+    const int64_t u0 = ((int64_t)blockIdx.x * kWrWarps + warp) * per;
     const int64_t n = max((int64_t)0, min(nunits, u0 + per) - u0);
+    unsigned char *slots = ring + (size_t)warp * kWrStages * kUnitBytes;
+    uint64_t *bars = full + warp * kWrStages;
 
-    if (warp == kTmaConsumers) {  // producer
-        if (lane != 0)
-            return;
-        int64_t issued = 0;
-        int64_t t = u0 / P.nchunks;
-        int c = (int)(u0 - t * P.nchunks);
-        int r = n > 0 ? find_request(P, t) : 0;
-        int64_t r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;  // first row after request r
-        float cs = 0.f;
-        int greedy = 1;
-        int64_t info_t = -1;
-        for (int64_t i = 0; i < n; ++i) {
-            const int s = (int)(i % kTmaStages);
-            const uint32_t round = (uint32_t)(i / kTmaStages);
-            if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1, P.err))
-                break;
-            if (t != info_t) {
-                info_t = t;
-                while (t >= r_end && r < P.B - 1) {  // next request (rows are request-major)
-                    ++r;
-                    r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;
-                }
-                const float temp = __ldg(P.temp + r);
-                greedy = force_argmax || !(temp > 0.f);
-                cs = greedy ? 0.f : kLog2e / temp;
-            }
-            info[s] = StageInfo{t, c, cs, greedy};
-            const int64_t lo = (int64_t)c * P.chunk;
-            const int64_t hi = min((int64_t)P.V, lo + P.chunk);
-            const uint32_t bytes = (uint32_t)((hi - lo) * ES) & ~15u;
-            mbar_arrive_expect_tx(&full[s], bytes);
-            if (bytes)
-                bulk_g2s(ring + (size_t)s * kUnitBytes, row_ptr<DT>(P, t) + lo * ES, bytes, &full[s]);
-            ++issued;
-            if (++c == P.nchunks) {
-                c = 0;
-                ++t;
-            }
+    // issue side (lane 0): unit u0 + qi, walked incrementally
+    int64_t it = u0 / P.nchunks;
+    int ic = (int)(u0 - it * P.nchunks);
+    int64_t qi = 0;
+    auto issue = [&]() {
+        const int s = (int)(qi % kWrStages);
+        const int64_t lo = (int64_t)ic * P.chunk;
+        const int64_t hi = min((int64_t)P.V, lo + P.chunk);
+        const uint32_t bytes = (uint32_t)((hi - lo) * ES) & ~15u;
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        if (bytes)
+            bulk_g2s(slots + (size_t)s * kUnitBytes, row_ptr<DT>(P, it) + lo * ES, bytes, &bars[s]);
+        ++qi;
+        if (++ic == P.nchunks) {
+            ic = 0;
+            ++it;
         }
-        if (issued < n) {  // gave up: let the copies still in flight land before the block exits
-            for (int64_t i = max((int64_t)0, issued - kTmaStages); i < issued; ++i)
-                mbar_wait(&full[i % kTmaStages], (uint32_t)(i / kTmaStages) & 1, P.err);
-        }
-        return;
-    }
+    };
+    if (lane == 0)
+        while (qi < n && qi < kWrStages)
+            issue();
 
-    for (int64_t i = warp; i < n; i += kTmaConsumers) {
-        const int s = (int)(i % kTmaStages);
-        const bool ok = __all_sync(kFull, mbar_wait(&full[s], (uint32_t)(i / kTmaStages) & 1, P.err));
-        if (!ok)
+    // compute side: unit u0 + q, row and request walked incrementally
+    int64_t t = u0 / P.nchunks;
+    int c = (int)(u0 - t * P.nchunks);
+    int r = n > 0 ? find_request(P, t) : 0;
+    int64_t r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;
+    int64_t info_t = -1;
+    bool greedy = true;
+    float cs = 0.f;
+    int64_t q = 0;
+    for (; q < n; ++q) {
+        const int s = (int)(q % kWrStages);
+        if (!__all_sync(kFull, mbar_wait(&bars[s], (uint32_t)(q / kWrStages) & 1, P.err)))
             break;
-        const StageInfo si = info[s];
-        const int64_t t = si.t;
-        const int c = si.c;
-        const char *row = row_ptr<DT>(P, t);
         UnitRange R;
         R.lo = (int64_t)c * P.chunk;
         R.hi = min((int64_t)P.V, R.lo + P.chunk);
         R.vlo = R.lo;
         R.nvec = ((R.hi - R.lo) * ES) / 16;
         R.vhi = R.vlo + R.nvec * VEC;
-        const uint4 *stage = reinterpret_cast<const uint4 *>(ring + (size_t)s * kUnitBytes);
+        const uint4 *stage = reinterpret_cast<const uint4 *>(slots + (size_t)s * kUnitBytes);
         uint4 v[kVecPerLane];
 #pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) {
@@ -783,39 +752,37 @@ __global__ void __launch_bounds__(kTmaThreads, SPEC_TMA_MIN_BLOCKS) rowstats_tma
             v[k] = (vi < R.nvec) ? stage[vi] : neg_inf_vec<DT>();
         }
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[s]);  // the stage is in registers: hand it back at once
-        if (si.greedy)
+        if (lane == 0 && qi < n)
+            issue();  // the slot is in registers: refill it with the unit kWrStages ahead
+        if (t != info_t) {
+            info_t = t;
+            while (t >= r_end && r < P.B - 1) {
+                ++r;
+                r_end = (int64_t)__ldg(P.cu + r + 1) + r + 1;
+            }
+            const float temp = __ldg(P.temp + r);
+            greedy = force_argmax || !(temp > 0.f);
+            cs = greedy ? 0.f : kLog2e / temp;
+        }
+        const char *row = row_ptr<DT>(P, t);
+        if (greedy)
             argmax_regs<DT>(P, t, c, lane, v, R, row);
         else
-            softmax_regs<DT>(P, t, c, si.cs, lane, v, R, row);
+            softmax_regs<DT>(P, t, c, cs, lane, v, R, row);
+        if (++c == P.nchunks) {
+            c = 0;
+            ++t;
+        }
     }
+    // gave up on a wait: let this warp's copies still in flight land before exiting
+    if (lane == 0)
+        for (int64_t q2 = q + 1; q2 < qi; ++q2)
+            mbar_wait(&bars[q2 % kWrStages], (uint32_t)(q2 / kWrStages) & 1, P.err);
 }
 
 // ---------------------------------------------------------------------------------------
 // Chunk combines (used by K2 / K4)
 // ---------------------------------------------------------------------------------------
-
-// Sequential combine of one row's softmax partials by a single lane: M = max fl(m_c * c),
-// S = sum s_c 2^(fl(m_c * c) - M).
-__device__ __forceinline__ void lane_combine_soft(const Params &P, int64_t t, float cs, float &M, float &S)
-{
-    M = -INFINITY;
-    S = 0.f;
-    const float2 *pp = P.part + t * P.nchunks;
-    for (int c = 0; c < P.nchunks; ++c) {
-        const float2 pc = pp[c];
-        if (pc.x == -INFINITY)
-            continue;
-        const float Mc = pc.x * cs;
-        if (Mc > M) {
-            S = (M == -INFINITY) ? pc.y : S * ex2(M - Mc) + pc.y;
-            M = Mc;
-        } else {
-            S += pc.y * ex2(Mc - M);
-        }
-    }
-}
 
 __device__ __forceinline__ int lane_combine_argmax(const Params &P, int64_t t, float *best_out)
 {
@@ -1016,10 +983,7 @@ template <class F> __device__ __forceinline__ float warp_range_mass(const F &f, 
     return warp_sum(f.range(s0, s1));
 }
 
-struct ChunkMassFromArray {
-    const float *z;
-    __device__ __forceinline__ float operator()(int c) const { return z[c]; }
-};
+
 
 // Warp scan over the chunk masses: total Z, then the chunk holding u * Z and the
 // remaining threshold inside it.  Both passes use the same scan, so they agree bit for bit.
@@ -1079,8 +1043,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
     if (errbits & SPEC_DEVERR_LAYOUT) {
         if (lane == 0) {
             P.out_acc[r] = -1;
-            if (P.rstate)
+            if (P.rstate) {
                 P.rstate[r] = -1;
+                P.rcnt[r] = 0;
+            }
             if (P.dbg_z)
                 P.dbg_z[r] = 0.f;
         }
@@ -1100,8 +1066,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             P.out_tokens[tb + i] = -1;
         if (lane == 0) {
             P.out_acc[r] = -1;
-            if (P.rstate)
+            if (P.rstate) {
                 P.rstate[r] = -1;
+                P.rcnt[r] = 0;
+            }
             if (P.dbg_z)
                 P.dbg_z[r] = 0.f;
             atomicOr(P.err, too_long ? SPEC_DEVERR_SPEC_LEN : SPEC_DEVERR_DRAFT_ID);
@@ -1114,22 +1082,82 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
     const bool greedy = !(temp > 0.f);
     const float cs = greedy ? 0.f : kLog2e / temp;
 
+    // Gathers of draft row `lane` that only need x*: issued before the partial combine.
+    float ls = 0.f, qs = 1.f, ua = 0.f;
+    if (lane < k && !greedy) {
+        ls = load1<DT>(row_ptr<DT>(P, tb + lane), xs);
+        if (P.q)
+            qs = __ldg(P.q + (db + lane) * P.qstride + xs);
+        ua = P.uni[2 * (tb + lane)];
+    }
+
+    // Row statistics of the draft rows, eight rows at a time: lanes run over the chunk
+    // partials (coalesced, every load of the eight rows in flight together), then warp
+    // reductions; lane i keeps row i's result.
+    constexpr int G = 8;
+    int am = 0;
+    float Mi = -INFINITY, Si = 0.f;
+    for (int i0 = 0; i0 < k; i0 += G) {
+        float m[G], sv[G], best[G];
+        int idx[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            m[j] = -INFINITY;
+            sv[j] = 0.f;
+            best[j] = -INFINITY;
+            idx[j] = INT_MAX;
+        }
+        for (int c = lane; c < P.nchunks; c += 32) {
+            float2 pc[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                pc[j] = (i0 + j < k) ? P.part[(tb + i0 + j) * P.nchunks + c] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                if (greedy) {
+                    const int ci = __float_as_int(pc[j].y);
+                    if (pc[j].x > best[j] || (pc[j].x == best[j] && ci < idx[j])) {
+                        best[j] = pc[j].x;
+                        idx[j] = ci;
+                    }
+                } else if (pc[j].x != -INFINITY) {
+                    const float Mc = pc[j].x * cs;
+                    if (Mc > m[j]) {
+                        sv[j] = (m[j] == -INFINITY) ? pc[j].y : sv[j] * ex2(m[j] - Mc) + pc[j].y;
+                        m[j] = Mc;
+                    } else {
+                        sv[j] += pc[j].y * ex2(Mc - m[j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            if (greedy) {
+                warp_argmax(best[j], idx[j]);
+                if (lane == i0 + j)
+                    am = idx[j] == INT_MAX ? 0 : idx[j];
+            } else {
+                const float mw = warp_max(m[j]);
+                const float sw = warp_sum(m[j] == -INFINITY ? 0.f : sv[j] * ex2(m[j] - mw));
+                if (lane == i0 + j) {
+                    Mi = mw;
+                    Si = sw;
+                }
+            }
+        }
+    }
+
     // Acceptance decision of draft row `lane`.
     bool accept = true;
-    int am = 0;
-    float Mi = -INFINITY, Si = 0.f, wstar = 0.f;
+    float wstar = 0.f;
     if (lane < k) {
-        const int64_t t = tb + lane;
         if (greedy) {
-            am = lane_combine_argmax(P, t, nullptr);
             accept = (xs == am);
         } else {
-            lane_combine_soft(P, t, cs, Mi, Si);  // every token, x* included
-            const float e = fmaf(load1<DT>(row_ptr<DT>(P, t), xs), cs, -Mi);
+            const float e = fmaf(ls, cs, -Mi);  // x* is in Si
             wstar = ex2(e);
-            const float qs = P.q ? __ldg(P.q + (db + lane) * P.qstride + xs) : 1.f;
-            const float us = P.uni[2 * t];
-            const double lhs = (double)us * (double)qs;  // exact
+            const double lhs = (double)ua * (double)qs;  // exact
             const float ps = wstar / Si;
             if (ps > 1e-30f)
                 accept = lhs < (double)ps;
@@ -1195,8 +1223,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
     }
     if (lane == 0) {
         P.out_acc[r] = j;
-        if (P.rstate)
+        if (P.rstate) {
             P.rstate[r] = pending ? j : -1;
+            P.rcnt[r] = 0;
+        }
         if (P.dbg_z && !pending)
             P.dbg_z[r] = zdbg;
     }
@@ -1208,11 +1238,53 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 }
 
 // ---------------------------------------------------------------------------------------
-// K3: explicit-q residual chunk masses for rejecting requests
+// K3: explicit-q recovery, one block per request that rejected a draft
 // ---------------------------------------------------------------------------------------
 
+// Residual mass sum max(0, p(v) - q(v)) over the chunk [lo, hi) by one warp: lane-strided
+// 16-byte groups of target logits and draft probabilities, four groups in flight per lane.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) residual_kernel(Params P)
+__device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT> &f, int64_t lo, int64_t hi, int lane)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    constexpr int ES = Elem<DT>::kSize;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int64_t tail = lo;
+    if (((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo)) & 15) == 0) {
+        const int64_t ng = (hi - lo) / VEC;
+#pragma unroll 4
+        for (int64_t g = lane; g < ng; g += 32) {
+            const int64_t v = lo + g * VEC;
+            float x[VEC];
+            unpack<DT>(ld_stream(f.row + v * ES), x);
+#pragma unroll
+            for (int h = 0; h < VEC / 4; ++h) {
+                const uint4 qw = ld_stream(f.qrow + v + 4 * h);
+                acc[0] += fmaxf(0.f, ex2(fmaf(x[4 * h + 0], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.x));
+                acc[1] += fmaxf(0.f, ex2(fmaf(x[4 * h + 1], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.y));
+                acc[2] += fmaxf(0.f, ex2(fmaf(x[4 * h + 2], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.z));
+                acc[3] += fmaxf(0.f, ex2(fmaf(x[4 * h + 3], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.w));
+            }
+        }
+        tail = lo + ng * VEC;
+    }
+    for (int64_t v = tail + lane; v < hi; v += 32)
+        acc[0] += f.one(v);
+    return warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+}
+
+
+struct ChunkMassFromL2 {  // masses written by other warps of this launch: read past L1
+    const float *z;
+    __device__ __forceinline__ float operator()(int c) const { return __ldcg(z + c); }
+};
+
+// Warps own contiguous ranges of (request, chunk) units; each unit's residual mass goes to
+// rpart.  The warp that completes a request's last chunk (a per-request counter, zeroed by
+// K2 in this same call) draws the recovered token from the chunk masses: chunk scan and
+// warp descent as in K2.  No warp waits for another.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nunits = (int64_t)P.B * P.nchunks;
@@ -1232,61 +1304,41 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(Params P)
         const int64_t d = (int64_t)cu0 + j;
         const float2 st = P.rstat[r];
         const float cs = kLog2e / P.temp[r];
-        ResidualMass<DT> f{row_ptr<DT>(P, t), P.q + d * P.qstride, cs, st.x, 1.f / st.y};
-        const int64_t lo = (int64_t)c * P.chunk;
-        const int64_t hi = min((int64_t)P.V, lo + P.chunk);
-        // lane-strided 8-element groups keep the loads coalesced
-        float s = 0.f;
-        const int64_t n8 = (hi - lo + 7) / 8;
-        for (int64_t g = lane; g < n8; g += 32)
-            s += f.range(lo + g * 8, min(hi, lo + g * 8 + 8));
-        s = warp_sum(s);
-        if (lane == 0)
-            P.rpart[(int64_t)r * P.nchunks + c] = s;
-    }
-}
-
-// ---------------------------------------------------------------------------------------
-// K4: explicit-q recovered token
-// ---------------------------------------------------------------------------------------
-
-template <int DT>
-__global__ void __launch_bounds__(kThreads) recover_kernel(Params P)
-{
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (r >= P.B)
-        return;
-    const int j = P.rstate[r];
-    if (j < 0)
-        return;
-    const int cu0 = P.cu[r];
-    const int64_t t = (int64_t)cu0 + r + j;
-    const int64_t d = (int64_t)cu0 + j;
-    const float2 st = P.rstat[r];
-    const float cs = kLog2e / P.temp[r];
-    const float us = P.uni[2 * t + 1];
-    const char *row = row_ptr<DT>(P, t);
-    ChunkMassFromArray cmz{P.rpart + (int64_t)r * P.nchunks};
-    const float Z = chunk_total(cmz, P.nchunks, lane);
-    int token;
-    if (Z > 0.f) {
-        float th;
-        const int c = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
-        ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y};
-        token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
-    } else {  // empty residual: draw from p itself
-        ChunkMassFromPartials cm{P.part + t * P.nchunks, cs, st.x, -1, 0.f};
-        const float Zp = chunk_total(cm, P.nchunks, lane);
-        float th;
-        const int c = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
-        TargetMass<DT> f{row, cs, st.x, -1};
-        token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
-    }
-    if (lane == 0) {
-        P.out_tokens[t] = token;
-        if (P.dbg_z)
-            P.dbg_z[r] = Z > 0.f ? Z : 0.f;
+        const char *row = row_ptr<DT>(P, t);
+        const ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y};
+        const float z = warp_residual_chunk(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk),
+                                            lane);
+        int last = 0;
+        if (lane == 0) {
+            P.rpart[(int64_t)r * P.nchunks + c] = z;
+            __threadfence();  // the mass is visible before the count says so
+            last = atomicAdd(P.rcnt + r, 1) == P.nchunks - 1;
+        }
+        if (!__shfl_sync(kFull, last, 0))
+            continue;
+        __threadfence();
+        const float us = P.uni[2 * t + 1];
+        const ChunkMassFromL2 cmz{P.rpart + (int64_t)r * P.nchunks};
+        const float Z = chunk_total(cmz, P.nchunks, lane);
+        int token;
+        if (Z > 0.f) {
+            float th;
+            const int cc = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
+            token = (int)warp_find(f, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
+        } else {  // empty residual: draw from p itself
+            const ChunkMassFromPartials cm{P.part + t * P.nchunks, cs, st.x, -1, 0.f};
+            const float Zp = chunk_total(cm, P.nchunks, lane);
+            float th;
+            const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
+            const TargetMass<DT> ft{row, cs, st.x, -1};
+            token = (int)warp_find(ft, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th,
+                                   lane);
+        }
+        if (lane == 0) {
+            P.out_tokens[t] = token;
+            if (P.dbg_z)
+                P.dbg_z[r] = Z > 0.f ? Z : 0.f;
+        }
     }
 }
 
@@ -1356,10 +1408,10 @@ struct DeviceInfo {
     int sms = 0;
     int blocks_rowstats[2] = {0, 0};
     int blocks_residual[2] = {0, 0};
-    int blocks_tma[2] = {0, 0};
+    int blocks_wr[2] = {0, 0};
 };
 
-constexpr size_t kTmaSmem = (size_t)kTmaStages * kUnitBytes;
+constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];  // per-device launch-shape cache (SM count, occupancy)
@@ -1369,10 +1421,10 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
     cudaError_t e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_rowstats[DT], rowstats_kernel<DT>, kThreads, 0)))
         return e;
-    if ((e = cudaFuncSetAttribute(rowstats_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem)))
+    if ((e = cudaFuncSetAttribute(rowstats_wr_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWrSmem)))
         return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_tma[DT], rowstats_tma_kernel<DT>, kTmaThreads,
-                                                           kTmaSmem)))
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
+                                                           kWrSmem)))
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT>, kThreads, 0);
 }
@@ -1439,13 +1491,14 @@ void launch_rowstats(int DT, const Params &P, const DeviceInfo &di, int64_t T, i
 {
     const size_t es = DT ? 2 : 4;
     const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * es) % 16 == 0;
-    if (rows_aligned && di.blocks_tma[DT] > 0) {
+    if (rows_aligned && di.blocks_wr[DT] > 0) {
         const int64_t units = T * (int64_t)nchunks;
-        const int grid = (int)clamp_grid((int64_t)di.sms * di.blocks_tma[DT], (units + 3) / 4);
+        const int64_t warps_needed = (units + 3) / 4;  // at least ~4 units per warp
+        const int grid = (int)clamp_grid((int64_t)di.sms * di.blocks_wr[DT], (warps_needed + kWrWarps - 1) / kWrWarps);
         if (DT)
-            rowstats_tma_kernel<1><<<grid, kTmaThreads, kTmaSmem, stream>>>(P, force_argmax);
+            rowstats_wr_kernel<1><<<grid, kWrThreads, kWrSmem, stream>>>(P, force_argmax);
         else
-            rowstats_tma_kernel<0><<<grid, kTmaThreads, kTmaSmem, stream>>>(P, force_argmax);
+            rowstats_wr_kernel<0><<<grid, kWrThreads, kWrSmem, stream>>>(P, force_argmax);
     } else {
         if (DT)
             rowstats_kernel<1><<<gridA, kThreads, 0, stream>>>(P, force_argmax);
@@ -1492,6 +1545,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     P.rstate = q ? reinterpret_cast<int32_t *>(base + pl.off_rstate) : nullptr;
     P.rstat = reinterpret_cast<float2 *>(base + pl.off_rstat);
     P.rpart = q ? reinterpret_cast<float *>(base + pl.off_rpart) : nullptr;
+    P.rcnt = q ? reinterpret_cast<int32_t *>(base + pl.off_rcnt) : nullptr;
     P.chunk = pl.chunk;
     P.nchunks = pl.nchunks;
     P.dbg_pdraft = dbg_pd;
@@ -1504,7 +1558,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     const int gridB = (int)((B + kWarps - 1) / kWarps);
     const bool debug = dbg_m || dbg_s || dbg_am || dbg_pd || dbg_z;
 
-    // stage events: [0] before K1, [1] after K1, [2] after K2, [3] after K3, [4] after K4
+    // stage events: [0] before K1, [1] after K1, [2] after K2, [3] after K3
     int evi = 0;
     auto mark = [&]() {
         if (evi < nev && ev[evi])
@@ -1535,11 +1589,6 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 residual_kernel<1><<<gridC, kThreads, 0, stream>>>(P);
             else
                 residual_kernel<0><<<gridC, kThreads, 0, stream>>>(P);
-            mark();
-            if (DT)
-                recover_kernel<1><<<gridB, kThreads, 0, stream>>>(P);
-            else
-                recover_kernel<0><<<gridB, kThreads, 0, stream>>>(P);
             mark();
         }
     }
@@ -1771,6 +1820,6 @@ const char *spec_reject_status_string(spec_status status)
 
 int spec_reject_version(void) { return 100; }
 
-int spec_reject_num_kernels(int has_draft_probs) { return has_draft_probs ? 4 : 2; }
+int spec_reject_num_kernels(int has_draft_probs) { return has_draft_probs ? 3 : 2; }
 
 }  // extern "C"
