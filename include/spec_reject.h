@@ -199,6 +199,53 @@ spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype log
                                        const float *uniforms, const float *temperature, int32_t *out_tokens,
                                        int32_t *out_num_accepted, int32_t *device_error_word, void *stream);
 
+/*
+ * Acceptance counters, cumulative across calls (the caller zeroes `counters` once):
+ * the spec_decode_num_drafts / num_draft_tokens / num_accepted_tokens /
+ * num_accepted_tokens_per_pos counters of "第12章 投机解码：以小博大" §12.7.5, and the verify
+ * count that "投机解码（Speculative Decoding）端到端深挖" §13 divides by:
+ *   accept rate   alpha = counters[NUM_ACCEPTED_TOKENS] / counters[NUM_DRAFT_TOKENS]
+ *   accept length tau   = (counters[NUM_ACCEPTED_TOKENS] + counters[NUM_VERIFIES]) / counters[NUM_VERIFIES]
+ * (the bonus or recovered token counts in tau, not in alpha).
+ *
+ *   cu_num_draft, out_num_accepted  device int32 [B + 1] and [B] of a spec_reject_sample() call
+ *   counters                        device int64 [SPEC_METRIC_COUNT], 8-byte aligned
+ *
+ * Requests reported invalid (out_num_accepted = -1) are not counted.  Asynchronous on
+ * `stream`; integer sums, so the result is independent of scheduling.
+ */
+#define SPEC_METRIC_NUM_DRAFTS 0          /* requests with at least one draft */
+#define SPEC_METRIC_NUM_DRAFT_TOKENS 1    /* sum of k_r */
+#define SPEC_METRIC_NUM_ACCEPTED_TOKENS 2 /* sum of accepted drafts */
+#define SPEC_METRIC_NUM_VERIFIES 3        /* requests verified (each emits accepted + 1 tokens) */
+#define SPEC_METRIC_ACCEPTED_PER_POS 4    /* [4 + i]: requests whose draft at position i was accepted */
+#define SPEC_METRIC_COUNT (4 + SPEC_REJECT_MAX_SPEC_LEN)
+spec_status spec_reject_metrics_update(const int32_t *cu_num_draft, const int32_t *out_num_accepted, int32_t B,
+                                       int64_t *counters, void *stream);
+
+/*
+ * n-gram (prompt-lookup) draft proposer, "第12章 投机解码：以小博大" §12.4.4: for each
+ * request, for n = max_n down to min_n, the last n context tokens are searched for their
+ * leftmost earlier occurrence (one that ends before the final n tokens); the first n that
+ * matches wins and the tokens that follow the occurrence are proposed, at most
+ * min(k, max_model_len - L) of them (fewer when the context ends first).  No match, or a
+ * context that already reaches max_model_len, proposes nothing.
+ *
+ *   tokens          device int32, all contexts back to back
+ *   cu_tokens       device int64 [B + 1]: context r is tokens[cu[r] .. cu[r+1])
+ *   min_n, max_n    1 <= min_n <= max_n <= SPEC_NGRAM_MAX_N
+ *   k               1 <= k <= 32 (MAX_SPEC_LEN)
+ *   max_model_len   <= 0 for no limit
+ *   out_drafts      device int32 [B, k], -1 padded
+ *   out_num_drafts  device int32 [B]
+ * Asynchronous on `stream`; the page runs this search on the CPU with KMP, here every
+ * candidate start is tested in parallel by one thread block per request.
+ */
+#define SPEC_NGRAM_MAX_N 64
+spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, int32_t B, int32_t min_n,
+                               int32_t max_n, int32_t k, int64_t max_model_len, int32_t *out_drafts,
+                               int32_t *out_num_drafts, void *stream);
+
 /* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 3 with). */
 int spec_reject_num_kernels(int has_draft_probs);
 

@@ -55,3 +55,33 @@ def accept_length(completion_tokens: int, verify_count: int) -> float:
 def tokens_advanced(num_accepted: int) -> int:
     """Position advance of one step: accepted drafts + 1 ("以小博大" §12.3.4; "投机解码端到端深挖" §8.1)."""
     return num_accepted + 1
+
+
+def acceptance_counters(cu_num_draft, num_accepted, max_spec_len: int = 32) -> list[int]:
+    """Acceptance counters of one batch, by plain loops.
+
+    [0] requests that drafted at least one token (vLLM spec_decode_num_drafts),
+    [1] draft tokens proposed (num_draft_tokens), [2] drafts accepted (num_accepted_tokens),
+    [3] verify steps (one per request), [4 + i] requests whose draft at position i was
+    accepted (num_accepted_tokens_per_pos).  "第12章 投机解码：以小博大" §12.7.5 names the
+    counters; "投机解码端到端深挖" §13 defines alpha and tau from them.  Requests reported
+    invalid (accepted = -1) are skipped.
+    """
+    c = [0] * (4 + max_spec_len)
+    for r in range(len(num_accepted)):
+        a = int(num_accepted[r])
+        if a < 0:
+            continue
+        k = int(cu_num_draft[r + 1]) - int(cu_num_draft[r])
+        c[0] += 1 if k > 0 else 0
+        c[1] += k
+        c[2] += a
+        c[3] += 1
+        for i in range(min(a, max_spec_len)):
+            c[4 + i] += 1
+    return c
+
+
+def rate_and_length(counters) -> tuple[float, float]:
+    """alpha = accepted / proposed; tau = (accepted + verifies) / verifies (the bonus counts in tau)."""
+    return accept_rate(counters[2], counters[1]), accept_length(counters[2] + counters[3], counters[3])

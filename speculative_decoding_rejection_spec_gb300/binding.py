@@ -24,8 +24,11 @@ EXPORTED = [
     "spec_reject_workspace_size", "spec_reject_sample", "spec_reject_last_device_error",
     "spec_reject_host_arena_size", "spec_reject_sample_host", "spec_reject_debug_rowstats",
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
-    "spec_reject_sample_noalloc",
+    "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
 ]
+METRIC_NUM_DRAFTS, METRIC_NUM_DRAFT_TOKENS, METRIC_NUM_ACCEPTED_TOKENS, METRIC_NUM_VERIFIES = 0, 1, 2, 3
+METRIC_ACCEPTED_PER_POS = 4
+METRIC_COUNT = 4 + MAX_SPEC_LEN
 
 _lib = None
 
@@ -66,6 +69,10 @@ def load():
     lib.spec_reject_sample_profiled.argtypes = sample_args + [P, ctypes.c_int]
     lib.spec_reject_sample_noalloc.restype = ctypes.c_int
     lib.spec_reject_sample_noalloc.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, P]
+    lib.spec_reject_metrics_update.restype = ctypes.c_int
+    lib.spec_reject_metrics_update.argtypes = [P, P, i32, P, P]
+    lib.spec_ngram_propose.restype = ctypes.c_int
+    lib.spec_ngram_propose.argtypes = [P, P, i32, i32, i32, i32, i64, P, P, P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int]
     _lib = lib
@@ -218,6 +225,39 @@ def sample_noalloc(target_logits, draft_ids, cu_num_draft, uniforms, temperature
     if st != 0:
         raise SpecRejectError(st, "spec_reject_sample_noalloc")
     return out_tokens, out_num_accepted
+
+
+def metrics_update(cu_num_draft, out_num_accepted, counters, stream=None):
+    """Accumulate one call's acceptance counters into ``counters`` (device int64 [METRIC_COUNT])."""
+    B = int(cu_num_draft.shape[0]) - 1
+    st = load().spec_reject_metrics_update(_ptr(cu_num_draft), _ptr(out_num_accepted), B, _ptr(counters),
+                                           _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_metrics_update")
+    return counters
+
+
+def accept_rate_and_length(counters) -> tuple[float, float]:
+    """(alpha, tau) from accumulated counters (host copy)."""
+    c = [int(x) for x in counters]
+    return (c[METRIC_NUM_ACCEPTED_TOKENS] / max(c[METRIC_NUM_DRAFT_TOKENS], 1),
+            (c[METRIC_NUM_ACCEPTED_TOKENS] + c[METRIC_NUM_VERIFIES]) / max(c[METRIC_NUM_VERIFIES], 1))
+
+
+def ngram_propose(tokens, cu_tokens, min_n: int, max_n: int, k: int, max_model_len: int = 0, stream=None):
+    """n-gram draft proposals for a batch of contexts (device int32 tokens, int64 offsets [B + 1]).
+
+    Returns (drafts int32 [B, k] padded with -1, counts int32 [B]).
+    """
+    import torch
+    B = int(cu_tokens.shape[0]) - 1
+    out = torch.empty((B, k), dtype=torch.int32, device=tokens.device)
+    num = torch.empty(B, dtype=torch.int32, device=tokens.device)
+    st = load().spec_ngram_propose(_ptr(tokens), _ptr(cu_tokens), B, int(min_n), int(max_n), int(k),
+                                   int(max_model_len), _ptr(out), _ptr(num), _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_ngram_propose")
+    return out, num
 
 
 def num_kernels(has_draft_probs: bool) -> int:

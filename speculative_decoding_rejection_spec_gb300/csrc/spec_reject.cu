@@ -1343,6 +1343,96 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
 }
 
 // ---------------------------------------------------------------------------------------
+// Acceptance counters (vLLM's spec_decode_* counters, SGLang's accept rate / length)
+// ---------------------------------------------------------------------------------------
+
+// counters[SPEC_METRIC_*] += this batch's contributions; requests reported invalid (-1)
+// are left out.  Integer sums: the result does not depend on the order of the atomics.
+__global__ void __launch_bounds__(kThreads) metrics_kernel(const int32_t *cu, const int32_t *acc, int32_t B,
+                                                           unsigned long long *counters)
+{
+    __shared__ unsigned long long s_cnt[SPEC_METRIC_COUNT];
+    for (int i = threadIdx.x; i < SPEC_METRIC_COUNT; i += blockDim.x)
+        s_cnt[i] = 0;
+    __syncthreads();
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < B; r += gridDim.x * blockDim.x) {
+        const int a = acc[r];
+        if (a < 0)
+            continue;
+        const int k = cu[r + 1] - cu[r];
+        if (k > 0)
+            atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFTS], 1ull);
+        atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFT_TOKENS], (unsigned long long)k);
+        atomicAdd(&s_cnt[SPEC_METRIC_NUM_ACCEPTED_TOKENS], (unsigned long long)a);
+        atomicAdd(&s_cnt[SPEC_METRIC_NUM_VERIFIES], 1ull);
+        for (int i = 0; i < a && i < SPEC_REJECT_MAX_SPEC_LEN; ++i)
+            atomicAdd(&s_cnt[SPEC_METRIC_ACCEPTED_PER_POS + i], 1ull);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < SPEC_METRIC_COUNT; i += blockDim.x)
+        if (s_cnt[i])
+            atomicAdd(counters + i, s_cnt[i]);
+}
+
+// ---------------------------------------------------------------------------------------
+// n-gram draft proposer ("第12章 投机解码：以小博大" §12.4.4)
+// ---------------------------------------------------------------------------------------
+
+// One block per request.  For n = max_n .. min_n, the block's threads test candidate
+// starts s in ascending blocks of blockDim.x positions (every s in [0, L - 2n], so the
+// occurrence lies wholly before the final n tokens); the first block of candidates with a
+// hit gives the leftmost occurrence.  The proposal is the (at most k) tokens after it.
+__global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int64_t *cu, int32_t B,
+                                                         int min_n, int max_n, int k, int64_t max_model_len,
+                                                         int32_t *out, int32_t *out_num)
+{
+    __shared__ int32_t pat[SPEC_NGRAM_MAX_N];
+    __shared__ int s_first;
+    for (int r = blockIdx.x; r < B; r += gridDim.x) {
+        const int64_t c0 = cu[r];
+        const int64_t L = cu[r + 1] - c0;
+        const int32_t *ctx = tokens + c0;
+        int64_t kk = k;
+        if (max_model_len > 0)
+            kk = min(kk, max_model_len - L);
+        int64_t found = -1;
+        int found_n = 0;
+        for (int n = max_n; kk > 0 && n >= min_n && found < 0; --n) {
+            if (n <= 0 || 2 * (int64_t)n > L)
+                continue;
+            __syncthreads();  // pat of the previous n is no longer read
+            if (threadIdx.x < n)
+                pat[threadIdx.x] = ctx[L - n + threadIdx.x];
+            __syncthreads();
+            const int64_t last = L - 2 * (int64_t)n;
+            for (int64_t s0 = 0; s0 <= last; s0 += blockDim.x) {
+                const int64_t st = s0 + threadIdx.x;
+                bool hit = st <= last;
+                for (int i = 0; hit && i < n; ++i)
+                    hit = ctx[st + i] == pat[i];
+                if (__syncthreads_or(hit)) {  // uniform: every thread takes this branch
+                    if (threadIdx.x == 0)
+                        s_first = INT_MAX;
+                    __syncthreads();
+                    if (hit)
+                        atomicMin(&s_first, (int)threadIdx.x);
+                    __syncthreads();
+                    found = s0 + s_first;
+                    found_n = n;
+                    break;
+                }
+            }
+        }
+        const int cnt = found < 0 ? 0 : (int)min(kk, L - (found + found_n));
+        for (int i = threadIdx.x; i < k; i += blockDim.x)
+            out[(int64_t)r * k + i] = i < cnt ? ctx[found + found_n + i] : -1;
+        if (threadIdx.x == 0)
+            out_num[r] = cnt;
+        __syncthreads();  // s_first / pat are reused by this block's next request
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // Diagnostics: per-row statistics from K1's partials
 // ---------------------------------------------------------------------------------------
 
@@ -1802,6 +1892,43 @@ spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype log
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return SPEC_OK;
+}
+
+spec_status spec_reject_metrics_update(const int32_t *cu_num_draft, const int32_t *out_num_accepted, int32_t B,
+                                       int64_t *counters, void *stream)
+{
+    if (B < 0 || !counters || (B > 0 && (!cu_num_draft || !out_num_accepted)) || !aligned(counters, 8) ||
+        !aligned(cu_num_draft, 4) || !aligned(out_num_accepted, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if (B == 0)
+        return SPEC_OK;
+    DeviceInfo *di;
+    if (device_info(&di) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    const int grid = (int)clamp_grid(di->sms, (B + kThreads - 1) / kThreads);
+    metrics_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        cu_num_draft, out_num_accepted, B, reinterpret_cast<unsigned long long *>(counters));
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, int32_t B, int32_t min_n,
+                               int32_t max_n, int32_t k, int64_t max_model_len, int32_t *out_drafts,
+                               int32_t *out_num_drafts, void *stream)
+{
+    if (B < 0 || min_n < 1 || max_n < min_n || max_n > SPEC_NGRAM_MAX_N || k < 1 || k > SPEC_REJECT_MAX_SPEC_LEN)
+        return SPEC_ERR_INVALID_ARG;
+    if (B == 0)
+        return SPEC_OK;
+    if (!tokens || !cu_tokens || !out_drafts || !out_num_drafts || !aligned(tokens, 4) || !aligned(cu_tokens, 8) ||
+        !aligned(out_drafts, 4) || !aligned(out_num_drafts, 4))
+        return SPEC_ERR_INVALID_ARG;
+    DeviceInfo *di;
+    if (device_info(&di) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    const int grid = (int)clamp_grid((int64_t)di->sms * 8, B);
+    ngram_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tokens, cu_tokens, B, min_n, max_n, k,
+                                                                            max_model_len, out_drafts, out_num_drafts);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 const char *spec_reject_status_string(spec_status status)

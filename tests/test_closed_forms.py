@@ -55,3 +55,24 @@ def test_rollback_arithmetic(golden_dir):
     g = _load(golden_dir, "rollback.json")
     for c in g["cases"]:
         assert cf.tokens_advanced(c["num_accepted"]) == c["advance"]
+
+
+def test_acceptance_counters_reproduce_metrics_example(golden_dir):
+    """Ten verify steps of K=4 drafts with 25 accepted give alpha 0.625 and tau 3.5."""
+    g = _load(golden_dir, "metrics_example.json")
+    acc = [4, 4, 4, 3, 3, 2, 2, 2, 1, 0]
+    assert sum(acc) == g["accepted"] and len(acc) == g["verify_count"]
+    cu = [g["drafts_per_step"] * i for i in range(len(acc) + 1)]
+    c = cf.acceptance_counters(cu, acc)
+    alpha, tau = cf.rate_and_length(c)
+    assert alpha == pytest.approx(g["accept_rate"]) and tau == pytest.approx(g["accept_length"])
+    assert c[2] + c[3] == g["completion_tokens"]
+    # per-position counts: position i is accepted in every request that accepted more than i drafts
+    assert c[4:8] == [9, 8, 5, 3] and c[0] == 10
+
+
+def test_acceptance_counters_skip_invalid_and_count_zero_draft_requests():
+    # k = 0, 3, 2, 6; request 0 verifies without drafting, request 2 is invalid
+    c = cf.acceptance_counters([0, 0, 3, 5, 11], [0, 2, -1, 4])
+    assert c[:4] == [2, 9, 6, 3]
+    assert c[4:9] == [2, 2, 1, 1, 0]
