@@ -73,6 +73,7 @@ typedef enum spec_dtype { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 #define SPEC_DEVERR_SPEC_LEN 2   /* some k_r > 32 */
 #define SPEC_DEVERR_DRAFT_ID 4   /* some draft id outside [0, V) */
 #define SPEC_DEVERR_TIMEOUT 8    /* a bounded wait inside a kernel gave up (results invalid) */
+#define SPEC_DEVERR_TREE 16      /* tree verification: a malformed tree (see spec_tree_verify_greedy) */
 
 /*
  * Bytes of device workspace spec_reject_sample() needs for a batch of B
@@ -222,6 +223,33 @@ spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype log
 #define SPEC_METRIC_COUNT (4 + SPEC_REJECT_MAX_SPEC_LEN)
 spec_status spec_reject_metrics_update(const int32_t *cu_num_draft, const int32_t *out_num_accepted, int32_t B,
                                        int64_t *counters, void *stream);
+
+/*
+ * Greedy tree verification, "投机解码（Speculative Decoding）端到端深挖" §6.2 and §7.1 (draft
+ * trees with several siblings per depth, temperature 0).  Request r's nodes are
+ * cu_nodes[r] .. cu_nodes[r+1] - 1 (local index i = node - cu_nodes[r]); node 0 is the root
+ * (the last verified token), every other node i has parent[node] in [0, i) and draft token
+ * node_tokens[node].  target_logits row `node` holds the target's logits for the token after
+ * that node's prefix.  From the root: take the lowest-index argmax of the current node's row;
+ * the lowest-index child carrying that token is accepted and becomes the current node;
+ * otherwise stop.  The argmax at the last accepted node is the bonus token.
+ *
+ *   target_logits     device [N, V] (fp32 / bf16, rows logits_row_stride apart, stride >= V or 0)
+ *   parent            device int32 [N] (-1 at each root)
+ *   node_tokens       device int32 [N] (ignored at roots)
+ *   cu_nodes          device int32 [B + 1], cu_nodes[B] = N
+ *   out_tokens        device int32 [N]: per request, the accepted tokens then the bonus, -1 after
+ *   out_num_accepted  device int32 [B] (-1 for a malformed tree)
+ *   out_last_node     device int32 [B]: local index of the last accepted node (0 = root)
+ *   workspace         spec_tree_workspace_size(N, B, V, dtype) bytes (contents need no setup)
+ * Malformed trees set SPEC_DEVERR_TREE in the error word (spec_reject_last_device_error).
+ */
+size_t spec_tree_workspace_size(int64_t N, int32_t B, int32_t V, spec_dtype logits_dtype);
+spec_status spec_tree_verify_greedy(const void *target_logits, spec_dtype logits_dtype, int64_t N, int32_t V,
+                                    int64_t logits_row_stride, const int32_t *parent, const int32_t *node_tokens,
+                                    const int32_t *cu_nodes, int32_t B, int32_t *out_tokens,
+                                    int32_t *out_num_accepted, int32_t *out_last_node, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /*
  * n-gram (prompt-lookup) draft proposer, "第12章 投机解码：以小博大" §12.4.4: for each

@@ -18,13 +18,14 @@ LIBRARY = os.path.join(_HERE, "libspecreject.so")
 
 F32, BF16 = 0, 1
 MAX_SPEC_LEN = 32
-DEVERR_LAYOUT, DEVERR_SPEC_LEN, DEVERR_DRAFT_ID = 1, 2, 4
+DEVERR_LAYOUT, DEVERR_SPEC_LEN, DEVERR_DRAFT_ID, DEVERR_TIMEOUT, DEVERR_TREE = 1, 2, 4, 8, 16
 
 EXPORTED = [
     "spec_reject_workspace_size", "spec_reject_sample", "spec_reject_last_device_error",
     "spec_reject_host_arena_size", "spec_reject_sample_host", "spec_reject_debug_rowstats",
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
     "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
+    "spec_tree_workspace_size", "spec_tree_verify_greedy",
 ]
 METRIC_NUM_DRAFTS, METRIC_NUM_DRAFT_TOKENS, METRIC_NUM_ACCEPTED_TOKENS, METRIC_NUM_VERIFIES = 0, 1, 2, 3
 METRIC_ACCEPTED_PER_POS = 4
@@ -73,6 +74,10 @@ def load():
     lib.spec_reject_metrics_update.argtypes = [P, P, i32, P, P]
     lib.spec_ngram_propose.restype = ctypes.c_int
     lib.spec_ngram_propose.argtypes = [P, P, i32, i32, i32, i32, i64, P, P, P]
+    lib.spec_tree_workspace_size.restype = sz
+    lib.spec_tree_workspace_size.argtypes = [i64, i32, i32, ctypes.c_int]
+    lib.spec_tree_verify_greedy.restype = ctypes.c_int
+    lib.spec_tree_verify_greedy.argtypes = [P, ctypes.c_int, i64, i32, i64, P, P, P, i32, P, P, P, P, sz, P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int]
     _lib = lib
@@ -258,6 +263,31 @@ def ngram_propose(tokens, cu_tokens, min_n: int, max_n: int, k: int, max_model_l
     if st != 0:
         raise SpecRejectError(st, "spec_ngram_propose")
     return out, num
+
+
+def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None):
+    """Greedy tree verification on device tensors.
+
+    Returns (out_tokens [N], out_num_accepted [B], out_last_node [B], workspace).
+    """
+    import torch
+    N, V = int(target_logits.shape[0]), int(target_logits.shape[1])
+    B = int(cu_nodes.shape[0]) - 1
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    n_ws = load().spec_tree_workspace_size(N, B, V, dt)
+    if n_ws == 0:
+        raise ValueError("invalid sizes for spec_tree_workspace_size")
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+    out = torch.empty(N, dtype=torch.int32, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    last = torch.empty(B, dtype=torch.int32, device=dev)
+    st = load().spec_tree_verify_greedy(_ptr(target_logits), dt, N, V, _row_stride(target_logits), _ptr(parent),
+                                        _ptr(node_tokens), _ptr(cu_nodes), B, _ptr(out), _ptr(acc), _ptr(last),
+                                        _ptr(ws), n_ws, _stream(stream))
+    if st != 0:
+        raise SpecRejectError(st, "spec_tree_verify_greedy")
+    return out, acc, last, ws
 
 
 def num_kernels(has_draft_probs: bool) -> int:

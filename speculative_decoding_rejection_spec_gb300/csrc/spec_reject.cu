@@ -1375,6 +1375,71 @@ __global__ void __launch_bounds__(kThreads) metrics_kernel(const int32_t *cu, co
 }
 
 // ---------------------------------------------------------------------------------------
+// Greedy tree verification ("投机解码（Speculative Decoding）端到端深挖" §6.2, §7.1)
+// ---------------------------------------------------------------------------------------
+
+// One warp per tree.  K1 has left per-chunk (max, argmax) partials for every node row.
+// From the root: argmax at the current node; the lowest-index child carrying that token is
+// accepted and becomes the current node; otherwise the walk stops and the argmax is the
+// bonus.  Invalid trees (node 0 not a root, a parent not preceding its child, a token
+// outside the vocabulary) report -1.
+__global__ void __launch_bounds__(kThreads) tree_walk_kernel(Params P, const int32_t *parent, const int32_t *tok,
+                                                             const int32_t *cu_nodes, int32_t B, int32_t *out_tokens,
+                                                             int32_t *out_acc, int32_t *out_last)
+{
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (r >= B)
+        return;
+    const int n0 = cu_nodes[r];
+    const int n = cu_nodes[r + 1] - n0;
+    bool bad = n < 1 || n0 < 0 || (int64_t)n0 + n > P.T;
+    if (!bad) {
+        bool lbad = false;
+        for (int i = lane; i < n; i += 32) {
+            const int pi = parent[n0 + i];
+            lbad |= (i == 0) ? pi != -1 : (pi < 0 || pi >= i || tok[n0 + i] < 0 || tok[n0 + i] >= P.V);
+        }
+        bad = __any_sync(kFull, lbad);
+    }
+    if (bad) {
+        if (n >= 1 && n0 >= 0 && (int64_t)n0 + n <= P.T)
+            for (int i = lane; i < n; i += 32)
+                out_tokens[n0 + i] = -1;
+        if (lane == 0) {
+            out_acc[r] = -1;
+            out_last[r] = -1;
+            atomicOr(P.err, SPEC_DEVERR_TREE);
+            atomicMin(P.err + 1, r);
+        }
+        return;
+    }
+    int cur = 0, acc = 0;
+    for (int step = 0; step < n; ++step) {
+        const int am = warp_combine_argmax(P, (int64_t)n0 + cur, lane);
+        int child = INT_MAX;
+        for (int i = 1 + lane; i < n; i += 32)
+            if (parent[n0 + i] == cur && tok[n0 + i] == am)
+                child = min(child, i);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            child = min(child, __shfl_xor_sync(kFull, child, o));
+        if (lane == 0)
+            out_tokens[n0 + acc] = am;
+        if (child == INT_MAX)
+            break;
+        ++acc;
+        cur = child;
+    }
+    for (int i = acc + 1 + lane; i < n; i += 32)
+        out_tokens[n0 + i] = -1;
+    if (lane == 0) {
+        out_acc[r] = acc;
+        out_last[r] = cur;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // n-gram draft proposer ("第12章 投机解码：以小博大" §12.4.4)
 // ---------------------------------------------------------------------------------------
 
@@ -1928,6 +1993,78 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
     const int grid = (int)clamp_grid((int64_t)di->sms * 8, B);
     ngram_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tokens, cu_tokens, B, min_n, max_n, k,
                                                                             max_model_len, out_drafts, out_num_drafts);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Tree workspace: the sampler's plan for N one-row "requests" (error word, partials), then
+// an all-zero cu_num_draft [N + 1] and temperature [N] that make K1 take the argmax of
+// every node row.
+static bool tree_plan(int64_t N, int32_t B, int32_t V, spec_dtype dt, Plan *pl, size_t *off_cu, size_t *off_temp,
+                      size_t *total)
+{
+    if (N < 0 || N > INT32_MAX - 1 || B < 0 || !make_plan((int32_t)N, N, V, dt, 0, pl))
+        return false;
+    *off_cu = align256(pl->total);
+    *off_temp = align256(*off_cu + sizeof(int32_t) * (size_t)(N + 1));
+    *total = align256(*off_temp + sizeof(float) * (size_t)(N > 0 ? N : 1)) + 256;
+    return true;
+}
+
+size_t spec_tree_workspace_size(int64_t N, int32_t B, int32_t V, spec_dtype logits_dtype)
+{
+    Plan pl;
+    size_t oc, ot, total;
+    return tree_plan(N, B, V, logits_dtype, &pl, &oc, &ot, &total) ? total : 0;
+}
+
+spec_status spec_tree_verify_greedy(const void *target_logits, spec_dtype logits_dtype, int64_t N, int32_t V,
+                                    int64_t logits_row_stride, const int32_t *parent, const int32_t *node_tokens,
+                                    const int32_t *cu_nodes, int32_t B, int32_t *out_tokens,
+                                    int32_t *out_num_accepted, int32_t *out_last_node, void *workspace,
+                                    size_t workspace_bytes, void *stream)
+{
+    Plan pl;
+    size_t off_cu, off_temp, total;
+    if ((logits_dtype != SPEC_F32 && logits_dtype != SPEC_BF16) || V < 1 || V > SPEC_REJECT_MAX_VOCAB ||
+        !tree_plan(N, B, V, logits_dtype, &pl, &off_cu, &off_temp, &total))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || !cu_nodes || (N > 0 && (!target_logits || !parent || !node_tokens || !out_tokens)) ||
+        (B > 0 && (!out_num_accepted || !out_last_node)) || (logits_row_stride != 0 && logits_row_stride < V))
+        return SPEC_ERR_INVALID_ARG;
+    const size_t es = logits_dtype == SPEC_BF16 ? 2 : 4;
+    if (!aligned(target_logits, es) || !aligned(parent, 4) || !aligned(node_tokens, 4) || !aligned(cu_nodes, 4) ||
+        !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) || !aligned(out_last_node, 4))
+        return SPEC_ERR_INVALID_ARG;
+    if (workspace_bytes < total)
+        return SPEC_ERR_WORKSPACE;
+    DeviceInfo *di;
+    if (device_info(&di) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
+    int32_t *fcu = reinterpret_cast<int32_t *>(base + off_cu);
+    float *ftemp = reinterpret_cast<float *>(base + off_temp);
+    if (cudaMemsetAsync(fcu, 0, (off_temp - off_cu) + sizeof(float) * (size_t)(N > 0 ? N : 1), st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    Params P{};
+    P.logits = target_logits;
+    P.T = N;
+    P.V = V;
+    P.lstride = logits_row_stride;
+    P.cu = fcu;
+    P.B = (int32_t)N;
+    P.temp = ftemp;
+    P.part = reinterpret_cast<float2 *>(base + pl.off_part);
+    P.err = reinterpret_cast<int32_t *>(base + pl.off_err);
+    P.chunk = pl.chunk;
+    P.nchunks = pl.nchunks;
+    const int DT = logits_dtype == SPEC_BF16 ? 1 : 0;
+    const int64_t full = (int64_t)di->sms * (di->blocks_rowstats[DT] > 0 ? di->blocks_rowstats[DT] : 1);
+    const int gridA = (int)clamp_grid(full, (N * (int64_t)pl.nchunks + kWarps - 1) / kWarps);
+    launch_rowstats(DT, P, *di, N, pl.nchunks, target_logits, logits_row_stride, gridA, st, 1);
+    if (B > 0)
+        tree_walk_kernel<<<(B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P, parent, node_tokens, cu_nodes, B,
+                                                                        out_tokens, out_num_accepted, out_last_node);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

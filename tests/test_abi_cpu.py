@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(spec_(?:reject|ngram)_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(spec_(?:reject|ngram|tree)_\w+)\s*\(", src)))
 
 
 def test_header_declares_expected_entry_points():
