@@ -252,7 +252,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = k1_bytes / k1_s / 1e9
     tr = traffic_for(args.workload)
-    roofline = {"bound": "hbm", "kernel": "row statistics (K1: rowstats_tma_kernel for aligned rows)",
+    roofline = {"bound": "hbm", "kernel": "row statistics (K1: rowstats_wr_kernel, warp-private TMA pipelines)",
                 "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": None if tr is None else int(tr * w["T"]),
