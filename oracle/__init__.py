@@ -40,7 +40,8 @@ NEAR_SAMPLE_ABS = 4
 DEGENERATE = 8
 BAD_INPUT = 16
 NONFINITE = 32
-NEAR_ANY = NEAR_ACCEPT | NEAR_SAMPLE | NEAR_SAMPLE_ABS | DEGENERATE
+NEAR_TOPP = 64
+NEAR_ANY = NEAR_ACCEPT | NEAR_SAMPLE | NEAR_SAMPLE_ABS | DEGENERATE | NEAR_TOPP
 
 MAX_SPEC_LEN = 32
 
@@ -74,6 +75,7 @@ class Oracle:
             P, P, P,  # out tokens, out accepted, out flags
             P, P, P, P, P, P,  # dbg row max / sum / argmax, p draft, z, margins
             ctypes.c_int,  # nthreads
+            P, P,  # top_k, top_p (optional)
         ]
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -118,7 +120,8 @@ def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.nd
                   temperature: np.ndarray, draft_probs: np.ndarray | None = None, *, dtype: str | None = None,
                   vocab: int | None = None, logits_row_stride: int | None = None, q_row_stride: int | None = None,
                   debug: bool = False, nthreads: int = 0, num_rows: int | None = None,
-                  impl: Oracle | None = None) -> OracleResult:
+                  impl: Oracle | None = None, top_k: np.ndarray | None = None,
+                  top_p: np.ndarray | None = None) -> OracleResult:
     """Run the oracle on host arrays.
 
     ``logits`` is float32 [T, V] or uint16 (raw bf16 bits) [T, V].  With an
@@ -162,11 +165,13 @@ def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.nd
                    margin=np.full((max(B, 0), 2), np.inf))
     if ids.size == 0:
         ids = np.zeros(1, dtype=np.int32)
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
+    tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
     status = (impl or _load()).lib.oracle_reject_sample(
         _ptr(logits), dcode, T, V, stride, _ptr(q), qs, _ptr(ids), _ptr(cu), B, _ptr(u), _ptr(temp),
         _ptr(tokens), _ptr(acc), _ptr(flags), _ptr(dbg.get("row_max")), _ptr(dbg.get("row_sum")),
         _ptr(dbg.get("row_argmax")), _ptr(dbg.get("p_draft")), _ptr(dbg.get("z")), _ptr(dbg.get("margin")),
-        int(nthreads))
+        int(nthreads), _ptr(tk), _ptr(tp))
     return OracleResult(tokens=tokens, num_accepted=acc, flags=flags, status=int(status), **dbg)
 
 
@@ -179,12 +184,14 @@ def reject_sample_workload(w: dict, debug: bool = False, nthreads: int = 0, num_
     """
     cu = w["cu_num_draft"]
     q = w.get("draft_probs")
+    tk, tp = w.get("top_k"), w.get("top_p")
     if num_requests is not None and num_requests < cu.shape[0] - 1:
         B = int(num_requests)
         cu = cu[: B + 1]
         nd = int(cu[-1])
         T = nd + B
         return reject_sample(w["logits"][:T], w["draft_ids"][:nd], cu, w["uniforms"][:T], w["temperature"][:B],
-                             None if q is None else q[:nd], debug=debug, nthreads=nthreads, impl=impl)
+                             None if q is None else q[:nd], debug=debug, nthreads=nthreads, impl=impl,
+                             top_k=None if tk is None else tk[:B], top_p=None if tp is None else tp[:B])
     return reject_sample(w["logits"], w["draft_ids"], cu, w["uniforms"], w["temperature"], q, debug=debug,
-                         nthreads=nthreads, impl=impl)
+                         nthreads=nthreads, impl=impl, top_k=tk, top_p=tp)

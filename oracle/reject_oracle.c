@@ -72,6 +72,7 @@
 #define OF_DEGENERATE 8u       /* residual mass Z <= 0: sampled p itself                      */
 #define OF_BAD_INPUT 16u       /* request rejected as invalid: out_num_accepted = -1          */
 #define OF_NONFINITE 32u       /* a visited row had NaN / +inf / an all -inf maximum          */
+#define OF_NEAR_TOPP 64u       /* a top-p cut: the cumulative mass within 1e-5 of top_p       */
 
 #define REL_BAND 1e-5
 #define ABS_BAND 2e-6
@@ -128,20 +129,79 @@ static int32_t row_argmax(const logit_rows *L, int64_t t)
     return best;
 }
 
-/* p(v) = exp((l(v) - m) / temp) / S with S = sum_v exp((l(v) - m) / temp). Returns S. */
-static double row_softmax(const logit_rows *L, int64_t t, double temp, double *p, double *m_out, int *nonfinite)
+/* Optional top-k / top-p restriction of the target distribution ("以小博大" §12.2.3, §12.9:
+ * the target gets temperature, then top-k / top-p).  top_k <= 0 or >= V and top_p >= 1 (or
+ * <= 0) mean "off". */
+typedef struct {
+    int32_t top_k;
+    double top_p;
+    double *scratch; /* V doubles, for sorting */
+} filter_spec;
+
+static int cmp_desc(const void *a, const void *b)
 {
+    double x = *(const double *)a, y = *(const double *)b;
+    return (x < y) - (x > y);
+}
+
+/*
+ * p(v) = exp((l(v) - m) / temp) / S over the kept tokens (0 elsewhere), S their total.
+ * Kept: all tokens without a filter; with top-k the tokens whose logit is at least the
+ * k-th largest logit (ties kept); with top-p, among those, the tokens whose logit is at
+ * least that of the token at which the descending cumulative probability first reaches
+ * top_p (ties kept).  Returns S; sets *near_topp when that cumulative came within 1e-5 of
+ * top_p on either side of the cut.
+ */
+static double row_softmax_f(const logit_rows *L, int64_t t, double temp, const filter_spec *F, double *p,
+                            double *m_out, int *nonfinite, int *near_topp)
+{
+    const int32_t V = L->V;
     double m = row_max(L, t, nonfinite);
+    double cut = -INFINITY;
+    const int use_k = F && F->top_k > 0 && F->top_k < V;
+    const int use_p = F && F->top_p > 0.0 && F->top_p < 1.0;
+    if (use_k || use_p) {
+        double *sorted = F->scratch;
+        for (int32_t v = 0; v < V; ++v)
+            sorted[v] = logit_at(L, t, v);
+        qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+        if (use_k)
+            cut = sorted[F->top_k - 1];
+        if (use_p) {
+            double Sk = 0.0;
+            for (int32_t i = 0; i < V && sorted[i] >= cut; ++i)
+                Sk += exp((sorted[i] - m) / temp);
+            double cum = 0.0;
+            for (int32_t i = 0; i < V && sorted[i] >= cut; ++i) {
+                double before = cum;
+                cum += exp((sorted[i] - m) / temp) / Sk;
+                if (cum >= F->top_p) {
+                    if (near_topp && (fabs(cum - F->top_p) <= 1e-5 || fabs(before - F->top_p) <= 1e-5))
+                        *near_topp = 1;
+                    if (sorted[i] > cut)
+                        cut = sorted[i];
+                    break;
+                }
+            }
+        }
+    }
     double S = 0.0;
-    for (int32_t v = 0; v < L->V; ++v) {
-        p[v] = exp((logit_at(L, t, v) - m) / temp);
+    for (int32_t v = 0; v < V; ++v) {
+        const double l = logit_at(L, t, v);
+        p[v] = (l >= cut) ? exp((l - m) / temp) : 0.0;
         S += p[v];
     }
-    for (int32_t v = 0; v < L->V; ++v)
+    for (int32_t v = 0; v < V; ++v)
         p[v] /= S;
     if (m_out)
         *m_out = m;
     return S;
+}
+
+/* p(v) = exp((l(v) - m) / temp) / S with S = sum_v exp((l(v) - m) / temp). Returns S. */
+static double row_softmax(const logit_rows *L, int64_t t, double temp, double *p, double *m_out, int *nonfinite)
+{
+    return row_softmax_f(L, t, temp, NULL, p, m_out, nonfinite, NULL);
 }
 
 /*
@@ -187,6 +247,8 @@ static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u, doubl
  *                     |u*q* - p*| / max(p*, u*q*) over the visited positions, [1] the
  *                     sampling margin (distance from theta to the nearest boundary of
  *                     the chosen interval) divided by Z; +inf where not applicable
+ *   top_k[B], top_p[B] optional per-request target filters (NULL = off), applied to every
+ *                     sampled row of the request (greedy requests ignore them)
  * Every dbg_* pointer may be NULL.  nthreads <= 0 uses the OpenMP default.
  * Returns 0, or 1 when the batch as a whole is inconsistent (cu[0] != 0, cu[B] + B != T or
  * cu decreasing), in which case every request is reported invalid and no token is written.
@@ -196,7 +258,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                          const int32_t *cu_num_draft, int32_t B, const float *uniforms, const float *temperature,
                          int32_t *out_tokens, int32_t *out_num_accepted, uint32_t *out_flags, double *dbg_row_max,
                          double *dbg_row_sum, int32_t *dbg_row_argmax, double *dbg_p_draft, double *dbg_z,
-                         double *dbg_margin, int nthreads)
+                         double *dbg_margin, int nthreads, const int32_t *top_k, const float *top_p)
 {
     logit_rows L = {target_logits, dtype, T, V, logits_row_stride};
     const int64_t num_draft_rows = T - B;
@@ -218,6 +280,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
     {
         double *p = (double *)malloc(sizeof(double) * (size_t)V);
         double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        double *srt = (double *)malloc(sizeof(double) * (size_t)V);
 
 #pragma omp for schedule(dynamic, 1)
         for (int32_t req = 0; req < B; ++req) {
@@ -245,6 +308,8 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
 
             const double temp = (double)temperature[req];
             const int greedy = !(temp > 0.0);
+            const filter_spec F = {top_k ? top_k[req] : 0, top_p ? (double)top_p[req] : 1.0, srt};
+            int near_topp = 0;
             int64_t j = k; /* output position: first rejection, or k for the bonus */
             int nonfinite = 0;
             double margin_accept = INFINITY, margin_sample = INFINITY;
@@ -261,7 +326,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                     continue;
                 }
                 int nf = 0;
-                row_softmax(&L, t, temp, p, NULL, &nf);
+                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &near_topp);
                 nonfinite |= nf;
                 const double qs = draft_probs ? (double)draft_probs[d * q_row_stride + xs] : 1.0;
                 const double us = (double)uniforms[2 * t + 0];
@@ -285,7 +350,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 token = row_argmax(&L, t);
             } else {
                 int nf = 0;
-                row_softmax(&L, t, temp, p, NULL, &nf);
+                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &near_topp);
                 nonfinite |= nf;
                 int explicit_residual = 0;
                 if (j < k) {
@@ -340,6 +405,8 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
             out_num_accepted[req] = (int32_t)j;
             if (nonfinite)
                 flags |= OF_NONFINITE;
+            if (near_topp)
+                flags |= OF_NEAR_TOPP;
             if (out_flags)
                 out_flags[req] = flags;
             if (dbg_z)
@@ -360,13 +427,14 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                     continue;
                 const double temp = (double)temperature[req];
                 const int greedy = !(temp > 0.0);
+                const filter_spec F = {top_k ? top_k[req] : 0, top_p ? (double)top_p[req] : 1.0, srt};
                 for (int64_t i = 0; i <= k; ++i) {
                     const int64_t t = tb + i;
                     double m, S = 0.0;
                     if (greedy) {
                         m = row_max(&L, t, NULL);
                     } else {
-                        S = row_softmax(&L, t, temp, p, &m, NULL);
+                        S = row_softmax_f(&L, t, temp, &F, p, &m, NULL, NULL);
                     }
                     if (dbg_row_max)
                         dbg_row_max[t] = m;
@@ -383,6 +451,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
         }
         free(p);
         free(r);
+        free(srt);
     }
 
     if (global_bad) {

@@ -505,9 +505,75 @@ def check_degenerate_residual(impl=None):
     return True, "ok"
 
 
+def _filtered(p, top_k, top_p):
+    """Kept set of the top-k / top-p restriction by library routines (numpy sort / cumsum)."""
+    order = np.argsort(-p, kind="stable")
+    keep = np.ones_like(p, dtype=bool)
+    if 0 < top_k < p.size:
+        keep &= p >= p[order[top_k - 1]]
+    if 0 < top_p < 1:
+        pk = np.where(keep, p, 0.0)
+        pk = pk / pk.sum()
+        srt = np.sort(pk)[::-1]
+        n = int(np.searchsorted(np.cumsum(srt), top_p))  # first index where the cumulative reaches top_p
+        keep &= pk >= srt[min(n, srt.size - 1)]
+    q = np.where(keep, p, 0.0)
+    return q / q.sum()
+
+
+def check_top_k_top_p(impl=None, N=300_000):
+    """Top-k / top-p: every emitted position is distributed as the renormalised restricted p
+    (chi-square), and the special cases top-k = 1 and a tiny top-p give the argmax."""
+    base = np.array([0.4, -0.3, 1.2, 0.1, -1.0, 0.6, 0.0, -0.5], dtype=np.float32)
+    cases = [(3, 1.0, 1.0), (0, 0.8, 0.9), (5, 0.6, 0.7), (8, 0.5, 1.0), (2, 0.3, 1.3)]
+    ntests = 2 * len(cases)
+    for ci, (tk, tp, temp) in enumerate(cases):
+        l = (base * np.float32(1.7)).astype(np.float32)
+        pf = _filtered(_p_from_logits(l, temp), tk, tp)
+        K = 1
+        ids, u, cu, temps = _iid_batch(N, K, l, temp, Q8, Q8, seed=900 + ci)
+        res = oracle.reject_sample(l, ids, cu, u, temps, Q8.astype(np.float32), logits_row_stride=0, q_row_stride=0,
+                                   vocab=8, num_rows=N * (K + 1), impl=impl, top_k=np.full(N, tk, np.int32),
+                                   top_p=np.full(N, tp, np.float32))
+        tok = res.tokens.reshape(N, K + 1)
+        for m in range(K + 1):
+            sel = res.num_accepted >= m
+            obs = np.bincount(tok[sel, m], minlength=8)
+            if obs.shape[0] != 8:
+                return False, "token out of range"
+            exp_ = pf * sel.sum()
+            if (obs[exp_ == 0] > 0).any():
+                return False, f"case {ci}: a filtered-out token was emitted at position {m}"
+            nz = exp_ > 0
+            if nz.sum() > 1:
+                pval = stats.chisquare(obs[nz], exp_[nz]).pvalue
+                if not pval > 1e-4 / ntests:
+                    return False, f"case {ci} (top_k={tk}, top_p={tp}) pos {m}: chi-square p={pval:.3g}"
+    rng = np.random.default_rng(950)
+    l = (rng.standard_normal((20, 300)) * 2).astype(np.float32)
+    am = np.argmax(l, axis=1)
+    for tk, tp in ((1, 1.0), (0, 1e-9)):
+        res = oracle.reject_sample(l, np.zeros(0, np.int32), np.zeros(21, np.int32),
+                                   rng.random((20, 2), dtype=np.float32), np.ones(20, np.float32), None, impl=impl,
+                                   top_k=np.full(20, tk, np.int32), top_p=np.full(20, tp, np.float32))
+        if not np.array_equal(res.tokens, am):
+            return False, f"top_k={tk} top_p={tp} should give the argmax"
+    # filters off (k >= V, p = 1) change nothing
+    w = None
+    res0 = oracle.reject_sample(l, np.zeros(0, np.int32), np.zeros(21, np.int32),
+                                np.full((20, 2), 0.37, np.float32), np.ones(20, np.float32), None, impl=impl)
+    res1 = oracle.reject_sample(l, np.zeros(0, np.int32), np.zeros(21, np.int32),
+                                np.full((20, 2), 0.37, np.float32), np.ones(20, np.float32), None, impl=impl,
+                                top_k=np.full(20, 300, np.int32), top_p=np.ones(20, np.float32))
+    if not np.array_equal(res0.tokens, res1.tokens):
+        return False, "disabled filters changed the result"
+    return True, "ok"
+
+
 ALL_CHECKS = [
     check_output_distribution, check_acceptance_rate, check_residual_mass, check_accepted_length,
     check_exact_enumeration, check_q_equals_p, check_disjoint_supports, check_one_hot_draft,
     check_greedy_worked_chain, check_rollback_arithmetic, check_greedy_ties_and_bonus, check_zero_drafts,
     check_extreme_uniforms, check_row_statistics, check_invalid_inputs, check_degenerate_residual,
+    check_top_k_top_p,
 ]

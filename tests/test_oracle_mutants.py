@@ -20,7 +20,12 @@ MUTANTS = {
     "output_row_off_by_one": ("const int64_t t = tb + j;", "const int64_t t = tb + (j > 0 ? j - 1 : 0);"),
     "one_hot_residual_keeps_draft": ("r[xs] = 0.0;", "r[xs] = r[xs];"),
     "inverse_cdf_non_strict": ("if (C > theta) {", "if (C >= theta) {"),
-    "temperature_dropped": ("p[v] = exp((logit_at(L, t, v) - m) / temp);", "p[v] = exp((logit_at(L, t, v) - m));"),
+    "temperature_dropped": ("p[v] = (l >= cut) ? exp((l - m) / temp) : 0.0;", "p[v] = (l >= cut) ? exp((l - m)) : 0.0;"),
+    "top_k_off_by_one": ("cut = sorted[F->top_k - 1];", "cut = sorted[F->top_k];"),
+    "top_p_cut_one_token_late": ("                    if (sorted[i] > cut)\n                        cut = sorted[i];",
+                                 "                    if (i + 1 < V && sorted[i + 1] > cut)\n                        cut = sorted[i + 1];"),
+    "top_p_normalised_over_all_tokens": ("for (int32_t i = 0; i < V && sorted[i] >= cut; ++i)\n                Sk += ",
+                                         "for (int32_t i = 0; i < V; ++i)\n                Sk += "),
     "greedy_emits_draft": ("token = row_argmax(&L, t);", "token = (j < k) ? draft_ids[db + j] : row_argmax(&L, t);"),
     "count_includes_recovered": ("out_num_accepted[req] = (int32_t)j;", "out_num_accepted[req] = (int32_t)j + 1;"),
     "bonus_not_sampled_from_p": ("} else {\n                    for (int32_t v = 0; v < V; ++v)\n                        r[v] = p[v];\n                }",
@@ -38,6 +43,7 @@ FAST_CHECKS = [
     P.check_exact_enumeration, P.check_q_equals_p, P.check_disjoint_supports, P.check_one_hot_draft,
     P.check_greedy_worked_chain, P.check_rollback_arithmetic, P.check_greedy_ties_and_bonus, P.check_zero_drafts,
     P.check_extreme_uniforms, P.check_row_statistics, P.check_invalid_inputs, P.check_degenerate_residual,
+    P.check_top_k_top_p,
 ]
 
 
