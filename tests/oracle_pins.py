@@ -525,7 +525,7 @@ def check_top_k_top_p(impl=None, N=300_000):
     """Top-k / top-p: every emitted position is distributed as the renormalised restricted p
     (chi-square), and the special cases top-k = 1 and a tiny top-p give the argmax."""
     base = np.array([0.4, -0.3, 1.2, 0.1, -1.0, 0.6, 0.0, -0.5], dtype=np.float32)
-    cases = [(3, 1.0, 1.0), (0, 0.8, 0.9), (5, 0.6, 0.7), (8, 0.5, 1.0), (2, 0.3, 1.3)]
+    cases = [(3, 1.0, 1.0), (0, 0.8, 0.9), (5, 0.6, 0.7), (8, 0.5, 1.0), (2, 0.3, 1.3), (5, 0.8, 1.3), (3, 0.7, 1.0)]
     ntests = 2 * len(cases)
     for ci, (tk, tp, temp) in enumerate(cases):
         l = (base * np.float32(1.7)).astype(np.float32)
