@@ -113,6 +113,32 @@ spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtyp
                                int32_t *out_num_accepted, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_reject_sample() with top-k / top-p applied to the target distribution, as
+ * "第12章 投机解码：以小博大" §12.2.3 and §12.9 describe (temperature, then top-k, then top-p,
+ * on the target only; the draft distribution is used as given).  For a sampled request
+ * (temperature > 0) the target p of each of its rows is restricted to
+ *   top-k: the tokens whose logit is at least the top_k[r]-th largest (ties kept), then
+ *   top-p: among those, the tokens whose logit is at least that of the token at which the
+ *          descending cumulative probability first reaches top_p[r] (ties kept),
+ * and renormalised; that p' is used for the acceptance test, the recovered token and the
+ * bonus token.  top_k[r] <= 0 or >= V, and top_p[r] >= 1 or <= 0, switch a filter off;
+ * greedy requests ignore both.  top_k (int32 [B]) and top_p (fp32 [B]) are device arrays,
+ * either may be NULL.  Filtered rows are handled by one thread-block cluster per row
+ * holding the row in distributed shared memory, which limits V to 8 x 20 chunks (V <=
+ * 655360 bf16 or 327680 fp32; SPEC_ERR_UNSUPPORTED beyond).  row_sum and p_draft are
+ * optional diagnostic outputs (device fp32 [T] and [T - B]): the restricted normaliser
+ * sum over kept tokens of exp((l - m) / T_r) and p'(x*).  Same workspace as
+ * spec_reject_sample().
+ */
+spec_status spec_reject_sample_filtered(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                        int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                        const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                        const float *uniforms, const float *temperature, const int32_t *top_k,
+                                        const float *top_p, int32_t *out_tokens, int32_t *out_num_accepted,
+                                        void *workspace, size_t workspace_bytes, void *stream, float *row_sum,
+                                        float *p_draft);
+
+/*
  * Reads the device error word of the last call that used `workspace` (waits for
  * `stream`).  Returns SPEC_OK when the device data was valid, else
  * SPEC_ERR_DEVICE_INPUT with *error_bits (SPEC_DEVERR_* bits) and

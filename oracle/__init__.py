@@ -113,7 +113,7 @@ class OracleResult:
     row_argmax: np.ndarray | None = None
     p_draft: np.ndarray | None = None
     z: np.ndarray | None = None
-    margin: np.ndarray | None = None  # [B, 2]: acceptance margin (relative), sampling margin / Z
+    margin: np.ndarray | None = None  # [B, 3]: acceptance margin (relative), sampling margin / Z, top-p margin
 
 
 def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.ndarray, uniforms: np.ndarray,
@@ -162,7 +162,7 @@ def reject_sample(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.nd
     if debug:
         dbg = dict(row_max=np.full(T, np.nan), row_sum=np.full(T, np.nan), row_argmax=np.full(T, -1, np.int32),
                    p_draft=np.full(max(T - B, 0), np.nan), z=np.full(B, np.nan),
-                   margin=np.full((max(B, 0), 2), np.inf))
+                   margin=np.full((max(B, 0), 3), np.inf))
     if ids.size == 0:
         ids = np.zeros(1, dtype=np.int32)
     tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)

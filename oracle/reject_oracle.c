@@ -72,10 +72,11 @@
 #define OF_DEGENERATE 8u       /* residual mass Z <= 0: sampled p itself                      */
 #define OF_BAD_INPUT 16u       /* request rejected as invalid: out_num_accepted = -1          */
 #define OF_NONFINITE 32u       /* a visited row had NaN / +inf / an all -inf maximum          */
-#define OF_NEAR_TOPP 64u       /* a top-p cut: the cumulative mass within 1e-5 of top_p       */
+#define OF_NEAR_TOPP 64u       /* a top-p cut: the cumulative mass within 5e-6 of top_p       */
 
 #define REL_BAND 1e-5
 #define ABS_BAND 2e-6
+#define TOPP_BAND 5e-6 /* relative band of the top-p cut (single tokens can carry ~1e-5 of the mass) */
 
 typedef struct {
     const void *logits;
@@ -149,11 +150,11 @@ static int cmp_desc(const void *a, const void *b)
  * Kept: all tokens without a filter; with top-k the tokens whose logit is at least the
  * k-th largest logit (ties kept); with top-p, among those, the tokens whose logit is at
  * least that of the token at which the descending cumulative probability first reaches
- * top_p (ties kept).  Returns S; sets *near_topp when that cumulative came within 1e-5 of
- * top_p on either side of the cut.
+ * top_p (ties kept).  Returns S; lowers *topp_margin to the relative distance between
+ * top_p and the cumulative on either side of the cut.
  */
 static double row_softmax_f(const logit_rows *L, int64_t t, double temp, const filter_spec *F, double *p,
-                            double *m_out, int *nonfinite, int *near_topp)
+                            double *m_out, int *nonfinite, double *topp_margin)
 {
     const int32_t V = L->V;
     double m = row_max(L, t, nonfinite);
@@ -176,8 +177,12 @@ static double row_softmax_f(const logit_rows *L, int64_t t, double temp, const f
                 double before = cum;
                 cum += exp((sorted[i] - m) / temp) / Sk;
                 if (cum >= F->top_p) {
-                    if (near_topp && (fabs(cum - F->top_p) <= 1e-5 || fabs(before - F->top_p) <= 1e-5))
-                        *near_topp = 1;
+                    if (topp_margin) {
+                        const double d1 = fabs(cum - F->top_p) / F->top_p, d2 = fabs(before - F->top_p) / F->top_p;
+                        const double d = d1 < d2 ? d1 : d2;
+                        if (d < *topp_margin)
+                            *topp_margin = d;
+                    }
                     if (sorted[i] > cut)
                         cut = sorted[i];
                     break;
@@ -243,10 +248,12 @@ static int32_t inverse_cdf(const double *r, int32_t V, double Z, double u, doubl
  *   dbg_p_draft[T-B]  per draft row: p(x*) (0 on greedy rows or bad ids)
  *   dbg_z[B]          per request: normalised residual mass at the output row (1 for the
  *                     bonus, 0 for greedy)
- *   dbg_margin[2*B]   per request: [0] the smallest relative acceptance margin
+ *   dbg_margin[3*B]   per request: [0] the smallest relative acceptance margin
  *                     |u*q* - p*| / max(p*, u*q*) over the visited positions, [1] the
  *                     sampling margin (distance from theta to the nearest boundary of
- *                     the chosen interval) divided by Z; +inf where not applicable
+ *                     the chosen interval) divided by Z, [2] the smallest relative
+ *                     distance of a top-p cut's cumulative to top_p; +inf where not
+ *                     applicable
  *   top_k[B], top_p[B] optional per-request target filters (NULL = off), applied to every
  *                     sampled row of the request (greedy requests ignore them)
  * Every dbg_* pointer may be NULL.  nthreads <= 0 uses the OpenMP default.
@@ -309,7 +316,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
             const double temp = (double)temperature[req];
             const int greedy = !(temp > 0.0);
             const filter_spec F = {top_k ? top_k[req] : 0, top_p ? (double)top_p[req] : 1.0, srt};
-            int near_topp = 0;
+            double topp_margin = INFINITY;
             int64_t j = k; /* output position: first rejection, or k for the bonus */
             int nonfinite = 0;
             double margin_accept = INFINITY, margin_sample = INFINITY;
@@ -326,7 +333,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                     continue;
                 }
                 int nf = 0;
-                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &near_topp);
+                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &topp_margin);
                 nonfinite |= nf;
                 const double qs = draft_probs ? (double)draft_probs[d * q_row_stride + xs] : 1.0;
                 const double us = (double)uniforms[2 * t + 0];
@@ -350,7 +357,7 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
                 token = row_argmax(&L, t);
             } else {
                 int nf = 0;
-                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &near_topp);
+                row_softmax_f(&L, t, temp, &F, p, NULL, &nf, &topp_margin);
                 nonfinite |= nf;
                 int explicit_residual = 0;
                 if (j < k) {
@@ -405,15 +412,16 @@ int oracle_reject_sample(const void *target_logits, int dtype, int64_t T, int32_
             out_num_accepted[req] = (int32_t)j;
             if (nonfinite)
                 flags |= OF_NONFINITE;
-            if (near_topp)
+            if (topp_margin <= TOPP_BAND)
                 flags |= OF_NEAR_TOPP;
             if (out_flags)
                 out_flags[req] = flags;
             if (dbg_z)
                 dbg_z[req] = greedy ? 0.0 : zr;
             if (dbg_margin) {
-                dbg_margin[2 * req] = margin_accept;
-                dbg_margin[2 * req + 1] = margin_sample;
+                dbg_margin[3 * req] = margin_accept;
+                dbg_margin[3 * req + 1] = margin_sample;
+                dbg_margin[3 * req + 2] = topp_margin;
             }
         }
 

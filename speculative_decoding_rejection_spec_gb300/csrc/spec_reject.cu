@@ -35,6 +35,7 @@
 // identical inputs give identical outputs; there are no floating-point atomics.  No kernel
 // waits on another block, so nothing can hang.
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <limits.h>
@@ -64,7 +65,7 @@ constexpr unsigned kFull = 0xffffffffu;
 struct Plan {
     int chunk;    // logits per chunk
     int nchunks;  // chunks per row
-    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, off_rcnt, total;
+    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, off_rcnt, off_thr, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -89,6 +90,8 @@ bool make_plan(int32_t B, int64_t T, int32_t V, spec_dtype dt, int has_q, Plan *
     o = align256(o + (has_q ? sizeof(float) * (size_t)B * (size_t)pl->nchunks : 0));
     pl->off_rcnt = o;
     o = align256(o + (has_q ? sizeof(int32_t) * (size_t)B : 0));
+    pl->off_thr = o;
+    o = align256(o + sizeof(uint32_t) * (size_t)T);
     pl->total = o + 256;  // slack for aligning the caller's pointer
     return true;
 }
@@ -115,6 +118,10 @@ struct Params {
     float *rpart;     // [B * nchunks] residual chunk masses
     int32_t *rcnt;    // [B] residual chunks done (zeroed by K2, counted up by K3)
     int chunk, nchunks;
+    // top-k / top-p restriction of the target (all null without filters)
+    const int32_t *top_k;  // [B]
+    const float *top_p;    // [B]
+    uint32_t *thr;         // [T] order key below which a token is cut (0 = none)
     // diagnostics (all may be null)
     float *dbg_pdraft;
     float *dbg_z;
@@ -184,6 +191,26 @@ template <> __device__ __forceinline__ float load1<1>(const char *row, int64_t v
 {
     const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(row) + v);
     return __uint_as_float(uint32_t(b) << 16);
+}
+
+// Order-preserving unsigned key of a logit (bf16: 16 bits, fp32: 32 bits): a < b iff
+// key(a) < key(b) for non-NaN values; -inf has the smallest key of any logit but 0x..7f.
+template <int DT> __device__ __forceinline__ uint32_t key_of(float x);
+template <> __device__ __forceinline__ uint32_t key_of<0>(float x)
+{
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+template <> __device__ __forceinline__ uint32_t key_of<1>(float x)
+{
+    const uint32_t b = __float_as_uint(x) >> 16;
+    return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+}
+
+// Whether a token survives the row's top-k / top-p cut (thr = 0: no cut).
+template <int DT> __device__ __forceinline__ bool kept(float x, uint32_t thr)
+{
+    return thr == 0 || key_of<DT>(x) >= thr;
 }
 
 template <int DT> __device__ __forceinline__ const char *row_ptr(const Params &P, int64_t t)
@@ -781,6 +808,285 @@ __global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_ke
 }
 
 // ---------------------------------------------------------------------------------------
+// K1F: top-k / top-p cut of a target row, one thread-block cluster per row
+// ---------------------------------------------------------------------------------------
+//
+// The cluster holds the whole row in distributed shared memory (each block a slice of whole
+// chunks, brought in with one bulk copy), so every pass below reads on-chip memory:
+//   1. row maximum m                               (cluster max)
+//   2. top-k: the k-th largest logit as an exact order key, digit by digit (8-bit radix
+//      select on counts)
+//   3. S_k = mass of the tokens at or above it      (fixed point, 2^-32 units: integer sums)
+//   4. top-p: the largest key whose tokens at or above it carry at least top_p * S_k of the
+//      mass, digit by digit on fixed-point mass histograms
+//   5. chunk partials (m_c, s_c) over the surviving tokens, in K1's format, and the row's
+//      cut key for K2 / K3.
+// Integer histograms and sums make every decision independent of scheduling.  Every block
+// of a cluster takes every cluster barrier, in the same order.
+
+namespace cg = cooperative_groups;
+
+constexpr int kFilterThreads = 512;
+constexpr int kFilterWarps = kFilterThreads / 32;
+constexpr int kFilterMaxChunksPerBlock = 20;  // 20 x 8 KB = 160 KB of the row per block
+constexpr int kFilterMaxCluster = 8;
+
+template <int DT> __device__ __forceinline__ float slice_elem(const unsigned char *sl, int64_t i)
+{
+    if (DT)
+        return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short *>(sl)[i] << 16);
+    return reinterpret_cast<const float *>(sl)[i];
+}
+
+// fn(x) for every element of the slice: 16-byte vectors, then the scalar tail.
+template <int DT, class Fn> __device__ __forceinline__ void slice_for_each(const unsigned char *sl, int64_t n, Fn fn)
+{
+    constexpr int VEC = Elem<DT>::kVec;
+    const int64_t nv = n / VEC;
+    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+        float x[VEC];
+        unpack<DT>(reinterpret_cast<const uint4 *>(sl)[v], x);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            fn(x[e]);
+    }
+    for (int64_t i = nv * VEC + threadIdx.x; i < n; i += blockDim.x)
+        fn(slice_elem<DT>(sl, i));
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int csize)
+{
+    constexpr int ES = Elem<DT>::kSize;
+    constexpr int KEY_BITS = DT ? 16 : 32;
+    extern __shared__ __align__(128) unsigned char slice[];
+    __shared__ unsigned int hcnt[kFilterWarps][256];           // per-warp count histograms
+    __shared__ unsigned long long hmass[kFilterWarps][256];    // per-warp fixed-point mass histograms
+    __shared__ unsigned long long hblk[256];                   // this block's histogram, read by the cluster
+    __shared__ unsigned long long tot[256];                    // cluster total
+    __shared__ float s_redf[kFilterWarps];
+    __shared__ unsigned long long s_redu[kFilterWarps];
+    __shared__ float s_max;
+    __shared__ unsigned long long s_sum;
+    __shared__ unsigned long long s_above;
+    __shared__ unsigned int s_bin;
+    __shared__ __align__(8) uint64_t bar;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int64_t t = blockIdx.x / csize;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (t >= P.T || P.B == 0)
+        return;  // uniform over the cluster
+    const int r = find_request(P, t);
+    const float temp = P.temp[r];
+    const int32_t tk = P.top_k ? P.top_k[r] : 0;
+    const float tp = P.top_p ? P.top_p[r] : 1.f;
+    const bool use_k = tk > 0 && tk < P.V;
+    const bool use_p = tp > 0.f && tp < 1.f;
+    if (!(temp > 0.f) || !(use_k || use_p)) {
+        if (rank == 0 && threadIdx.x == 0)
+            P.thr[t] = 0;
+        return;  // uniform over the cluster
+    }
+    const float cs = kLog2e / temp;
+    const int cpc = (P.nchunks + csize - 1) / csize;
+    const int c0 = min(P.nchunks, rank * cpc), c1 = min(P.nchunks, c0 + cpc);
+    const int64_t lo = (int64_t)c0 * P.chunk;
+    const int64_t n = max((int64_t)0, min((int64_t)P.V, (int64_t)c1 * P.chunk) - lo);
+    const char *row = row_ptr<DT>(P, t);
+
+    // ---- 0. the slice into shared memory
+    const uint32_t body =
+        ((reinterpret_cast<uintptr_t>(row + lo * ES) & 15) == 0) ? (uint32_t)((n * ES) & ~(int64_t)15) : 0u;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bar, body);
+        if (body)
+            bulk_g2s(slice, row + lo * ES, body, &bar);
+    }
+    for (int64_t i = body / ES + threadIdx.x; i < n; i += blockDim.x) {  // tail, or a misaligned slice
+        if (DT)
+            reinterpret_cast<unsigned short *>(slice)[i] = reinterpret_cast<const unsigned short *>(row)[lo + i];
+        else
+            reinterpret_cast<float *>(slice)[i] = reinterpret_cast<const float *>(row)[lo + i];
+    }
+    const bool landed = mbar_wait(&bar, 0, P.err);
+    __syncthreads();
+
+    // ---- 1. row maximum
+    float mx = -INFINITY;
+    slice_for_each<DT>(slice, n, [&](float x) { mx = fmaxf(mx, x); });
+    mx = warp_max(mx);
+    if (lane == 0)
+        s_redf[warp] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = -INFINITY;
+        for (int w = 0; w < kFilterWarps; ++w)
+            b = fmaxf(b, s_redf[w]);
+        s_max = b;
+    }
+    cluster.sync();
+    float m = -INFINITY;
+    for (int q = 0; q < csize; ++q)
+        m = fmaxf(m, *cluster.map_shared_rank(&s_max, q));
+    const float M = m * cs;
+    auto fx = [&](float x) -> unsigned long long {  // mass 2^(x c - M) <= 1 in units of 2^-32
+        return (unsigned long long)__float2ull_rz(ex2(fmaf(x, cs, -M)) * 4294967296.0f);
+    };
+
+    // One level of a radix select: histogram of digit (key >> shift) & 255 over the tokens
+    // whose key is >= lo_key and whose higher digits equal `prefix`; counts (by_mass false)
+    // or masses.  Leaves the cluster total in tot[].
+    auto radix_level = [&](int shift, uint32_t prefix, uint32_t pmask, uint32_t lo_key, bool by_mass) {
+        for (int b = lane; b < 256; b += 32) {
+            hcnt[warp][b] = 0;
+            hmass[warp][b] = 0;
+        }
+        __syncwarp();
+        slice_for_each<DT>(slice, n, [&](float x) {
+            const uint32_t key = key_of<DT>(x);
+            if (key >= lo_key && (key & pmask) == prefix) {
+                const uint32_t b = (key >> shift) & 255u;
+                if (by_mass)
+                    atomicAdd(&hmass[warp][b], fx(x));
+                else
+                    atomicAdd(&hcnt[warp][b], 1u);
+            }
+        });
+        __syncthreads();
+        if (threadIdx.x < 256) {
+            unsigned long long v = 0;
+            for (int w = 0; w < kFilterWarps; ++w)
+                v += by_mass ? hmass[w][threadIdx.x] : (unsigned long long)hcnt[w][threadIdx.x];
+            hblk[threadIdx.x] = v;
+        }
+        cluster.sync();
+        if (threadIdx.x < 256) {
+            unsigned long long v = 0;
+            for (int q = 0; q < csize; ++q)
+                v += *cluster.map_shared_rank(&hblk[threadIdx.x], q);
+            tot[threadIdx.x] = v;
+        }
+        cluster.sync();  // every block has read the others' hblk before it is rewritten
+    };
+
+    // ---- 2. top-k: exact key of the k-th largest logit
+    uint32_t tau = 0;
+    if (use_k) {
+        uint32_t prefix = 0, pmask = 0;
+        unsigned long long above = 0;
+        for (int shift = KEY_BITS - 8; shift >= 0; shift -= 8) {
+            radix_level(shift, prefix, pmask, 0u, false);
+            if (threadIdx.x == 0) {
+                unsigned long long a = above;
+                int b = 255;
+                for (; b > 0 && a + tot[b] < (unsigned long long)tk; --b)
+                    a += tot[b];
+                s_bin = (unsigned)b;
+                s_above = a;
+            }
+            __syncthreads();
+            above = s_above;
+            prefix |= s_bin << shift;
+            pmask |= 255u << shift;
+            __syncthreads();
+        }
+        tau = prefix;
+    }
+
+    // ---- 3. mass of the top-k survivors
+    unsigned long long sk = 0;
+    slice_for_each<DT>(slice, n, [&](float x) {
+        if (key_of<DT>(x) >= tau)
+            sk += fx(x);
+    });
+    sk = warp_sum_u64(sk);
+    if (lane == 0)
+        s_redu[warp] = sk;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long v = 0;
+        for (int w = 0; w < kFilterWarps; ++w)
+            v += s_redu[w];
+        s_sum = v;
+    }
+    cluster.sync();
+    unsigned long long Sk = 0;
+    for (int q = 0; q < csize; ++q)
+        Sk += *cluster.map_shared_rank(&s_sum, q);
+
+    // ---- 4. top-p: largest key whose tokens at or above it hold >= top_p * S_k
+    uint32_t lam = 0;
+    if (use_p) {
+        const double target = (double)tp * (double)Sk;
+        uint32_t prefix = 0, pmask = 0;
+        unsigned long long above = 0;
+        for (int shift = KEY_BITS - 8; shift >= 0; shift -= 8) {
+            radix_level(shift, prefix, pmask, tau, true);
+            if (threadIdx.x == 0) {
+                unsigned long long a = above;
+                int b = 255;
+                for (; b > 0 && (double)(a + tot[b]) < target; --b)
+                    a += tot[b];
+                s_bin = (unsigned)b;
+                s_above = a;
+            }
+            __syncthreads();
+            above = s_above;
+            prefix |= s_bin << shift;
+            pmask |= 255u << shift;
+            __syncthreads();
+        }
+        lam = prefix;
+    }
+    const uint32_t thr = max(max(tau, lam), 1u);
+
+    // ---- 5. chunk partials over the surviving tokens, in K1's format
+    for (int c = c0 + warp; c < c1; c += kFilterWarps) {
+        const int64_t e0 = (int64_t)c * P.chunk - lo;
+        const int64_t e1 = min(n, e0 + P.chunk);
+        float mc = -INFINITY;
+        for (int64_t i = e0 + lane; i < e1; i += 32) {
+            const float x = slice_elem<DT>(slice, i);
+            if (key_of<DT>(x) >= thr)
+                mc = fmaxf(mc, x);
+        }
+        mc = warp_max(mc);
+        float sc = 0.f;
+        if (mc > -INFINITY) {
+            const float Mc = mc * cs;
+            for (int64_t i = e0 + lane; i < e1; i += 32) {
+                const float x = slice_elem<DT>(slice, i);
+                if (key_of<DT>(x) >= thr)
+                    sc += ex2(fmaf(x, cs, -Mc));
+            }
+            sc = warp_sum(sc);
+        }
+        if (lane == 0)
+            P.part[t * P.nchunks + c] = make_float2(mc, mc == -INFINITY ? 0.f : sc);
+    }
+    if (rank == 0 && threadIdx.x == 0)
+        P.thr[t] = thr;
+    if (!landed && threadIdx.x == 0)
+        mbar_wait(&bar, 0, P.err);  // do not leave with the copy still in flight
+    cluster.sync();                 // no block leaves while another may still read its shared memory
+}
+
+// ---------------------------------------------------------------------------------------
 // Chunk combines (used by K2 / K4)
 // ---------------------------------------------------------------------------------------
 
@@ -850,9 +1156,11 @@ template <int DT> struct TargetMass {
     const char *row;
     float cs, M;
     int64_t excl;
+    uint32_t thr;  // top-k / top-p cut of the row (0 = none)
     __device__ __forceinline__ float one(int64_t v) const
     {
-        return v == excl ? 0.f : ex2(fmaf(load1<DT>(row, v), cs, -M));
+        const float x = load1<DT>(row, v);
+        return (v == excl || !kept<DT>(x, thr)) ? 0.f : ex2(fmaf(x, cs, -M));
     }
     // Sum of masses of elements [v0, v1); vector loads where the row is 16-byte aligned.
     __device__ __forceinline__ float range(int64_t v0, int64_t v1) const
@@ -867,7 +1175,7 @@ template <int DT> struct TargetMass {
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    s[e & 3] += (v + e == excl) ? 0.f : ex2(fmaf(x[e], cs, -M));
+                    s[e & 3] += (v + e == excl || !kept<DT>(x[e], thr)) ? 0.f : ex2(fmaf(x[e], cs, -M));
             }
         }
         float tail = 0.f;
@@ -882,9 +1190,14 @@ template <int DT> struct ResidualMass {
     const char *row;
     const float *qrow;
     float cs, M, inv_s;
+    uint32_t thr;  // top-k / top-p cut of the row (0 = none)
+    __device__ __forceinline__ float pm(float x) const  // target probability of a logit
+    {
+        return kept<DT>(x, thr) ? ex2(fmaf(x, cs, -M)) * inv_s : 0.f;
+    }
     __device__ __forceinline__ float one(int64_t v) const
     {
-        return fmaxf(0.f, ex2(fmaf(load1<DT>(row, v), cs, -M)) * inv_s - __ldg(qrow + v));
+        return fmaxf(0.f, pm(load1<DT>(row, v)) - __ldg(qrow + v));
     }
     __device__ __forceinline__ float range(int64_t v0, int64_t v1) const
     {
@@ -900,10 +1213,10 @@ template <int DT> struct ResidualMass {
 #pragma unroll
                 for (int h = 0; h < VEC / 4; ++h) {
                     const float4 q4 = __ldg(reinterpret_cast<const float4 *>(qrow + v) + h);
-                    s[0] += fmaxf(0.f, ex2(fmaf(x[4 * h + 0], cs, -M)) * inv_s - q4.x);
-                    s[1] += fmaxf(0.f, ex2(fmaf(x[4 * h + 1], cs, -M)) * inv_s - q4.y);
-                    s[2] += fmaxf(0.f, ex2(fmaf(x[4 * h + 2], cs, -M)) * inv_s - q4.z);
-                    s[3] += fmaxf(0.f, ex2(fmaf(x[4 * h + 3], cs, -M)) * inv_s - q4.w);
+                    s[0] += fmaxf(0.f, pm(x[4 * h + 0]) - q4.x);
+                    s[1] += fmaxf(0.f, pm(x[4 * h + 1]) - q4.y);
+                    s[2] += fmaxf(0.f, pm(x[4 * h + 2]) - q4.z);
+                    s[3] += fmaxf(0.f, pm(x[4 * h + 3]) - q4.w);
                 }
             }
         }
@@ -1084,7 +1397,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 
     // Gathers of draft row `lane` that only need x*: issued before the partial combine.
     float ls = 0.f, qs = 1.f, ua = 0.f;
+    uint32_t thr_i = 0;
     if (lane < k && !greedy) {
+        if (P.thr)
+            thr_i = P.thr[tb + lane];
         ls = load1<DT>(row_ptr<DT>(P, tb + lane), xs);
         if (P.q)
             qs = __ldg(P.q + (db + lane) * P.qstride + xs);
@@ -1155,11 +1471,11 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
         if (greedy) {
             accept = (xs == am);
         } else {
-            const float e = fmaf(ls, cs, -Mi);  // x* is in Si
-            wstar = ex2(e);
+            const float e = fmaf(ls, cs, -Mi);  // x* is in Si unless the top-k / top-p cut removed it
+            wstar = kept<DT>(ls, thr_i) ? ex2(e) : 0.f;
             const double lhs = (double)ua * (double)qs;  // exact
             const float ps = wstar / Si;
-            if (ps > 1e-30f)
+            if (ps > 1e-30f || wstar == 0.f)
                 accept = lhs < (double)ps;
             else  // below fp32's normal range: form p(x*) in double
                 accept = lhs < exp2((double)e) / (double)Si;
@@ -1179,6 +1495,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
     } else {
         const float us = P.uni[2 * tj + 1];
         const char *row = row_ptr<DT>(P, tj);
+        const uint32_t thr = P.thr ? P.thr[tj] : 0u;
         if (j == k) {  // bonus: draw from p
             float M, S;
             warp_combine_soft(P, tj, cs, lane, M, S);
@@ -1186,7 +1503,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             const float Z = chunk_total(cm, P.nchunks, lane);
             float th;
             const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-            TargetMass<DT> f{row, cs, M, -1};
+            TargetMass<DT> f{row, cs, M, -1, thr};
             token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
             zdbg = 1.f;
         } else {
@@ -1196,7 +1513,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             if (!P.q) {  // one-hot draft: residual = p without x*
                 // the chunk holding x*, summed again without it (no cancellation)
                 const int cx = xj / P.chunk;
-                TargetMass<DT> fx{row, cs, Mj, xj};
+                TargetMass<DT> fx{row, cs, Mj, xj, thr};
                 const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
                                                  min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
                 ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, Mj, cx, mx};
@@ -1211,7 +1528,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
                 }
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-                TargetMass<DT> f{row, cs, Mj, excl};
+                TargetMass<DT> f{row, cs, Mj, excl, thr};
                 token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
                                        lane);
             } else {  // explicit q: K3 / K4 finish this request
@@ -1260,10 +1577,10 @@ __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT> &f, 
 #pragma unroll
             for (int h = 0; h < VEC / 4; ++h) {
                 const uint4 qw = ld_stream(f.qrow + v + 4 * h);
-                acc[0] += fmaxf(0.f, ex2(fmaf(x[4 * h + 0], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.x));
-                acc[1] += fmaxf(0.f, ex2(fmaf(x[4 * h + 1], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.y));
-                acc[2] += fmaxf(0.f, ex2(fmaf(x[4 * h + 2], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.z));
-                acc[3] += fmaxf(0.f, ex2(fmaf(x[4 * h + 3], f.cs, -f.M)) * f.inv_s - __uint_as_float(qw.w));
+                acc[0] += fmaxf(0.f, f.pm(x[4 * h + 0]) - __uint_as_float(qw.x));
+                acc[1] += fmaxf(0.f, f.pm(x[4 * h + 1]) - __uint_as_float(qw.y));
+                acc[2] += fmaxf(0.f, f.pm(x[4 * h + 2]) - __uint_as_float(qw.z));
+                acc[3] += fmaxf(0.f, f.pm(x[4 * h + 3]) - __uint_as_float(qw.w));
             }
         }
         tail = lo + ng * VEC;
@@ -1305,7 +1622,8 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
         const float2 st = P.rstat[r];
         const float cs = kLog2e / P.temp[r];
         const char *row = row_ptr<DT>(P, t);
-        const ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y};
+        const uint32_t thr = P.thr ? P.thr[t] : 0u;
+        const ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y, thr};
         const float z = warp_residual_chunk(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk),
                                             lane);
         int last = 0;
@@ -1330,7 +1648,7 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
             const float Zp = chunk_total(cm, P.nchunks, lane);
             float th;
             const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
-            const TargetMass<DT> ft{row, cs, st.x, -1};
+            const TargetMass<DT> ft{row, cs, st.x, -1, thr};
             token = (int)warp_find(ft, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th,
                                    lane);
         }
@@ -1578,6 +1896,9 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
         return e;
     if ((e = cudaFuncSetAttribute(rowstats_wr_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWrSmem)))
         return e;
+    if ((e = cudaFuncSetAttribute(filter_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kFilterMaxChunksPerBlock * kUnitBytes)))
+        return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
         return e;
@@ -1662,11 +1983,31 @@ void launch_rowstats(int DT, const Params &P, const DeviceInfo &di, int64_t T, i
     }
 }
 
+// K1F: one cluster per target row (blocks of unfiltered rows exit at once).
+cudaError_t launch_filter(int DT, const Params &P, int64_t T, int nchunks, cudaStream_t stream)
+{
+    const int csize = (nchunks + kFilterMaxChunksPerBlock - 1) / kFilterMaxChunksPerBlock;
+    const int cpc = (nchunks + csize - 1) / csize;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(T * csize), 1, 1);
+    cfg.blockDim = dim3(kFilterThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)cpc * kUnitBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return DT ? cudaLaunchKernelEx(&cfg, filter_kernel<1>, P, csize) : cudaLaunchKernelEx(&cfg, filter_kernel<0>, P, csize);
+}
+
 spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t lstride, const float *q,
                 int64_t qstride, const int32_t *ids, const int32_t *cu, int32_t B, const float *uni,
                 const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
                 cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
-                cudaEvent_t *ev = nullptr, int nev = 0)
+                cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr)
 {
     spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
     if (st != SPEC_OK)
@@ -1681,7 +2022,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         return SPEC_ERR_CUDA;
 
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
-    Params P;
+    Params P{};  // every optional pointer starts null
     P.logits = logits;
     P.T = T;
     P.V = V;
@@ -1705,6 +2046,16 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     P.nchunks = pl.nchunks;
     P.dbg_pdraft = dbg_pd;
     P.dbg_z = dbg_z;
+    const bool filtered = top_k || top_p;
+    if (filtered) {
+        if (!aligned(top_k, 4) || !aligned(top_p, 4) ||
+            (pl.nchunks + kFilterMaxChunksPerBlock - 1) / kFilterMaxChunksPerBlock > kFilterMaxCluster)
+            return pl.nchunks > kFilterMaxChunksPerBlock * kFilterMaxCluster ? SPEC_ERR_UNSUPPORTED
+                                                                            : SPEC_ERR_INVALID_ARG;
+        P.top_k = top_k;
+        P.top_p = top_p;
+        P.thr = reinterpret_cast<uint32_t *>(base + pl.off_thr);
+    }
 
     const int DT = dt == SPEC_BF16 ? 1 : 0;
     const int64_t units = T * (int64_t)pl.nchunks;
@@ -1722,6 +2073,8 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     };
     mark();
     launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
+    if (filtered && T > 0 && B > 0 && launch_filter(DT, P, T, pl.nchunks, stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
     mark();
     if (debug && T > 0 && (dbg_m || dbg_s)) {
         const int g = (int)((T + kWarps - 1) / kWarps);
@@ -1783,6 +2136,20 @@ spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtyp
     return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
                cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
                static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+spec_status spec_reject_sample_filtered(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                        int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                        const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                        const float *uniforms, const float *temperature, const int32_t *top_k,
+                                        const float *top_p, int32_t *out_tokens, int32_t *out_num_accepted,
+                                        void *workspace, size_t workspace_bytes, void *stream, float *row_sum,
+                                        float *p_draft)
+{
+    return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
+               cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(stream), nullptr, row_sum, nullptr, p_draft, nullptr, nullptr, 0, top_k,
+               top_p);
 }
 
 spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,

@@ -99,7 +99,8 @@ def generate(spec: dict | str, seed: int | None = None, threads: int | None = No
                  "target_mix" (no q; a draw from softmax(l) w.p. p_match else a uniform token),
                  "uniform" (no q; uniform tokens);
       ``boost``: add this to one uniformly chosen logit per row;
-      ``temperature``: a scalar or a per-request sequence.
+      ``temperature``: a scalar or a per-request sequence;
+      ``top_k`` / ``top_p``: optional target filters, scalars or per-request sequences.
     """
     name = spec if isinstance(spec, str) else spec.get("name", "custom")
     spec = dict(CONFIGS[spec]) if isinstance(spec, str) else dict(spec)
@@ -189,8 +190,14 @@ def generate(spec: dict | str, seed: int | None = None, threads: int | None = No
             list(ex.map(make_block, range(nblocks)))
 
     uniforms = _rng(seed, 3).random((T, 2), dtype=np.float32)
-    return dict(name=name, dtype=dtype, B=B, T=T, V=V, logits=logits, draft_probs=draft_probs, draft_ids=draft_ids,
-                cu_num_draft=cu, uniforms=uniforms, temperature=temps, spec=spec)
+    out = dict(name=name, dtype=dtype, B=B, T=T, V=V, logits=logits, draft_probs=draft_probs, draft_ids=draft_ids,
+               cu_num_draft=cu, uniforms=uniforms, temperature=temps, spec=spec)
+    # optional top-k / top-p on the target (scalars or per-request sequences)
+    if spec.get("top_k") is not None:
+        out["top_k"] = np.broadcast_to(np.asarray(spec["top_k"], dtype=np.int32), (B,)).copy()
+    if spec.get("top_p") is not None:
+        out["top_p"] = np.broadcast_to(np.asarray(spec["top_p"], dtype=np.float32), (B,)).copy()
+    return out
 
 
 def total_drafts(w: dict) -> int:

@@ -40,7 +40,12 @@ def run_gpu(w, debug=False, device_tensors=None, buffers=None):
     d = device_tensors or binding.to_device(w)
     buf = buffers or binding.make_buffers(w["B"], w["T"], w["V"], dtype_code(w), d["draft_probs"] is not None)
     dbg = {} if debug else None
-    tok, acc = binding.sample(**d, buffers=buf, debug=dbg)
+    if w.get("top_k") is not None or w.get("top_p") is not None:
+        tk = None if w.get("top_k") is None else torch.from_numpy(w["top_k"]).cuda()
+        tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).cuda()
+        tok, acc = binding.sample_filtered(**d, top_k=tk, top_p=tp, buffers=buf, debug=dbg)
+    else:
+        tok, acc = binding.sample(**d, buffers=buf, debug=dbg)
     st, bits, first = binding.last_device_error(buf.workspace)
     torch.cuda.synchronize()
     out = dict(tokens=tok.cpu().numpy().copy(), acc=acc.cpu().numpy().copy(), status=st, bits=bits, first=first)
@@ -62,10 +67,10 @@ def compare(w, gpu, ref) -> Compared:
         same = gpu["acc"][r] == ref.num_accepted[r] and np.array_equal(gpu["tokens"][lo:hi], ref.tokens[lo:hi])
         if not same:
             if ref.margin is not None:
-                m_acc, m_smp = float(ref.margin[r, 0]), float(ref.margin[r, 1])
+                m_acc, m_smp, m_topp = (float(x) for x in ref.margin[r, :3])
                 if w.get("draft_probs") is not None and 0 <= ref.num_accepted[r] < cu[r + 1] - cu[r]:
                     m_smp *= float(ref.z[r])  # explicit-q residual: the fp32 error is absolute, not relative to Z
-                worst = max(worst, min(m_acc, m_smp))
+                worst = max(worst, min(m_acc, m_smp, m_topp))
             if flagged[r]:
                 mism_f += 1
             else:
