@@ -172,6 +172,8 @@ def main():
     ap.add_argument("--workload", default="large-1024")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--top-k", type=int, default=None, help="top-k on the target, every request")
+    ap.add_argument("--top-p", type=float, default=None, help="top-p on the target, every request")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -185,8 +187,11 @@ def main():
                         f", temperature {spec['temperature']}",
             "B_per_gpu": spec["B"], "V": spec["V"], "logits_dtype": spec["dtype"],
             "l2": "inputs larger than L2 (no flush)", "rng": "numpy PCG64, seeded"}
+    filtered = args.top_k is not None or args.top_p is not None
+    if filtered:
+        meta["workload"] += f", top-k {args.top_k}, top-p {args.top_p}"
     # each rank draws its own batch (independent requests: weak scaling, no data-path collective)
-    w = W.generate(args.workload, seed=spec["seed"] + 1000 * rank)
+    w = W.generate(args.workload, seed=spec["seed"] + 1000 * rank, top_k=args.top_k, top_p=args.top_p)
     if args.impl == "reference":
         run_reference(args, w, meta)
         return
@@ -205,7 +210,9 @@ def main():
     has_q = d["draft_probs"] is not None
     dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, has_q, dev)
-    nk = binding.num_kernels(has_q)
+    tk = None if w.get("top_k") is None else torch.from_numpy(w["top_k"]).to(dev)
+    tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).to(dev)
+    nk = binding.num_kernels(has_q, filtered)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in ev:
@@ -214,7 +221,7 @@ def main():
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        binding.sample(**d, buffers=buf)
+        binding.sample_profiled(d, buf, [], stream, tk, tp)
     st, bits, _ = binding.last_device_error(buf.workspace)
     if st != 0:
         raise SystemExit(f"device input error bits {bits}")
@@ -228,7 +235,7 @@ def main():
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
-        binding.sample_profiled(d, buf, ev[i], stream)
+        binding.sample_profiled(d, buf, ev[i], stream, tk, tp)
     stop.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -269,10 +276,13 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
             "hbm_gbs_effective": round(call_bytes / (ms / 1e3) / 1e9, 1),
-            "stage_ms": [round(x, 4) for x in stage_ms], "rows_per_s": w["T"] * world / (ms / 1e3),
+            "stage_ms": [round(x, 4) for x in stage_ms],
+            "stages": ["rowstats"] + (["topk_topp_cut"] if filtered else []) + ["finalize"]
+                      + (["residual"] if has_q else []),
+            "rows_per_s": w["T"] * world / (ms / 1e3),
             "roofline": roofline, "gpu_launches": nk * args.steps, "clocks": clocks}
 
-    if not args.no_e2e:
+    if not args.no_e2e and not filtered:  # the host-buffer entry point takes no filters
         line["e2e"] = e2e(w, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)

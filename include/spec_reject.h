@@ -183,10 +183,12 @@ spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype log
                                        float *p_draft, float *z_out);
 
 /*
- * Measurement form of spec_reject_sample(): identical work, plus cudaEventRecord of
- * caller-created events (cudaEvent_t handles) on `stream` between the kernels:
- * stage_events[0] before the row-statistics pass, [1] after it, [2] after the
- * per-request finalize, and with draft_probs [3] after the residual / recovery pass.  Entries beyond num_events, or NULL entries, are skipped.
+ * Measurement form of spec_reject_sample() / spec_reject_sample_filtered() (top_k and top_p
+ * may be NULL): identical work, plus cudaEventRecord of caller-created events (cudaEvent_t
+ * handles) on `stream`: stage_events[0] before the first kernel, then one after each kernel
+ * launched, in order: row statistics, the top-k / top-p cut (filtered calls only), the
+ * per-request finalize, the residual / recovery pass (with draft_probs only).  Entries
+ * beyond num_events, or NULL entries, are skipped.
  * The pages have no counterpart: this exists to time each kernel on its own stream.
  */
 spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
@@ -194,7 +196,8 @@ spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype lo
                                         const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
                                         const float *uniforms, const float *temperature, int32_t *out_tokens,
                                         int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
-                                        void *stream, void *const *stage_events, int num_events);
+                                        void *stream, const int32_t *top_k, const float *top_p,
+                                        void *const *stage_events, int num_events);
 
 /*
  * spec_reject_sample() for callers that cannot allocate device memory: for example a
@@ -300,8 +303,8 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
                                int32_t max_n, int32_t k, int64_t max_model_len, int32_t *out_drafts,
                                int32_t *out_num_drafts, void *stream);
 
-/* Kernels one spec_reject_sample() call launches (2 without draft probabilities, 3 with). */
-int spec_reject_num_kernels(int has_draft_probs);
+/* Kernels one call launches: 2, plus 1 with draft probabilities, plus 1 with top-k / top-p. */
+int spec_reject_num_kernels(int has_draft_probs, int has_filters);
 
 /* Static description of a status code. */
 const char *spec_reject_status_string(spec_status status);

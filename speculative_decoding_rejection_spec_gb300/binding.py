@@ -67,7 +67,7 @@ def load():
     lib.spec_reject_status_string.argtypes = [ctypes.c_int]
     lib.spec_reject_version.restype = ctypes.c_int
     lib.spec_reject_sample_profiled.restype = ctypes.c_int
-    lib.spec_reject_sample_profiled.argtypes = sample_args + [P, ctypes.c_int]
+    lib.spec_reject_sample_profiled.argtypes = sample_args + [P, P, P, ctypes.c_int]
     lib.spec_reject_sample_noalloc.restype = ctypes.c_int
     lib.spec_reject_sample_noalloc.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, P]
     lib.spec_reject_metrics_update.restype = ctypes.c_int
@@ -82,7 +82,7 @@ def load():
     lib.spec_reject_sample_filtered.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, P,
                                                 P, sz, P, P, P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
-    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int]
+    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int]
     _lib = lib
     return lib
 
@@ -194,11 +194,12 @@ def sample(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_
     return buffers.out_tokens, buffers.out_num_accepted
 
 
-def sample_profiled(d: dict, buffers: Buffers, events: list, stream=None):
+def sample_profiled(d: dict, buffers: Buffers, events: list, stream=None, top_k=None, top_p=None):
     """``sample`` plus CUDA events recorded between the kernels (see spec_reject_sample_profiled).
 
     ``events`` are torch.cuda.Event(enable_timing=True) objects that have been recorded once
-    (so that their handles exist).
+    (so that their handles exist).  ``top_k`` / ``top_p`` are optional device tensors as in
+    ``sample_filtered``.
     """
     lib = load()
     t = d["target_logits"]
@@ -210,7 +211,7 @@ def sample_profiled(d: dict, buffers: Buffers, events: list, stream=None):
         _ptr(t), _dtype_code(t), T, V, _row_stride(t), _ptr(q), 0 if q is None else _row_stride(q),
         _ptr(d["draft_ids"]), _ptr(d["cu_num_draft"]), B, _ptr(d["uniforms"]), _ptr(d["temperature"]),
         _ptr(buffers.out_tokens), _ptr(buffers.out_num_accepted), _ptr(buffers.workspace),
-        int(buffers.workspace.numel()), _stream(stream), handles, len(events))
+        int(buffers.workspace.numel()), _stream(stream), _ptr(top_k), _ptr(top_p), handles, len(events))
     if st != 0:
         raise SpecRejectError(st, "spec_reject_sample_profiled")
 
@@ -293,8 +294,8 @@ def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None
     return out, acc, last, ws
 
 
-def num_kernels(has_draft_probs: bool) -> int:
-    return int(load().spec_reject_num_kernels(int(bool(has_draft_probs))))
+def num_kernels(has_draft_probs: bool, has_filters: bool = False) -> int:
+    return int(load().spec_reject_num_kernels(int(bool(has_draft_probs)), int(bool(has_filters))))
 
 
 def sample_filtered(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *,

@@ -194,17 +194,31 @@ template <> __device__ __forceinline__ float load1<1>(const char *row, int64_t v
 }
 
 // Order-preserving unsigned key of a logit (bf16: 16 bits, fp32: 32 bits): a < b iff
-// key(a) < key(b) for non-NaN values; -inf has the smallest key of any logit but 0x..7f.
+// key(a) < key(b), and a == b (-0 == +0) iff the keys are equal, for non-NaN values.  The
+// key is 0x8000.. plus the signed magnitude, so every key is at least 1.
 template <int DT> __device__ __forceinline__ uint32_t key_of(float x);
 template <> __device__ __forceinline__ uint32_t key_of<0>(float x)
 {
     const uint32_t b = __float_as_uint(x);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    const uint32_t s = (uint32_t)((int32_t)b >> 31);
+    return 0x80000000u + (((b & 0x7fffffffu) ^ s) - s);
 }
 template <> __device__ __forceinline__ uint32_t key_of<1>(float x)
 {
-    const uint32_t b = __float_as_uint(x) >> 16;
-    return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t s = (uint32_t)((int32_t)b >> 31);
+    return 0x8000u + ((((b >> 16) & 0x7fffu) ^ s) - s);
+}
+
+// The logit whose order key is `key` (inverse of key_of; -0 comes back as +0).
+template <int DT> __device__ __forceinline__ float x_of(uint32_t key);
+template <> __device__ __forceinline__ float x_of<0>(uint32_t key)
+{
+    return __uint_as_float(key >= 0x80000000u ? key - 0x80000000u : 0x80000000u | (0x80000000u - key));
+}
+template <> __device__ __forceinline__ float x_of<1>(uint32_t key)
+{
+    return __uint_as_float((key >= 0x8000u ? key - 0x8000u : 0x8000u | (0x8000u - key)) << 16);
 }
 
 // Whether a token survives the row's top-k / top-p cut (thr = 0: no cut).
@@ -812,17 +826,31 @@ __global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_ke
 // ---------------------------------------------------------------------------------------
 //
 // The cluster holds the whole row in distributed shared memory (each block a slice of whole
-// chunks, brought in with one bulk copy), so every pass below reads on-chip memory:
-//   1. row maximum m                               (cluster max)
-//   2. top-k: the k-th largest logit as an exact order key, digit by digit (8-bit radix
-//      select on counts)
-//   3. S_k = mass of the tokens at or above it      (fixed point, 2^-32 units: integer sums)
-//   4. top-p: the largest key whose tokens at or above it carry at least top_p * S_k of the
-//      mass, digit by digit on fixed-point mass histograms
-//   5. chunk partials (m_c, s_c) over the surviving tokens, in K1's format, and the row's
-//      cut key for K2 / K3.
-// Integer histograms and sums make every decision independent of scheduling.  Every block
-// of a cluster takes every cluster barrier, in the same order.
+// chunks, brought in with one bulk copy).  K1 has already written the row's unfiltered chunk
+// partials, which give the row maximum m, each chunk's maximum and (for top-p alone) the
+// normaliser Z.  A token's mass is 2^(l c - m c) in fixed point (2^-32 units), so the sums
+// that decide the cut are integer sums and no decision depends on scheduling.
+//
+// bf16 rows first try one pass: each warp counts its chunk's tokens by their order key's
+// offset below the maximum's key, over the kFKeys largest keys.  One count and one mass per
+// key give the exact k-th largest key, S_k, the exact top-p key, and each chunk's partial
+// (m_c, s_c) over the survivors, with no second pass.  A cut further down than kFKeys keys,
+// and every fp32 row, takes the general path:
+//   1. one pass: token counts over kFBins bins of d = m c - l c (kFBinScale bins per unit of
+//      log2 relative probability, the last bin open-ended).  The bin is a monotone function of
+//      the logit, so every token of a lower bin outranks every token of a higher one.
+//   2. the last bin that can hold a survivor: top-k, the bin where the count scan reaches k;
+//      top-p alone, the bin where a lower bound of the cumulative mass (each bin's count times
+//      the least mass its tokens can have) reaches top_p * Z.
+//   3. one pass: every token up to that bin goes into a candidate list (order key, position).
+//   4. from the list: the k-th largest key (ranking the tokens of its bin), S_k = the exact
+//      mass at or above it, the bin where the exact cumulative mass reaches top_p * S_k and
+//      the exact key inside it, and each chunk's partial over the survivors.
+// A list longer than kFList falls back to passes over the slice (mass histograms and radix
+// selects on the order key), and a bin with more than kFWindow tokens is resolved by a radix
+// select over the slice.  The row's cut key goes to K2 / K3.  Every block of a cluster takes
+// every cluster barrier, in the same order, and makes the same decisions from the same
+// cluster-wide totals.
 
 namespace cg = cooperative_groups;
 
@@ -830,6 +858,16 @@ constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kFilterMaxChunksPerBlock = 20;  // 20 x 8 KB = 160 KB of the row per block
 constexpr int kFilterMaxCluster = 8;
+constexpr int kFBins = 2048;                  // bins of d
+constexpr float kFBinScale = 64.f;            // bins per unit of log2 relative probability
+constexpr int kFList = 2048;                  // candidate list entries (per block, and merged)
+constexpr int kFWindow = 512;                 // tokens of one bin ranked directly
+#ifndef SPEC_FILTER_KEYS
+#define SPEC_FILTER_KEYS 512
+#endif
+constexpr int kFKeys = SPEC_FILTER_KEYS;      // bf16 one-pass window: the largest keys counted
+static_assert(kFBins == 4 * kFilterThreads, "bins are owned four per thread");
+static_assert(kFWindow <= kFilterThreads, "one window token per thread");
 
 template <int DT> __device__ __forceinline__ float slice_elem(const unsigned char *sl, int64_t i)
 {
@@ -838,20 +876,27 @@ template <int DT> __device__ __forceinline__ float slice_elem(const unsigned cha
     return reinterpret_cast<const float *>(sl)[i];
 }
 
-// fn(x) for every element of the slice: 16-byte vectors, then the scalar tail.
-template <int DT, class Fn> __device__ __forceinline__ void slice_for_each(const unsigned char *sl, int64_t n, Fn fn)
+// fn(x, i) for every element i of sl[e0, e1) with threads tid0, tid0 + step, ...: 16-byte
+// vectors over the aligned middle (e0 a multiple of the vector width), then the scalar tail.
+template <int DT, class Fn>
+__device__ __forceinline__ void slice_range(const unsigned char *sl, int64_t e0, int64_t e1, int tid0, int step, Fn fn)
 {
     constexpr int VEC = Elem<DT>::kVec;
-    const int64_t nv = n / VEC;
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+    const int v0 = (int)(e0 / VEC), v1 = (int)(e1 / VEC);
+    for (int v = v0 + tid0; v < v1; v += step) {
         float x[VEC];
         unpack<DT>(reinterpret_cast<const uint4 *>(sl)[v], x);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-            fn(x[e]);
+            fn(x[e], v * VEC + e);
     }
-    for (int64_t i = nv * VEC + threadIdx.x; i < n; i += blockDim.x)
-        fn(slice_elem<DT>(sl, i));
+    for (int i = v1 * VEC + tid0; i < (int)e1; i += step)
+        fn(slice_elem<DT>(sl, i), i);
+}
+
+template <int DT, class Fn> __device__ __forceinline__ void slice_for_each(const unsigned char *sl, int64_t n, Fn fn)
+{
+    slice_range<DT>(sl, 0, n, threadIdx.x, blockDim.x, fn);
 }
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
@@ -862,22 +907,157 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
     return v;
 }
 
+__device__ __forceinline__ double warp_sum_f64(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Scalars of one K1F block.
+struct FilterShared {
+    unsigned long long red[kFilterWarps];
+    double z;
+    float maxv;
+    unsigned nlocal;
+    int nlist;
+    int pos;
+    unsigned long long above;
+    unsigned long long sum;
+    unsigned best;
+    unsigned nwin;
+};
+
+// Arrays of the general path.
+struct FilterGeneral {
+    unsigned cnt[kFBins];                // bin counts (cluster totals after the sum)
+    unsigned long long mh[kFBins];       // bin masses: 64-bit sums, or (list path) 16-bit halves
+    unsigned long long local[kFList];    // this block's candidates; after the merge, scratch
+    unsigned long long list[kFList];     // the cluster's candidates: key << 32 | position
+};
+
+// Arrays of the bf16 one-pass path.
+struct FilterKeys {
+    unsigned hc[kFilterMaxChunksPerBlock][kFKeys + 32];  // per chunk: tokens per key offset, then
+                                                         // one sink per lane for the rest
+    unsigned bh[kFKeys];                                 // per key offset: block, then cluster totals
+    unsigned gather[kFilterMaxCluster][kFKeys];          // every block's totals, pushed by its owner
+    unsigned long long km[kFKeys];                       // mass of one token at each key offset
+};
+
+union FilterArrays {
+    FilterGeneral g;
+    FilterKeys k;
+};
+
+// Sum over the block (every thread gets it).
+__device__ __forceinline__ unsigned long long block_sum_u64(FilterShared &S, unsigned long long v)
+{
+    v = warp_sum_u64(v);
+    __syncthreads();  // S.red is free
+    if ((threadIdx.x & 31) == 0)
+        S.red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    unsigned long long t = 0;
+    for (int w = 0; w < kFilterWarps; ++w)
+        t += S.red[w];
+    return t;
+}
+
+// Sum of a per-thread value over the block, then over the cluster (every thread gets it).
+__device__ __forceinline__ unsigned long long cluster_sum_u64(FilterShared &S, cg::cluster_group &cluster, int csize,
+                                                              unsigned long long v)
+{
+    const unsigned long long b = block_sum_u64(S, v);
+    if (threadIdx.x == 0)
+        S.sum = b;
+    cluster.sync();
+    unsigned long long t = 0;
+    for (int q = 0; q < csize; ++q)
+        t += *cluster.map_shared_rank(&S.sum, q);
+    cluster.sync();  // every block has read every S.sum before any is rewritten
+    return t;
+}
+
+// In-place cluster-wide sum of the first nb entries of every block's histogram h (h at the
+// same offset in every block).  Threads own nb / blockDim consecutive bins (nb <= 4 *
+// blockDim, a multiple of blockDim or at most blockDim).
+template <class W>
+__device__ __forceinline__ void cluster_sum_hist(W *h, cg::cluster_group &cluster, int csize, int nb)
+{
+    const int per = nb > (int)blockDim.x ? nb / (int)blockDim.x : 1;
+    const int b0 = threadIdx.x * per;
+    W v[4] = {0, 0, 0, 0};
+    cluster.sync();  // every block's histogram is complete
+    if (b0 < nb)
+        for (int q = 0; q < csize; ++q) {
+            const W *hq = cluster.map_shared_rank(h, q);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < per)
+                    v[k] += hq[b0 + k];
+        }
+    cluster.sync();  // every block has read every histogram
+    if (b0 < nb)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < per)
+                h[b0 + k] = v[k];
+    __syncthreads();
+}
+
+// Scan of weights w(0..nb) in order: the first position i at which
+// above0 + w(0) + ... + w(i) >= target.  Leaves i in S.pos (-1 when the total falls short)
+// and above0 + w(0) + ... + w(i - 1) in S.above.  Same ownership as cluster_sum_hist.
+template <class WF>
+__device__ __forceinline__ void find_crossing(FilterShared &S, int nb, unsigned long long above0,
+                                              unsigned long long target, WF w)
+{
+    const int per = nb > (int)blockDim.x ? nb / (int)blockDim.x : 1;
+    const int b0 = threadIdx.x * per;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long mine = 0;
+    if (b0 < nb)
+        for (int k = 0; k < per; ++k)
+            mine += w(b0 + k);
+    unsigned long long inc = mine;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o)
+            inc += y;
+    }
+    __syncthreads();  // S.red and S.pos are free
+    if (threadIdx.x == 0)
+        S.pos = -1;
+    if (lane == 31)
+        S.red[warp] = inc;
+    __syncthreads();
+    unsigned long long c = above0 + inc - mine;
+    for (int q = 0; q < warp; ++q)
+        c += S.red[q];
+    if (b0 < nb && c < target && c + mine >= target)
+        for (int k = 0; k < per; ++k) {
+            const unsigned long long wk = w(b0 + k);
+            if (c + wk >= target) {
+                S.pos = b0 + k;
+                S.above = c;
+                break;
+            }
+            c += wk;
+        }
+    __syncthreads();
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int csize)
 {
-    constexpr int ES = Elem<DT>::kSize;
     constexpr int KEY_BITS = DT ? 16 : 32;
+    constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char slice[];
-    __shared__ unsigned int hcnt[kFilterWarps][256];           // per-warp count histograms
-    __shared__ unsigned long long hmass[kFilterWarps][256];    // per-warp fixed-point mass histograms
-    __shared__ unsigned long long hblk[256];                   // this block's histogram, read by the cluster
-    __shared__ unsigned long long tot[256];                    // cluster total
-    __shared__ float s_redf[kFilterWarps];
-    __shared__ unsigned long long s_redu[kFilterWarps];
-    __shared__ float s_max;
-    __shared__ unsigned long long s_sum;
-    __shared__ unsigned long long s_above;
-    __shared__ unsigned int s_bin;
+    __shared__ FilterShared S;
+    __shared__ FilterArrays U;
     __shared__ __align__(8) uint64_t bar;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -903,8 +1083,9 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
     const int64_t lo = (int64_t)c0 * P.chunk;
     const int64_t n = max((int64_t)0, min((int64_t)P.V, (int64_t)c1 * P.chunk) - lo);
     const char *row = row_ptr<DT>(P, t);
+    float2 *pp = P.part + t * P.nchunks;
 
-    // ---- 0. the slice into shared memory
+    // ---- 0. the slice into shared memory; meanwhile m (and Z) from K1's partials
     const uint32_t body =
         ((reinterpret_cast<uintptr_t>(row + lo * ES) & 15) == 0) ? (uint32_t)((n * ES) & ~(int64_t)15) : 0u;
     if (threadIdx.x == 0) {
@@ -923,167 +1104,411 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
         else
             reinterpret_cast<float *>(slice)[i] = reinterpret_cast<const float *>(row)[lo + i];
     }
+    if (warp == 0) {
+        float mm = -INFINITY;
+        for (int c = lane; c < P.nchunks; c += 32)
+            mm = fmaxf(mm, pp[c].x);
+        mm = warp_max(mm);
+        double z = 0.0;
+        if (!use_k && mm > -INFINITY) {
+            const float Mm = mm * cs;
+            for (int c = lane; c < P.nchunks; c += 32) {
+                const float2 pc = pp[c];
+                if (pc.x != -INFINITY)
+                    z += (double)pc.y * (double)ex2(pc.x * cs - Mm);
+            }
+            z = warp_sum_f64(z);
+        }
+        if (lane == 0) {
+            S.maxv = mm;
+            S.z = z * 4294967296.0;
+        }
+    }
     const bool landed = mbar_wait(&bar, 0, P.err);
     __syncthreads();
-
-    // ---- 1. row maximum
-    float mx = -INFINITY;
-    slice_for_each<DT>(slice, n, [&](float x) { mx = fmaxf(mx, x); });
-    mx = warp_max(mx);
-    if (lane == 0)
-        s_redf[warp] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float b = -INFINITY;
-        for (int w = 0; w < kFilterWarps; ++w)
-            b = fmaxf(b, s_redf[w]);
-        s_max = b;
+    const float m = S.maxv;
+    if (!(m > -INFINITY)) {  // no finite logit in the row (the same in every block): no cut
+        if (rank == 0 && threadIdx.x == 0)
+            P.thr[t] = 0;
+        if (!landed && threadIdx.x == 0)
+            mbar_wait(&bar, 0, P.err);
+        return;
     }
-    cluster.sync();
-    float m = -INFINITY;
-    for (int q = 0; q < csize; ++q)
-        m = fmaxf(m, *cluster.map_shared_rank(&s_max, q));
     const float M = m * cs;
-    auto fx = [&](float x) -> unsigned long long {  // mass 2^(x c - M) <= 1 in units of 2^-32
-        return (unsigned long long)__float2ull_rz(ex2(fmaf(x, cs, -M)) * 4294967296.0f);
+    auto fx = [&](float x) -> unsigned long long {  // mass 2^(x c - M) in units of 2^-32
+        return __float2ull_rn(ex2(fmaf(x, cs, -M)) * 4294967296.0f);
     };
+    // s_c of K1's format from a fixed-point sum 2^32 * sum 2^(x c - Mc)
+    auto fx_chunk = [&](float x, float Mc) -> unsigned long long {
+        return __float2ull_rn(ex2(fmaf(x, cs, -Mc)) * 4294967296.0f);
+    };
+    constexpr float kTwoM32 = 2.3283064365386963e-10f;  // 2^-32
 
-    // One level of a radix select: histogram of digit (key >> shift) & 255 over the tokens
-    // whose key is >= lo_key and whose higher digits equal `prefix`; counts (by_mass false)
-    // or masses.  Leaves the cluster total in tot[].
-    auto radix_level = [&](int shift, uint32_t prefix, uint32_t pmask, uint32_t lo_key, bool by_mass) {
-        for (int b = lane; b < 256; b += 32) {
-            hcnt[warp][b] = 0;
-            hmass[warp][b] = 0;
-        }
-        __syncwarp();
-        slice_for_each<DT>(slice, n, [&](float x) {
-            const uint32_t key = key_of<DT>(x);
-            if (key >= lo_key && (key & pmask) == prefix) {
-                const uint32_t b = (key >> shift) & 255u;
-                if (by_mass)
-                    atomicAdd(&hmass[warp][b], fx(x));
-                else
-                    atomicAdd(&hcnt[warp][b], 1u);
-            }
-        });
+    uint32_t thr = 0;
+    bool done = false;
+
+    // ---- bf16: one pass over the kFKeys largest keys
+    if constexpr (DT == 1) {
+        const int nck = c1 - c0;
+        const uint32_t kmax = key_of<1>(m);
+        for (int i = threadIdx.x; i < nck * (kFKeys + 32); i += blockDim.x)
+            (&U.k.hc[0][0])[i] = 0u;
         __syncthreads();
-        if (threadIdx.x < 256) {
-            unsigned long long v = 0;
-            for (int w = 0; w < kFilterWarps; ++w)
-                v += by_mass ? hmass[w][threadIdx.x] : (unsigned long long)hcnt[w][threadIdx.x];
-            hblk[threadIdx.x] = v;
+        for (int ci = warp; ci < nck; ci += kFilterWarps) {
+            unsigned *h = U.k.hc[ci];
+            const uint32_t sink = (uint32_t)kFKeys + (uint32_t)lane;
+            auto count = [&](uint32_t b16) {  // bf16 bits in the low half: key offset below kmax
+                const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
+                const uint32_t off = kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
+                atomicAdd(&h[off < (uint32_t)kFKeys ? off : sink], 1u);  // no branch: a sink per lane
+            };
+            const int e0 = ci * P.chunk, e1 = min((int)n, e0 + P.chunk);
+            const int v1 = e1 / 8;
+            for (int v = e0 / 8 + lane; v < v1; v += 32) {
+                const uint4 w = reinterpret_cast<const uint4 *>(slice)[v];
+                count(w.x & 0xffffu);
+                count(w.x >> 16);
+                count(w.y & 0xffffu);
+                count(w.y >> 16);
+                count(w.z & 0xffffu);
+                count(w.z >> 16);
+                count(w.w & 0xffffu);
+                count(w.w >> 16);
+            }
+            for (int i = v1 * 8 + lane; i < e1; i += 32)
+                count(reinterpret_cast<const unsigned short *>(slice)[i]);
+        }
+        __syncthreads();
+        // block totals, pushed into every block's gather slot of this rank: one cluster barrier
+        for (int o = threadIdx.x; o < kFKeys; o += blockDim.x) {
+            unsigned tot = 0;
+            for (int ci = 0; ci < nck; ++ci)
+                tot += U.k.hc[ci][o];
+            for (int q = 0; q < csize; ++q)
+                cluster.map_shared_rank(&U.k.gather[0][0], q)[rank * kFKeys + o] = tot;
+            U.k.km[o] = (uint32_t)o < kmax ? fx(x_of<1>(kmax - (uint32_t)o)) : 0ull;
         }
         cluster.sync();
-        if (threadIdx.x < 256) {
-            unsigned long long v = 0;
+        for (int o = threadIdx.x; o < kFKeys; o += blockDim.x) {
+            unsigned tot = 0;
             for (int q = 0; q < csize; ++q)
-                v += *cluster.map_shared_rank(&hblk[threadIdx.x], q);
-            tot[threadIdx.x] = v;
+                tot += U.k.gather[q][o];
+            U.k.bh[o] = tot;
         }
-        cluster.sync();  // every block has read the others' hblk before it is rewritten
-    };
-
-    // ---- 2. top-k: exact key of the k-th largest logit
-    uint32_t tau = 0;
-    if (use_k) {
-        uint32_t prefix = 0, pmask = 0;
-        unsigned long long above = 0;
-        for (int shift = KEY_BITS - 8; shift >= 0; shift -= 8) {
-            radix_level(shift, prefix, pmask, 0u, false);
-            if (threadIdx.x == 0) {
-                unsigned long long a = above;
-                int b = 255;
-                for (; b > 0 && a + tot[b] < (unsigned long long)tk; --b)
-                    a += tot[b];
-                s_bin = (unsigned)b;
-                s_above = a;
+        __syncthreads();
+        auto kmass = [&](int o) -> unsigned long long { return U.k.km[o]; };  // one token at key offset o
+        bool ok = true;
+        int pcut = kFKeys - 1;
+        if (use_k) {
+            find_crossing(S, kFKeys, 0ull, (unsigned long long)tk, [&](int o) { return (unsigned long long)U.k.bh[o]; });
+            ok = S.pos >= 0;  // fewer than k tokens in the window: the general path
+            pcut = S.pos;
+        }
+        if (ok && use_p) {
+            unsigned long long target;
+            const int pk = pcut;
+            if (use_k) {
+                unsigned long long sk = 0;
+                for (int o = threadIdx.x; o <= pk; o += blockDim.x)
+                    sk += (unsigned long long)U.k.bh[o] * kmass(o);
+                target = (unsigned long long)ceil((double)tp * (double)block_sum_u64(S, sk));
+            } else {
+                target = (unsigned long long)ceil((double)tp * S.z);
             }
-            __syncthreads();
-            above = s_above;
-            prefix |= s_bin << shift;
-            pmask |= 255u << shift;
-            __syncthreads();
+            find_crossing(S, kFKeys, 0ull, target,
+                          [&](int o) { return o <= pk ? (unsigned long long)U.k.bh[o] * kmass(o) : 0ull; });
+            if (S.pos >= 0)
+                pcut = S.pos;
+            else
+                ok = use_k;  // with top-k every survivor is counted; top-p alone: the cut lies deeper
         }
-        tau = prefix;
+        if (ok) {
+            thr = kmax - (uint32_t)pcut;
+            for (int ci = warp; ci < nck; ci += kFilterWarps) {
+                const int c = c0 + ci;
+                const float mk = pp[c].x;
+                float mc = -INFINITY, sc = 0.f;
+                if (mk > -INFINITY && key_of<1>(mk) >= thr) {
+                    mc = mk;
+                    const float Mc = mc * cs;
+                    unsigned long long sum = 0;
+                    for (int o = (int)(kmax - key_of<1>(mk)) + lane; o <= pcut; o += 32) {
+                        const unsigned k = U.k.hc[ci][o];
+                        if (k)
+                            sum += (unsigned long long)k * fx_chunk(x_of<1>(kmax - (uint32_t)o), Mc);
+                    }
+                    sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32;
+                }
+                if (lane == 0)
+                    pp[c] = make_float2(mc, sc);
+            }
+            done = true;
+        }
+        __syncthreads();  // the key counts are dead from here on
     }
 
-    // ---- 3. mass of the top-k survivors
-    unsigned long long sk = 0;
-    slice_for_each<DT>(slice, n, [&](float x) {
-        if (key_of<DT>(x) >= tau)
-            sk += fx(x);
-    });
-    sk = warp_sum_u64(sk);
-    if (lane == 0)
-        s_redu[warp] = sk;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned long long v = 0;
-        for (int w = 0; w < kFilterWarps; ++w)
-            v += s_redu[w];
-        s_sum = v;
-    }
-    cluster.sync();
-    unsigned long long Sk = 0;
-    for (int q = 0; q < csize; ++q)
-        Sk += *cluster.map_shared_rank(&s_sum, q);
+    if (!done) {
+        if (DT == 1)
+            cluster.sync();  // every block is done with the one-pass arrays (the same storage)
+        unsigned *cnt = U.g.cnt;
+        auto binof = [&](float x) -> unsigned {  // round(d * kFBinScale), monotone; NaN and -inf last
+            const float f = fmaf(-fmaf(x, cs, -M), kFBinScale, 12582912.f);
+            return min(__float_as_uint(f) - 0x4B400000u, (unsigned)(kFBins - 1));
+        };
+        // least mass of a token of bin b (d <= (b + 1/2) / kFBinScale), with room for rounding
+        auto lo_mass = [&](int b) -> unsigned long long {
+            return b >= kFBins - 1 ? 0ull
+                                   : __float2ull_rz(exp2f(-((float)b + 0.5f) / kFBinScale) * (4294967296.0f * 0.99998f));
+        };
 
-    // ---- 4. top-p: largest key whose tokens at or above it hold >= top_p * S_k
-    uint32_t lam = 0;
-    if (use_p) {
-        const double target = (double)tp * (double)Sk;
-        uint32_t prefix = 0, pmask = 0;
-        unsigned long long above = 0;
-        for (int shift = KEY_BITS - 8; shift >= 0; shift -= 8) {
-            radix_level(shift, prefix, pmask, tau, true);
-            if (threadIdx.x == 0) {
-                unsigned long long a = above;
-                int b = 255;
-                for (; b > 0 && (double)(a + tot[b]) < target; --b)
-                    a += tot[b];
-                s_bin = (unsigned)b;
-                s_above = a;
+        // ---- 1. token counts per bin
+        for (int b = threadIdx.x; b < kFBins; b += blockDim.x)
+            cnt[b] = 0;
+        __syncthreads();
+        slice_for_each<DT>(slice, n, [&](float x, int) { atomicAdd(&cnt[binof(x)], 1u); });
+        cluster_sum_hist(cnt, cluster, csize, kFBins);
+
+        // ---- 2. the last bin that can hold a survivor
+        int bk = kFBins;                // bin of the k-th largest logit (kFBins: no top-k)
+        unsigned long long cabove = 0;  // tokens in the bins before bk
+        int bhi;
+        if (use_k) {
+            find_crossing(S, kFBins, 0ull, (unsigned long long)tk, [&](int i) { return (unsigned long long)cnt[i]; });
+            bk = S.pos < 0 ? kFBins - 1 : S.pos;
+            cabove = S.pos < 0 ? 0ull : S.above;
+            bhi = bk;
+        } else {
+            const unsigned long long target = (unsigned long long)ceil((double)tp * S.z);
+            find_crossing(S, kFBins, 0ull, target, [&](int i) { return (unsigned long long)cnt[i] * lo_mass(i); });
+            bhi = S.pos < 0 ? kFBins - 1 : S.pos;
+        }
+        unsigned long long nl = 0;
+        for (int b = threadIdx.x; b <= bhi; b += blockDim.x)
+            nl += cnt[b];
+        const bool listed = block_sum_u64(S, nl) <= (unsigned long long)kFList;
+
+        // scratch in U.g.local once the lists are merged (or when there are none)
+        uint32_t *wkey = reinterpret_cast<uint32_t *>(U.g.local);       // window keys    [kFWindow]
+        unsigned long long *wmass = U.g.local + kFWindow / 2;            // window weights [kFWindow]
+        unsigned long long *dh = U.g.local + kFWindow / 2 + kFWindow;    // digit histogram [256]
+
+        // The largest key K of the window with above + (weights of window keys >= K) >= target.
+        auto rank_window = [&](unsigned long long above, unsigned long long target) {
+            const int nw = min((int)S.nwin, kFWindow);
+            if (threadIdx.x == 0)
+                S.best = 0;
+            __syncthreads();
+            if ((int)threadIdx.x < nw) {
+                const uint32_t ki = wkey[threadIdx.x];
+                unsigned long long c = above;
+                for (int j = 0; j < nw; ++j)
+                    if (wkey[j] >= ki)
+                        c += wmass[j];
+                if (c >= target)
+                    atomicMax(&S.best, ki);
             }
             __syncthreads();
-            above = s_above;
-            prefix |= s_bin << shift;
-            pmask |= 255u << shift;
-            __syncthreads();
-        }
-        lam = prefix;
-    }
-    const uint32_t thr = max(max(tau, lam), 1u);
-
-    // ---- 5. chunk partials over the surviving tokens, in K1's format
-    for (int c = c0 + warp; c < c1; c += kFilterWarps) {
-        const int64_t e0 = (int64_t)c * P.chunk - lo;
-        const int64_t e1 = min(n, e0 + P.chunk);
-        float mc = -INFINITY;
-        for (int64_t i = e0 + lane; i < e1; i += 32) {
-            const float x = slice_elem<DT>(slice, i);
-            if (key_of<DT>(x) >= thr)
-                mc = fmaxf(mc, x);
-        }
-        mc = warp_max(mc);
-        float sc = 0.f;
-        if (mc > -INFINITY) {
-            const float Mc = mc * cs;
-            for (int64_t i = e0 + lane; i < e1; i += 32) {
-                const float x = slice_elem<DT>(slice, i);
-                if (key_of<DT>(x) >= thr)
-                    sc += ex2(fmaf(x, cs, -Mc));
+            return S.best;
+        };
+        // The same over all the tokens of bin `bin` with key >= lo_key in the slice, by a radix
+        // select on the order key (8-bit digits, one histogram pass each).
+        auto select_in_bin = [&](int bin, uint32_t lo_key, unsigned long long above, unsigned long long target,
+                                 bool by_mass) {
+            uint32_t prefix = 0, pmask = 0;
+            for (int shift = KEY_BITS - 8; shift >= 0; shift -= 8) {
+                __syncthreads();
+                for (int b = threadIdx.x; b < 256; b += blockDim.x)
+                    dh[b] = 0;
+                __syncthreads();
+                slice_for_each<DT>(slice, n, [&](float x, int) {
+                    const uint32_t key = key_of<DT>(x);
+                    if (key >= lo_key && (key & pmask) == prefix && binof(x) == (unsigned)bin)
+                        atomicAdd(&dh[(key >> shift) & 255u], by_mass ? fx(x) : 1ull);
+                });
+                cluster_sum_hist(dh, cluster, csize, 256);
+                find_crossing(S, 256, above, target, [&](int i) { return dh[255 - i]; });
+                const int pos = S.pos;
+                if (pos >= 0)
+                    above = S.above;
+                prefix |= (pos < 0 ? 0u : 255u - (uint32_t)pos) << shift;
+                pmask |= 255u << shift;
             }
-            sc = warp_sum(sc);
+            return prefix;
+        };
+
+        uint32_t tau = 0, lam = 0;
+        if (listed) {
+            // ---- 3. every token up to bin bhi into the cluster's candidate list
+            if (threadIdx.x == 0)
+                S.nlocal = 0;
+            __syncthreads();
+            slice_for_each<DT>(slice, n, [&](float x, int i) {
+                if (binof(x) <= (unsigned)bhi) {
+                    const unsigned j = atomicAdd(&S.nlocal, 1u);
+                    if (j < (unsigned)kFList)
+                        U.g.local[j] = ((unsigned long long)key_of<DT>(x) << 32) | (uint32_t)(lo + i);
+                }
+            });
+            cluster.sync();  // every block's list is complete
+            int off = 0;
+            for (int q = 0; q < csize; ++q) {
+                const int nq = min((int)*cluster.map_shared_rank(&S.nlocal, q), kFList - off);
+                const unsigned long long *lq = cluster.map_shared_rank(U.g.local, q);
+                for (int i = threadIdx.x; i < nq; i += blockDim.x)
+                    U.g.list[off + i] = lq[i];
+                off += nq;
+            }
+            if (threadIdx.x == 0)
+                S.nlist = off;
+            cluster.sync();  // every block has read every list: U.g.local is scratch from here on
+            const int nlst = S.nlist;
+
+            // gather the list's tokens of bin b with key >= lo_key into the window
+            auto gather = [&](int b, uint32_t lo_key, bool by_mass) {
+                if (threadIdx.x == 0)
+                    S.nwin = 0;
+                __syncthreads();
+                for (int j = threadIdx.x; j < nlst; j += blockDim.x) {
+                    const uint32_t key = (uint32_t)(U.g.list[j] >> 32);
+                    const float x = x_of<DT>(key);
+                    if (key >= lo_key && binof(x) == (unsigned)b) {
+                        const unsigned w = atomicAdd(&S.nwin, 1u);
+                        if (w < (unsigned)kFWindow) {
+                            wkey[w] = key;
+                            wmass[w] = by_mass ? fx(x) : 1ull;
+                        }
+                    }
+                }
+                __syncthreads();
+            };
+
+            // ---- 4. top-k
+            if (use_k) {
+                if (cnt[bk] <= (unsigned)kFWindow) {
+                    gather(bk, 0u, false);
+                    tau = rank_window(cabove, (unsigned long long)tk);
+                } else {
+                    tau = select_in_bin(bk, 0u, cabove, (unsigned long long)tk, false);
+                }
+            }
+            // ---- 4. top-p
+            if (use_p) {
+                unsigned long long target;
+                if (use_k) {
+                    unsigned long long sk = 0;
+                    for (int j = threadIdx.x; j < nlst; j += blockDim.x) {
+                        const uint32_t key = (uint32_t)(U.g.list[j] >> 32);
+                        if (key >= tau)
+                            sk += fx(x_of<DT>(key));
+                    }
+                    target = (unsigned long long)ceil((double)tp * (double)block_sum_u64(S, sk));
+                } else {
+                    target = (unsigned long long)ceil((double)tp * S.z);
+                }
+                // exact bin masses of the listed survivors of top-k, as 16-bit halves
+                unsigned *mlo = reinterpret_cast<unsigned *>(U.g.mh), *mhi = mlo + kFBins;
+                __syncthreads();
+                for (int b = threadIdx.x; b < 2 * kFBins; b += blockDim.x)
+                    mlo[b] = 0;
+                __syncthreads();
+                for (int j = threadIdx.x; j < nlst; j += blockDim.x) {
+                    const uint32_t key = (uint32_t)(U.g.list[j] >> 32);
+                    if (key >= tau) {
+                        const float x = x_of<DT>(key);
+                        const unsigned long long w = fx(x);
+                        const unsigned b = binof(x);
+                        atomicAdd(&mlo[b], (unsigned)(w & 0xffffu));
+                        atomicAdd(&mhi[b], (unsigned)(w >> 16));
+                    }
+                }
+                __syncthreads();
+                find_crossing(S, kFBins, 0ull, target,
+                              [&](int i) { return ((unsigned long long)mhi[i] << 16) + (unsigned long long)mlo[i]; });
+                const int bp = S.pos;
+                const unsigned long long pabove = S.above;
+                if (bp >= 0) {
+                    if (cnt[bp] <= (unsigned)kFWindow) {
+                        gather(bp, tau, true);
+                        lam = rank_window(pabove, target);
+                    } else {
+                        lam = select_in_bin(bp, tau, pabove, target, true);
+                    }
+                }
+            }
+        } else {
+            // ---- 3 / 4 over the slice: the list would be too long
+            if (use_k)
+                tau = select_in_bin(bk, 0u, cabove, (unsigned long long)tk, false);
+            if (use_p) {
+                unsigned long long target;
+                if (use_k) {
+                    unsigned long long sk = 0;
+                    slice_for_each<DT>(slice, n, [&](float x, int) {
+                        if (key_of<DT>(x) >= tau)
+                            sk += fx(x);
+                    });
+                    target = (unsigned long long)ceil((double)tp * (double)cluster_sum_u64(S, cluster, csize, sk));
+                } else {
+                    target = (unsigned long long)ceil((double)tp * S.z);
+                }
+                __syncthreads();
+                for (int b = threadIdx.x; b < kFBins; b += blockDim.x)
+                    U.g.mh[b] = 0;
+                __syncthreads();
+                slice_for_each<DT>(slice, n, [&](float x, int) {
+                    if (key_of<DT>(x) >= tau) {
+                        const unsigned long long w = fx(x);
+                        if (w)
+                            atomicAdd(&U.g.mh[binof(x)], w);
+                    }
+                });
+                cluster_sum_hist(U.g.mh, cluster, csize, kFBins);
+                find_crossing(S, kFBins, 0ull, target, [&](int i) { return U.g.mh[i]; });
+                const int bp = S.pos;
+                const unsigned long long pabove = S.above;
+                if (bp >= 0)
+                    lam = select_in_bin(bp, tau, pabove, target, true);
+            }
         }
-        if (lane == 0)
-            P.part[t * P.nchunks + c] = make_float2(mc, mc == -INFINITY ? 0.f : sc);
+        thr = max(max(tau, lam), 1u);
+
+        // ---- 4. chunk partials over the survivors, in K1's format: the kept maximum of a chunk
+        // is K1's chunk maximum when that survives (and the chunk has no survivor otherwise)
+        for (int c = c0 + warp; c < c1; c += kFilterWarps) {
+            const float mk = pp[c].x;
+            float mc = -INFINITY, sc = 0.f;
+            if (mk > -INFINITY && key_of<DT>(mk) >= thr) {
+                mc = mk;
+                const float Mc = mc * cs;
+                unsigned long long sum = 0;
+                if (listed) {
+                    const uint32_t plo = (uint32_t)c * (uint32_t)P.chunk, phi = plo + (uint32_t)P.chunk;
+                    for (int j = lane; j < S.nlist; j += 32) {
+                        const unsigned long long e = U.g.list[j];
+                        const uint32_t key = (uint32_t)(e >> 32), pos = (uint32_t)e;
+                        if (pos >= plo && pos < phi && key >= thr)
+                            sum += fx_chunk(x_of<DT>(key), Mc);
+                    }
+                } else {
+                    const int64_t e0 = (int64_t)c * P.chunk - lo;
+                    slice_range<DT>(slice, e0, min(n, e0 + P.chunk), lane, 32, [&](float x, int) {
+                        if (key_of<DT>(x) >= thr)
+                            sum += fx_chunk(x, Mc);
+                    });
+                }
+                sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32;
+            }
+            if (lane == 0)
+                pp[c] = make_float2(mc, sc);
+        }
     }
     if (rank == 0 && threadIdx.x == 0)
         P.thr[t] = thr;
     if (!landed && threadIdx.x == 0)
         mbar_wait(&bar, 0, P.err);  // do not leave with the copy still in flight
-    cluster.sync();                 // no block leaves while another may still read its shared memory
+    if (!done)
+        cluster.sync();  // no block leaves while another may still read its shared memory (the
+                         // one-pass path reads no other block's memory after its one barrier)
 }
 
 // ---------------------------------------------------------------------------------------
@@ -2064,7 +2489,8 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     const int gridB = (int)((B + kWarps - 1) / kWarps);
     const bool debug = dbg_m || dbg_s || dbg_am || dbg_pd || dbg_z;
 
-    // stage events: [0] before K1, [1] after K1, [2] after K2, [3] after K3
+    // stage events: [0] before K1, then one after each kernel launched: K1, K1F (filtered
+    // calls only), K2, K3 (explicit draft probabilities only)
     int evi = 0;
     auto mark = [&]() {
         if (evi < nev && ev[evi])
@@ -2073,9 +2499,12 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     };
     mark();
     launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
-    if (filtered && T > 0 && B > 0 && launch_filter(DT, P, T, pl.nchunks, stream) != cudaSuccess)
-        return SPEC_ERR_CUDA;
     mark();
+    if (filtered && T > 0 && B > 0) {
+        if (launch_filter(DT, P, T, pl.nchunks, stream) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        mark();
+    }
     if (debug && T > 0 && (dbg_m || dbg_s)) {
         const int g = (int)((T + kWarps - 1) / kWarps);
         if (DT)
@@ -2170,12 +2599,13 @@ spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype lo
                                         const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
                                         const float *uniforms, const float *temperature, int32_t *out_tokens,
                                         int32_t *out_num_accepted, void *workspace, size_t workspace_bytes,
-                                        void *stream, void *const *stage_events, int num_events)
+                                        void *stream, const int32_t *top_k, const float *top_p,
+                                        void *const *stage_events, int num_events)
 {
     return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
                cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
                static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, nullptr, nullptr,
-               reinterpret_cast<cudaEvent_t *>(const_cast<void **>(stage_events)), num_events);
+               reinterpret_cast<cudaEvent_t *>(const_cast<void **>(stage_events)), num_events, top_k, top_p);
 }
 
 spec_status spec_reject_last_device_error(const void *workspace, void *stream, int32_t *error_bits,
@@ -2451,6 +2881,9 @@ const char *spec_reject_status_string(spec_status status)
 
 int spec_reject_version(void) { return 100; }
 
-int spec_reject_num_kernels(int has_draft_probs) { return has_draft_probs ? 3 : 2; }
+int spec_reject_num_kernels(int has_draft_probs, int has_filters)
+{
+    return 2 + (has_draft_probs ? 1 : 0) + (has_filters ? 1 : 0);
+}
 
 }  // extern "C"

@@ -76,3 +76,25 @@ def test_filters_off_give_the_unfiltered_result():
     w2 = dict(w, top_k=np.zeros(w["B"], np.int32), top_p=np.ones(w["B"], np.float32))
     b = PT.run_gpu(w2)
     assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["acc"], b["acc"])
+
+
+def test_profiled_entry_with_filters_matches_filtered_entry():
+    import torch
+    w = W.generate("large-128", top_k=50, top_p=0.9)
+    a = PT.run_gpu(w)
+    dev = torch.device("cuda", 0)
+    d = binding.to_device(w, dev)
+    dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
+    buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, d["draft_probs"] is not None, dev)
+    nk = binding.num_kernels(d["draft_probs"] is not None, True)
+    assert nk == 3 + (d["draft_probs"] is not None)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    stream = torch.cuda.current_stream()
+    for e in ev:
+        e.record(stream)
+    binding.sample_profiled(d, buf, ev, stream, torch.from_numpy(w["top_k"]).to(dev),
+                            torch.from_numpy(w["top_p"]).to(dev))
+    torch.cuda.synchronize()
+    assert np.array_equal(buf.out_tokens.cpu().numpy(), a["tokens"])
+    assert np.array_equal(buf.out_num_accepted.cpu().numpy(), a["acc"])
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(nk))
