@@ -869,32 +869,36 @@ constexpr int kFKeys = SPEC_FILTER_KEYS;      // bf16 one-pass window: the large
 static_assert(kFBins == 4 * kFilterThreads, "bins are owned four per thread");
 static_assert(kFWindow <= kFilterThreads, "one window token per thread");
 
-template <int DT> __device__ __forceinline__ float slice_elem(const unsigned char *sl, int64_t i)
-{
-    if (DT)
-        return __uint_as_float((uint32_t)reinterpret_cast<const unsigned short *>(sl)[i] << 16);
-    return reinterpret_cast<const float *>(sl)[i];
-}
+// This block's part of a target row, read in place (global memory).
+struct RowSlice {
+    const char *p;  // element 0 of the part
+    bool vec;       // 16-byte aligned: 16-byte loads
+};
 
-// fn(x, i) for every element i of sl[e0, e1) with threads tid0, tid0 + step, ...: 16-byte
-// vectors over the aligned middle (e0 a multiple of the vector width), then the scalar tail.
+// fn(x, i) for every element i of the part's [e0, e1) with threads tid0, tid0 + step, ...:
+// 16-byte vectors over the aligned middle (e0 a multiple of the vector width), then the
+// scalar tail; scalar loads throughout when the part is not 16-byte aligned.
 template <int DT, class Fn>
-__device__ __forceinline__ void slice_range(const unsigned char *sl, int64_t e0, int64_t e1, int tid0, int step, Fn fn)
+__device__ __forceinline__ void slice_range(const RowSlice &sl, int64_t e0, int64_t e1, int tid0, int step, Fn fn)
 {
     constexpr int VEC = Elem<DT>::kVec;
-    const int v0 = (int)(e0 / VEC), v1 = (int)(e1 / VEC);
-    for (int v = v0 + tid0; v < v1; v += step) {
-        float x[VEC];
-        unpack<DT>(reinterpret_cast<const uint4 *>(sl)[v], x);
+    int tail0 = (int)e0;
+    if (sl.vec) {
+        const int v0 = (int)(e0 / VEC), v1 = (int)(e1 / VEC);
+        for (int v = v0 + tid0; v < v1; v += step) {
+            float x[VEC];
+            unpack<DT>(ld_stream(sl.p + (size_t)v * 16), x);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            fn(x[e], v * VEC + e);
+            for (int e = 0; e < VEC; ++e)
+                fn(x[e], v * VEC + e);
+        }
+        tail0 = v1 * VEC;
     }
-    for (int i = v1 * VEC + tid0; i < (int)e1; i += step)
-        fn(slice_elem<DT>(sl, i), i);
+    for (int i = tail0 + tid0; i < (int)e1; i += step)
+        fn(load1<DT>(sl.p, i), i);
 }
 
-template <int DT, class Fn> __device__ __forceinline__ void slice_for_each(const unsigned char *sl, int64_t n, Fn fn)
+template <int DT, class Fn> __device__ __forceinline__ void slice_for_each(const RowSlice &sl, int64_t n, Fn fn)
 {
     slice_range<DT>(sl, 0, n, threadIdx.x, blockDim.x, fn);
 }
@@ -920,6 +924,7 @@ struct FilterShared {
     unsigned long long red[kFilterWarps];
     double z;
     float maxv;
+    float cmax[kFilterMaxChunksPerBlock];  // K1's maxima of this block's chunks
     unsigned nlocal;
     int nlist;
     int pos;
@@ -1034,9 +1039,16 @@ __device__ __forceinline__ void find_crossing(FilterShared &S, int nb, unsigned 
     if (lane == 31)
         S.red[warp] = inc;
     __syncthreads();
-    unsigned long long c = above0 + inc - mine;
-    for (int q = 0; q < warp; ++q)
-        c += S.red[q];
+    // exclusive prefix of the warp totals, by a shuffle scan over lanes < number of warps
+    unsigned long long wt = lane < (int)(blockDim.x >> 5) ? S.red[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, wt, o);
+        if (lane >= o)
+            wt += y;
+    }
+    const unsigned long long before = warp > 0 ? __shfl_sync(kFull, wt, warp - 1) : 0ull;
+    unsigned long long c = above0 + before + inc - mine;
     if (b0 < nb && c < target && c + mine >= target)
         for (int k = 0; k < per; ++k) {
             const unsigned long long wk = w(b0 + k);
@@ -1051,14 +1063,12 @@ __device__ __forceinline__ void find_crossing(FilterShared &S, int nb, unsigned 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int csize)
+__global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(Params P, int csize)
 {
     constexpr int KEY_BITS = DT ? 16 : 32;
     constexpr int ES = Elem<DT>::kSize;
-    extern __shared__ __align__(128) unsigned char slice[];
     __shared__ FilterShared S;
     __shared__ FilterArrays U;
-    __shared__ __align__(8) uint64_t bar;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -1085,25 +1095,8 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
     const char *row = row_ptr<DT>(P, t);
     float2 *pp = P.part + t * P.nchunks;
 
-    // ---- 0. the slice into shared memory; meanwhile m (and Z) from K1's partials
-    const uint32_t body =
-        ((reinterpret_cast<uintptr_t>(row + lo * ES) & 15) == 0) ? (uint32_t)((n * ES) & ~(int64_t)15) : 0u;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bar, body);
-        if (body)
-            bulk_g2s(slice, row + lo * ES, body, &bar);
-    }
-    for (int64_t i = body / ES + threadIdx.x; i < n; i += blockDim.x) {  // tail, or a misaligned slice
-        if (DT)
-            reinterpret_cast<unsigned short *>(slice)[i] = reinterpret_cast<const unsigned short *>(row)[lo + i];
-        else
-            reinterpret_cast<float *>(slice)[i] = reinterpret_cast<const float *>(row)[lo + i];
-    }
+    // ---- 0. m (and Z) from K1's partials; the row itself is read in place
+    const RowSlice slice{row + lo * ES, (reinterpret_cast<uintptr_t>(row + lo * ES) & 15) == 0};
     if (warp == 0) {
         float mm = -INFINITY;
         for (int c = lane; c < P.nchunks; c += 32)
@@ -1123,15 +1116,14 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
             S.maxv = mm;
             S.z = z * 4294967296.0;
         }
+        if (lane < c1 - c0)
+            S.cmax[lane] = pp[c0 + lane].x;
     }
-    const bool landed = mbar_wait(&bar, 0, P.err);
     __syncthreads();
     const float m = S.maxv;
     if (!(m > -INFINITY)) {  // no finite logit in the row (the same in every block): no cut
         if (rank == 0 && threadIdx.x == 0)
             P.thr[t] = 0;
-        if (!landed && threadIdx.x == 0)
-            mbar_wait(&bar, 0, P.err);
         return;
     }
     const float M = m * cs;
@@ -1154,18 +1146,25 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
         for (int i = threadIdx.x; i < nck * (kFKeys + 32); i += blockDim.x)
             (&U.k.hc[0][0])[i] = 0u;
         __syncthreads();
+        // When the window holds no negative logit, a token's offset is kmax - 0x8000 minus its raw
+        // bits (negative logits wrap far above the window); otherwise the full order key.
+        const bool plain = kmax >= 0x8000u + (uint32_t)kFKeys;
         for (int ci = warp; ci < nck; ci += kFilterWarps) {
             unsigned *h = U.k.hc[ci];
             const uint32_t sink = (uint32_t)kFKeys + (uint32_t)lane;
-            auto count = [&](uint32_t b16) {  // bf16 bits in the low half: key offset below kmax
-                const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
-                const uint32_t off = kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
-                atomicAdd(&h[off < (uint32_t)kFKeys ? off : sink], 1u);  // no branch: a sink per lane
-            };
             const int e0 = ci * P.chunk, e1 = min((int)n, e0 + P.chunk);
-            const int v1 = e1 / 8;
-            for (int v = e0 / 8 + lane; v < v1; v += 32) {
-                const uint4 w = reinterpret_cast<const uint4 *>(slice)[v];
+            // no branch: offsets outside the window land in this lane's own sink
+            auto count = [&](uint32_t b16) {  // bf16 bits in the low half
+                uint32_t off;
+                if (plain) {
+                    off = kmax - 0x8000u - b16;
+                } else {
+                    const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
+                    off = kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
+                }
+                atomicAdd(&h[min(off, sink)], 1u);
+            };
+            auto count8 = [&](const uint4 &w) {
                 count(w.x & 0xffffu);
                 count(w.x >> 16);
                 count(w.y & 0xffffu);
@@ -1174,9 +1173,25 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
                 count(w.z >> 16);
                 count(w.w & 0xffffu);
                 count(w.w >> 16);
+            };
+            int tail0 = e0;
+            if (slice.vec) {
+                const int v1 = e1 / 8;
+                for (int v = e0 / 8 + lane; v < v1; v += 4 * 32) {  // four 16-byte loads in flight
+                    uint4 w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (v + 32 * u < v1)
+                            w[u] = ld_stream(slice.p + (size_t)(v + 32 * u) * 16);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (v + 32 * u < v1)
+                            count8(w[u]);
+                }
+                tail0 = v1 * 8;
             }
-            for (int i = v1 * 8 + lane; i < e1; i += 32)
-                count(reinterpret_cast<const unsigned short *>(slice)[i]);
+            for (int i = tail0 + lane; i < e1; i += 32)
+                count(__ldg(reinterpret_cast<const unsigned short *>(slice.p) + i));
         }
         __syncthreads();
         // block totals, pushed into every block's gather slot of this rank: one cluster barrier
@@ -1196,48 +1211,79 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
             U.k.bh[o] = tot;
         }
         __syncthreads();
-        auto kmass = [&](int o) -> unsigned long long { return U.k.km[o]; };  // one token at key offset o
-        bool ok = true;
-        int pcut = kFKeys - 1;
-        if (use_k) {
-            find_crossing(S, kFKeys, 0ull, (unsigned long long)tk, [&](int o) { return (unsigned long long)U.k.bh[o]; });
-            ok = S.pos >= 0;  // fewer than k tokens in the window: the general path
-            pcut = S.pos;
-        }
-        if (ok && use_p) {
-            unsigned long long target;
-            const int pk = pcut;
+        // selection by warp 0 alone (lanes own 16 consecutive offsets), published by one barrier
+        if (warp == 0) {
+            constexpr int PER = kFKeys / 32;
+            // first offset o at which w(0) + ... + w(o) >= target (-1 if never), over o <= olim
+            auto crossing = [&](unsigned long long target, int olim, bool by_mass) -> int {
+                const int b0 = lane * PER;
+                unsigned long long mine = 0;
+#pragma unroll 4
+                for (int k = 0; k < PER; ++k)
+                    if (b0 + k <= olim)
+                        mine += by_mass ? (unsigned long long)U.k.bh[b0 + k] * U.k.km[b0 + k]
+                                        : (unsigned long long)U.k.bh[b0 + k];
+                unsigned long long inc = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(kFull, inc, o);
+                    if (lane >= o)
+                        inc += y;
+                }
+                unsigned long long c = inc - mine;
+                int pos = -1;
+                if (c < target && inc >= target)
+                    for (int k = 0; k < PER; ++k) {
+                        c += by_mass ? (unsigned long long)U.k.bh[b0 + k] * U.k.km[b0 + k]
+                                     : (unsigned long long)U.k.bh[b0 + k];
+                        if (c >= target) {
+                            pos = b0 + k;
+                            break;
+                        }
+                    }
+                const unsigned found = __ballot_sync(kFull, pos >= 0);
+                return found ? __shfl_sync(kFull, pos, __ffs(found) - 1) : -1;
+            };
+            bool ok = true;
+            int pcut = kFKeys - 1;
             if (use_k) {
-                unsigned long long sk = 0;
-                for (int o = threadIdx.x; o <= pk; o += blockDim.x)
-                    sk += (unsigned long long)U.k.bh[o] * kmass(o);
-                target = (unsigned long long)ceil((double)tp * (double)block_sum_u64(S, sk));
-            } else {
-                target = (unsigned long long)ceil((double)tp * S.z);
+                pcut = crossing((unsigned long long)tk, kFKeys - 1, false);
+                ok = pcut >= 0;  // fewer than k tokens in the window: the general path
             }
-            find_crossing(S, kFKeys, 0ull, target,
-                          [&](int o) { return o <= pk ? (unsigned long long)U.k.bh[o] * kmass(o) : 0ull; });
-            if (S.pos >= 0)
-                pcut = S.pos;
-            else
-                ok = use_k;  // with top-k every survivor is counted; top-p alone: the cut lies deeper
+            if (ok && use_p) {
+                unsigned long long target;
+                if (use_k) {
+                    unsigned long long sk = 0;
+                    for (int o = lane; o <= pcut; o += 32)
+                        sk += (unsigned long long)U.k.bh[o] * U.k.km[o];
+                    target = (unsigned long long)ceil((double)tp * (double)warp_sum_u64(sk));
+                } else {
+                    target = (unsigned long long)ceil((double)tp * S.z);
+                }
+                const int pp2 = crossing(target, pcut, true);
+                if (pp2 >= 0)
+                    pcut = pp2;
+                else
+                    ok = use_k;  // with top-k every survivor is counted; top-p alone: the cut lies deeper
+            }
+            if (lane == 0)
+                S.pos = ok ? pcut : -1;
         }
-        if (ok) {
+        __syncthreads();
+        const int pcut = S.pos;
+        if (pcut >= 0) {
             thr = kmax - (uint32_t)pcut;
             for (int ci = warp; ci < nck; ci += kFilterWarps) {
                 const int c = c0 + ci;
-                const float mk = pp[c].x;
+                const float mk = S.cmax[ci];
                 float mc = -INFINITY, sc = 0.f;
                 if (mk > -INFINITY && key_of<1>(mk) >= thr) {
+                    // s_c relative to the chunk maximum, from the row-relative fixed-point masses
                     mc = mk;
-                    const float Mc = mc * cs;
                     unsigned long long sum = 0;
-                    for (int o = (int)(kmax - key_of<1>(mk)) + lane; o <= pcut; o += 32) {
-                        const unsigned k = U.k.hc[ci][o];
-                        if (k)
-                            sum += (unsigned long long)k * fx_chunk(x_of<1>(kmax - (uint32_t)o), Mc);
-                    }
-                    sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32;
+                    for (int o = (int)(kmax - key_of<1>(mk)) + lane; o <= pcut; o += 32)
+                        sum += (unsigned long long)U.k.hc[ci][o] * U.k.km[o];
+                    sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32 * ex2(M - mc * cs);
                 }
                 if (lane == 0)
                     pp[c] = make_float2(mc, sc);
@@ -1475,7 +1521,7 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
         // ---- 4. chunk partials over the survivors, in K1's format: the kept maximum of a chunk
         // is K1's chunk maximum when that survives (and the chunk has no survivor otherwise)
         for (int c = c0 + warp; c < c1; c += kFilterWarps) {
-            const float mk = pp[c].x;
+            const float mk = S.cmax[c - c0];
             float mc = -INFINITY, sc = 0.f;
             if (mk > -INFINITY && key_of<DT>(mk) >= thr) {
                 mc = mk;
@@ -1504,8 +1550,6 @@ __global__ void __launch_bounds__(kFilterThreads) filter_kernel(Params P, int cs
     }
     if (rank == 0 && threadIdx.x == 0)
         P.thr[t] = thr;
-    if (!landed && threadIdx.x == 0)
-        mbar_wait(&bar, 0, P.err);  // do not leave with the copy still in flight
     if (!done)
         cluster.sync();  // no block leaves while another may still read its shared memory (the
                          // one-pass path reads no other block's memory after its one barrier)
@@ -2321,8 +2365,9 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
         return e;
     if ((e = cudaFuncSetAttribute(rowstats_wr_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWrSmem)))
         return e;
-    if ((e = cudaFuncSetAttribute(filter_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kFilterMaxChunksPerBlock * kUnitBytes)))
+    // two cut blocks per SM: one block's loads overlap the other's selection
+    if ((e = cudaFuncSetAttribute(filter_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)))
         return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
@@ -2416,7 +2461,8 @@ cudaError_t launch_filter(int DT, const Params &P, int64_t T, int nchunks, cudaS
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(T * csize), 1, 1);
     cfg.blockDim = dim3(kFilterThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)cpc * kUnitBytes;
+    cfg.dynamicSmemBytes = 0;
+    (void)cpc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
