@@ -123,9 +123,9 @@ spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtyp
  * and renormalised; that p' is used for the acceptance test, the recovered token and the
  * bonus token.  top_k[r] <= 0 or >= V, and top_p[r] >= 1 or <= 0, switch a filter off;
  * greedy requests ignore both.  top_k (int32 [B]) and top_p (fp32 [B]) are device arrays,
- * either may be NULL.  Filtered rows are handled by one thread-block cluster per row
- * holding the row in distributed shared memory, which limits V to 8 x 20 chunks (V <=
- * 655360 bf16 or 327680 fp32; SPEC_ERR_UNSUPPORTED beyond).  row_sum and p_draft are
+ * either may be NULL.  Filtered rows are cut by one thread-block cluster per row, at most
+ * 8 blocks of at most 20 chunks of 8 KB, which limits V (V <= 655360 bf16 or 327680 fp32;
+ * SPEC_ERR_UNSUPPORTED beyond).  row_sum and p_draft are
  * optional diagnostic outputs (device fp32 [T] and [T - B]): the restricted normaliser
  * sum over kept tokens of exp((l - m) / T_r) and p'(x*).  Same workspace as
  * spec_reject_sample().
