@@ -221,10 +221,11 @@ template <> __device__ __forceinline__ float x_of<1>(uint32_t key)
     return __uint_as_float((key >= 0x8000u ? key - 0x8000u : 0x8000u | (0x8000u - key)) << 16);
 }
 
-// Whether a token survives the row's top-k / top-p cut (thr = 0: no cut).
-template <int DT> __device__ __forceinline__ bool kept(float x, uint32_t thr)
+// Whether a token survives the row's top-k / top-p cut.  F: the call has cuts (thr = 0 on a
+// row keeps everything, every key being at least 1); without cuts the test compiles away.
+template <int DT, bool F> __device__ __forceinline__ bool kept(float x, uint32_t thr)
 {
-    return thr == 0 || key_of<DT>(x) >= thr;
+    return !F || key_of<DT>(x) >= thr;
 }
 
 template <int DT> __device__ __forceinline__ const char *row_ptr(const Params &P, int64_t t)
@@ -1621,7 +1622,7 @@ __device__ __forceinline__ int warp_combine_argmax(const Params &P, int64_t t, i
 // ---------------------------------------------------------------------------------------
 
 // Mass of the target distribution in units of 2^M: w(v) = 2^(l_v c - M), x* optionally left out.
-template <int DT> struct TargetMass {
+template <int DT, bool F> struct TargetMass {
     const char *row;
     float cs, M;
     int64_t excl;
@@ -1629,7 +1630,7 @@ template <int DT> struct TargetMass {
     __device__ __forceinline__ float one(int64_t v) const
     {
         const float x = load1<DT>(row, v);
-        return (v == excl || !kept<DT>(x, thr)) ? 0.f : ex2(fmaf(x, cs, -M));
+        return (v == excl || !kept<DT, F>(x, thr)) ? 0.f : ex2(fmaf(x, cs, -M));
     }
     // Sum of masses of elements [v0, v1); vector loads where the row is 16-byte aligned.
     __device__ __forceinline__ float range(int64_t v0, int64_t v1) const
@@ -1644,7 +1645,7 @@ template <int DT> struct TargetMass {
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    s[e & 3] += (v + e == excl || !kept<DT>(x[e], thr)) ? 0.f : ex2(fmaf(x[e], cs, -M));
+                    s[e & 3] += (v + e == excl || !kept<DT, F>(x[e], thr)) ? 0.f : ex2(fmaf(x[e], cs, -M));
             }
         }
         float tail = 0.f;
@@ -1655,14 +1656,14 @@ template <int DT> struct TargetMass {
 };
 
 // Explicit-q residual mass r(v) = max(0, 2^(l_v c - M) / S - q(v)) in probability units.
-template <int DT> struct ResidualMass {
+template <int DT, bool F> struct ResidualMass {
     const char *row;
     const float *qrow;
     float cs, M, inv_s;
     uint32_t thr;  // top-k / top-p cut of the row (0 = none)
     __device__ __forceinline__ float pm(float x) const  // target probability of a logit
     {
-        return kept<DT>(x, thr) ? ex2(fmaf(x, cs, -M)) * inv_s : 0.f;
+        return kept<DT, F>(x, thr) ? ex2(fmaf(x, cs, -M)) * inv_s : 0.f;
     }
     __device__ __forceinline__ float one(int64_t v) const
     {
@@ -1814,7 +1815,7 @@ __device__ __forceinline__ int chunk_locate(const CM &cm, int nchunks, float the
 // K2: per-request finalize
 // ---------------------------------------------------------------------------------------
 
-template <int DT>
+template <int DT, bool F>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 {
     const int lane = threadIdx.x & 31;
@@ -1941,7 +1942,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             accept = (xs == am);
         } else {
             const float e = fmaf(ls, cs, -Mi);  // x* is in Si unless the top-k / top-p cut removed it
-            wstar = kept<DT>(ls, thr_i) ? ex2(e) : 0.f;
+            wstar = kept<DT, F>(ls, thr_i) ? ex2(e) : 0.f;
             const double lhs = (double)ua * (double)qs;  // exact
             const float ps = wstar / Si;
             if (ps > 1e-30f || wstar == 0.f)
@@ -1972,7 +1973,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             const float Z = chunk_total(cm, P.nchunks, lane);
             float th;
             const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-            TargetMass<DT> f{row, cs, M, -1, thr};
+            TargetMass<DT, F> f{row, cs, M, -1, thr};
             token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th, lane);
             zdbg = 1.f;
         } else {
@@ -1982,7 +1983,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
             if (!P.q) {  // one-hot draft: residual = p without x*
                 // the chunk holding x*, summed again without it (no cancellation)
                 const int cx = xj / P.chunk;
-                TargetMass<DT> fx{row, cs, Mj, xj, thr};
+                TargetMass<DT, F> fx{row, cs, Mj, xj, thr};
                 const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
                                                  min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
                 ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, Mj, cx, mx};
@@ -1997,7 +1998,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
                 }
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-                TargetMass<DT> f{row, cs, Mj, excl, thr};
+                TargetMass<DT, F> f{row, cs, Mj, excl, thr};
                 token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
                                        lane);
             } else {  // explicit q: K3 / K4 finish this request
@@ -2029,8 +2030,8 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 
 // Residual mass sum max(0, p(v) - q(v)) over the chunk [lo, hi) by one warp: lane-strided
 // 16-byte groups of target logits and draft probabilities, four groups in flight per lane.
-template <int DT>
-__device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT> &f, int64_t lo, int64_t hi, int lane)
+template <int DT, bool F>
+__device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &f, int64_t lo, int64_t hi, int lane)
 {
     constexpr int VEC = Elem<DT>::kVec;
     constexpr int ES = Elem<DT>::kSize;
@@ -2069,7 +2070,7 @@ struct ChunkMassFromL2 {  // masses written by other warps of this launch: read 
 // rpart.  The warp that completes a request's last chunk (a per-request counter, zeroed by
 // K2 in this same call) draws the recovered token from the chunk masses: chunk scan and
 // warp descent as in K2.  No warp waits for another.
-template <int DT>
+template <int DT, bool F>
 __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
 {
     const int lane = threadIdx.x & 31;
@@ -2092,7 +2093,7 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
         const float cs = kLog2e / P.temp[r];
         const char *row = row_ptr<DT>(P, t);
         const uint32_t thr = P.thr ? P.thr[t] : 0u;
-        const ResidualMass<DT> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y, thr};
+        const ResidualMass<DT, F> f{row, P.q + d * P.qstride, cs, st.x, 1.f / st.y, thr};
         const float z = warp_residual_chunk(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk),
                                             lane);
         int last = 0;
@@ -2117,7 +2118,7 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
             const float Zp = chunk_total(cm, P.nchunks, lane);
             float th;
             const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
-            const TargetMass<DT> ft{row, cs, st.x, -1, thr};
+            const TargetMass<DT, F> ft{row, cs, st.x, -1, thr};
             token = (int)warp_find(ft, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th,
                                    lane);
         }
@@ -2372,7 +2373,7 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
         return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT>, kThreads, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
 
 cudaError_t device_info(DeviceInfo **out)
@@ -2559,19 +2560,20 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             debug_soft_kernel<0><<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s);
     }
     if (B > 0) {
+        const bool F = P.thr != nullptr;
         if (DT)
-            finalize_kernel<1><<<gridB, kThreads, 0, stream>>>(P);
+            (F ? finalize_kernel<1, true> : finalize_kernel<1, false>)<<<gridB, kThreads, 0, stream>>>(P);
         else
-            finalize_kernel<0><<<gridB, kThreads, 0, stream>>>(P);
+            (F ? finalize_kernel<0, true> : finalize_kernel<0, false>)<<<gridB, kThreads, 0, stream>>>(P);
         mark();
         if (q) {
             const int64_t runits = (int64_t)B * pl.nchunks;
             const int64_t rfull = (int64_t)di->sms * (di->blocks_residual[DT] > 0 ? di->blocks_residual[DT] : 1);
             const int gridC = (int)clamp_grid(rfull, (runits + kWarps - 1) / kWarps);
             if (DT)
-                residual_kernel<1><<<gridC, kThreads, 0, stream>>>(P);
+                (F ? residual_kernel<1, true> : residual_kernel<1, false>)<<<gridC, kThreads, 0, stream>>>(P);
             else
-                residual_kernel<0><<<gridC, kThreads, 0, stream>>>(P);
+                (F ? residual_kernel<0, true> : residual_kernel<0, false>)<<<gridC, kThreads, 0, stream>>>(P);
             mark();
         }
     }
