@@ -10,6 +10,10 @@ logits, explicit fp32 draft probabilities, temperature 0.7 (2.36 GB of logits +
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (a bounded
 sample of the same workload on the host cores).
+
+`--path tree | ngram | counters` times the other entry points on their own synthetic
+workloads instead (greedy tree verification, the n-gram proposer, the acceptance
+counters), one JSON line each with the same keys.
 """
 from __future__ import annotations
 
@@ -163,6 +167,151 @@ def run_reference(args, w, meta):
     print(json.dumps(line), flush=True)
 
 
+def time_calls(fn, steps, warmup, dev):
+    """Per-call CUDA-event times (ms) of fn on the current stream, with clocks sampled."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    return start.elapsed_time(stop) / steps, [a.elapsed_time(b) for a, b in ev], clocks
+
+
+def bounded(fn, n0, nmax, target_s):
+    """Grow a sample size n until fn(n) takes about target_s / 2 .. target_s seconds."""
+    n = n0
+    while True:
+        n = min(n, nmax)
+        t0 = time.perf_counter()
+        fn(n)
+        dt = time.perf_counter() - t0
+        if dt > target_s / 4 or n >= nmax:
+            return n, dt
+        n = min(nmax, max(n * 2, int(n * (target_s / 2) / max(dt, 1e-3))))
+
+
+def bench_other_path(args):
+    """--path tree | ngram | counters on one GPU (rank 0 of a replica run)."""
+    import torch
+    import __graft_entry__ as G
+    from speculative_decoding_rejection_spec_gb300 import binding, workloads as W
+    G.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+    line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "data": "synthetic"}
+    if args.path == "tree":
+        name = args.workload if args.workload in W.TREE_CONFIGS else "tree-64x64"
+        w = W.generate_tree(name)
+        bf16 = w["dtype"] == "bf16"
+        lg = torch.from_numpy(w["logits"].view(np.int16) if bf16 else w["logits"]).to(dev)
+        if bf16:
+            lg = lg.view(torch.bfloat16)
+        par = torch.from_numpy(w["parent"]).to(dev)
+        tok = torch.from_numpy(w["node_tokens"]).to(dev)
+        cu = torch.from_numpy(w["cu_nodes"]).to(dev)
+        buf = binding.tree_verify_greedy(lg, par, tok, cu)
+        ms, per, clocks = time_calls(lambda: binding.tree_verify_greedy(lg, par, tok, cu, buffers=buf), args.steps,
+                                     args.warmup, dev)
+        es = 2 if bf16 else 4
+        nbytes = w["N"] * w["V"] * es
+        acc = buf[1].cpu().numpy()
+        line.update(metric="verified tree nodes/s (greedy tree verification)", unit="tree nodes/s",
+                    value=w["N"] / (ms / 1e3), ms_per_step=ms, dtype="bf16" if bf16 else "f32",
+                    config={"workload": f"{name}: B={w['B']} trees, N={w['N']} nodes, V={w['V']} "
+                                        f"{w['dtype']} logits, topk<= {w['spec']['topk']}, depth<= {w['spec']['depth']}",
+                            "l2": "inputs larger than L2 (no flush)" if nbytes > 129e6 else "L2-resident inputs"},
+                    mean_accepted_depth=float(acc.mean()), gpu_launches=2 * args.steps, clocks=clocks)
+        achieved = nbytes / (statistics.mean(per) / 1e3) / 1e9
+        line["roofline"] = {"bound": "hbm", "kernel": "whole call (argmax pass over every node row + tree walk)",
+                            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                            "algorithmic_bytes_per_launch": nbytes}
+        if not args.no_cpu:
+            from oracle import tree as otree
+            x64 = (W.bf16_bits_to_f32(w["logits"]) if bf16 else w["logits"])
+
+            def run(n):
+                e = int(w["cu_nodes"][n])
+                otree.verify_batch(x64[:e].astype(np.float64), w["parent"][:e], w["node_tokens"][:e],
+                                   w["cu_nodes"][:n + 1])
+            n, dt = bounded(run, 2, w["B"], 10.0)
+            nodes = int(w["cu_nodes"][n])
+            line["cpu_baseline"] = {"value": nodes / dt, "unit": "tree nodes/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"first {n} of {w['B']} trees ({nodes} nodes), {dt:.2f} s wall"}
+    elif args.path == "ngram":
+        name = args.workload if args.workload in W.NGRAM_CONFIGS else "ngram-1024x4096"
+        g = W.generate_ngram(name)
+        toks = torch.from_numpy(g["tokens"]).to(dev)
+        cu = torch.from_numpy(g["cu_tokens"]).to(dev)
+        out = torch.empty((g["B"], g["k"]), dtype=torch.int32, device=dev)
+        num = torch.empty(g["B"], dtype=torch.int32, device=dev)
+        call = lambda: binding.ngram_propose(toks, cu, g["min_n"], g["max_n"], g["k"], out=out, num=num)
+        ms, per, clocks = time_calls(call, args.steps, args.warmup, dev)
+        nbytes = g["B"] * g["L"] * 4
+        achieved = nbytes / (statistics.mean(per) / 1e3) / 1e9
+        line.update(metric="n-gram proposals/s (one proposal per context)", unit="proposals/s",
+                    value=g["B"] / (ms / 1e3), ms_per_step=ms, dtype="int32",
+                    config={"workload": f"{name}: B={g['B']} contexts of L={g['L']} tokens, n={g['min_n']}..{g['max_n']}, "
+                                        f"k={g['k']}", "l2": "L2-resident inputs (16 MB)"},
+                    hit_rate=float((num.cpu().numpy() > 0).mean()), context_tokens_per_s=g["B"] * g["L"] / (ms / 1e3),
+                    gpu_launches=args.steps, clocks=clocks)
+        line["roofline"] = {"bound": "hbm", "kernel": "ngram_kernel (block per context, candidate starts in parallel)",
+                            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                            "algorithmic_bytes_per_launch": nbytes}
+        if not args.no_cpu:
+            from oracle import ngram as ong
+
+            def run(n):
+                ong.propose_batch(g["tokens"][:n * g["L"]], g["cu_tokens"][:n + 1], g["min_n"], g["max_n"], g["k"])
+            n, dt = bounded(run, 8, g["B"], 10.0)
+            line["cpu_baseline"] = {"value": n / dt, "unit": "proposals/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"first {n} of {g['B']} contexts, {dt:.2f} s wall"}
+    else:  # counters
+        name = args.workload if args.workload in W.CONFIGS else "large-1024"
+        spec = W.CONFIGS[name]
+        B = spec["B"]
+        rng = np.random.default_rng(5)
+        ks = np.full(B, spec["K"], np.int32) if spec["K"] != "ragged" else rng.integers(0, spec["K_max"] + 1, B)
+        cu_h = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+        acc_h = rng.integers(0, np.maximum(ks, 0) + 1).astype(np.int32)
+        cu = torch.from_numpy(cu_h).to(dev)
+        acc = torch.from_numpy(acc_h).to(dev)
+        ctr = torch.zeros(binding.METRIC_COUNT, dtype=torch.int64, device=dev)
+        ms, per, clocks = time_calls(lambda: binding.metrics_update(cu, acc, ctr), args.steps, args.warmup, dev)
+        nbytes = (2 * B + 1) * 4
+        achieved = nbytes / (statistics.mean(per) / 1e3) / 1e9
+        line.update(metric="requests counted/s (acceptance counters update)", unit="requests/s",
+                    value=B / (ms / 1e3), ms_per_step=ms, dtype="int64",
+                    config={"workload": f"{name}: B={B} requests", "l2": "L2-resident inputs"},
+                    gpu_launches=args.steps, clocks=clocks)
+        line["roofline"] = {"bound": "hbm", "kernel": "metrics_kernel (launch-bound: a few KB per call)",
+                            "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 6), "peak_kind": peak_kind, "traffic": None,
+                            "algorithmic_bytes_per_launch": nbytes}
+        if not args.no_cpu:
+            from oracle import closed_forms as cf
+            n, dt = bounded(lambda n: [cf.acceptance_counters(cu_h, acc_h) for _ in range(n)], 1, 10 ** 6, 4.0)
+            line["cpu_baseline"] = {"value": n * B / dt, "unit": "requests/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{n} updates of {B} requests, {dt:.2f} s wall"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -174,6 +323,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--top-k", type=int, default=None, help="top-k on the target, every request")
     ap.add_argument("--top-p", type=float, default=None, help="top-p on the target, every request")
+    ap.add_argument("--path", default="sample", choices=["sample", "tree", "ngram", "counters"],
+                    help="entry point to time: the sampler (default) or one of the other calls")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -181,6 +332,10 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference" and rank != 0:
         return  # the reference arm runs on rank 0 only
+    if args.path != "sample":
+        if rank == 0 and args.impl == "ours":
+            bench_other_path(args)
+        return
     spec = W.CONFIGS[args.workload]
     meta = {"workload": f"{args.workload}: B={spec['B']} K={spec['K']} V={spec['V']} {spec['dtype']} logits, "
                         f"{'explicit fp32 draft probs' if spec['draft'] in ('noisy_q', 'target_q') else 'one-hot drafts'}"

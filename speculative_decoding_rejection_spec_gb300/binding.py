@@ -253,15 +253,19 @@ def accept_rate_and_length(counters) -> tuple[float, float]:
             (c[METRIC_NUM_ACCEPTED_TOKENS] + c[METRIC_NUM_VERIFIES]) / max(c[METRIC_NUM_VERIFIES], 1))
 
 
-def ngram_propose(tokens, cu_tokens, min_n: int, max_n: int, k: int, max_model_len: int = 0, stream=None):
+def ngram_propose(tokens, cu_tokens, min_n: int, max_n: int, k: int, max_model_len: int = 0, stream=None,
+                  out=None, num=None):
     """n-gram draft proposals for a batch of contexts (device int32 tokens, int64 offsets [B + 1]).
 
-    Returns (drafts int32 [B, k] padded with -1, counts int32 [B]).
+    Returns (drafts int32 [B, k] padded with -1, counts int32 [B]); ``out`` / ``num`` may be
+    given to reuse device buffers.
     """
     import torch
     B = int(cu_tokens.shape[0]) - 1
-    out = torch.empty((B, k), dtype=torch.int32, device=tokens.device)
-    num = torch.empty(B, dtype=torch.int32, device=tokens.device)
+    if out is None:
+        out = torch.empty((B, k), dtype=torch.int32, device=tokens.device)
+    if num is None:
+        num = torch.empty(B, dtype=torch.int32, device=tokens.device)
     st = load().spec_ngram_propose(_ptr(tokens), _ptr(cu_tokens), B, int(min_n), int(max_n), int(k),
                                    int(max_model_len), _ptr(out), _ptr(num), _stream(stream))
     if st != 0:
@@ -269,10 +273,11 @@ def ngram_propose(tokens, cu_tokens, min_n: int, max_n: int, k: int, max_model_l
     return out, num
 
 
-def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None):
+def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None, buffers=None):
     """Greedy tree verification on device tensors.
 
-    Returns (out_tokens [N], out_num_accepted [B], out_last_node [B], workspace).
+    Returns (out_tokens [N], out_num_accepted [B], out_last_node [B], workspace); passing that
+    tuple back as ``buffers`` reuses it.
     """
     import torch
     N, V = int(target_logits.shape[0]), int(target_logits.shape[1])
@@ -282,10 +287,13 @@ def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None
     n_ws = load().spec_tree_workspace_size(N, B, V, dt)
     if n_ws == 0:
         raise ValueError("invalid sizes for spec_tree_workspace_size")
-    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
-    out = torch.empty(N, dtype=torch.int32, device=dev)
-    acc = torch.empty(B, dtype=torch.int32, device=dev)
-    last = torch.empty(B, dtype=torch.int32, device=dev)
+    if buffers is not None:
+        out, acc, last, ws = buffers
+    else:
+        ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+        out = torch.empty(N, dtype=torch.int32, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        last = torch.empty(B, dtype=torch.int32, device=dev)
     st = load().spec_tree_verify_greedy(_ptr(target_logits), dt, N, V, _row_stride(target_logits), _ptr(parent),
                                         _ptr(node_tokens), _ptr(cu_nodes), B, _ptr(out), _ptr(acc), _ptr(last),
                                         _ptr(ws), n_ws, _stream(stream))

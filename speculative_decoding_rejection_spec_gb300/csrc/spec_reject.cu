@@ -670,29 +670,41 @@ __device__ __forceinline__ void softmax_regs(const Params &P, int64_t t, int c, 
         P.part[t * P.nchunks + c] = make_float2(mw, mw == -INFINITY ? 0.f : sw);
 }
 
+// Greedy rows: (max, lowest index of the max) of one unit held in registers.  Two passes with
+// independent operations: a max tree, then the least index equal to the warp's maximum (a
+// compare-and-select chain over 128 elements would serialise on its own latency).  A unit of
+// -inf only keeps the index unset (INT_MAX), as a running "x > best" scan would.
 template <int DT>
 __device__ __forceinline__ void argmax_regs(const Params &P, int64_t t, int c, int lane, const uint4 (&v)[kVecPerLane],
                                             const UnitRange &R, const char *row)
 {
     constexpr int VEC = Elem<DT>::kVec;
-    ArgAcc acc;
+    const bool has_tail = lane < R.hi - R.vhi;
+    const float xt = has_tail ? load1<DT>(row, R.vhi + lane) : -INFINITY;
+    float m = xt;
 #pragma unroll
-    for (int k = 0; k < kVecPerLane; ++k) {
-        const int64_t vi = (int64_t)k * 32 + lane;
-        if (vi < R.nvec) {
+    for (int k = 0; k < kVecPerLane; ++k)
+        m = fmaxf(m, vec_max<DT>(v[k]));  // vectors past the unit hold -inf
+    const float mw = warp_max(m);
+    int idx = INT_MAX;
+    if (mw > -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
             float x[VEC];
             unpack<DT>(v[k], x);
-            const int v0 = (int)(R.vlo + vi * VEC);
+            const int v0 = (int)(R.vlo + ((int64_t)k * 32 + lane) * VEC);
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
-                acc.add(x[e], v0 + e);
+                idx = min(idx, x[e] == mw ? v0 + e : INT_MAX);
         }
+        if (xt == mw)
+            idx = min(idx, (int)(R.vhi + lane));
     }
-    if (lane < R.hi - R.vhi)
-        acc.add(load1<DT>(row, R.vhi + lane), (int)(R.vhi + lane));
-    warp_argmax(acc.best, acc.idx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        idx = min(idx, __shfl_xor_sync(kFull, idx, o));
     if (lane == 0)
-        P.part[t * P.nchunks + c] = make_float2(acc.best, __int_as_float(acc.idx));
+        P.part[t * P.nchunks + c] = make_float2(mw, __int_as_float(idx));
 }
 
 // ---------------------------------------------------------------------------------------

@@ -203,3 +203,104 @@ def generate(spec: dict | str, seed: int | None = None, threads: int | None = No
 def total_drafts(w: dict) -> int:
     """Number of verified draft positions, sum_r k_r."""
     return int(w["cu_num_draft"][-1])
+
+
+# ---------------------------------------------------------------------------------------
+# Draft trees (greedy tree verification) and n-gram contexts
+# ---------------------------------------------------------------------------------------
+
+# EAGLE-style draft trees: up to `topk` children per node, up to `depth` levels, at most
+# `max_nodes` nodes per request (root included), one target row per node.
+TREE_CONFIGS = {
+    "tree-64x64": dict(B=64, max_nodes=64, topk=4, depth=6, V=128256, dtype="bf16", sigma=3.0, lead=30.0,
+                       p_follow=0.5, seed=21),
+    "tree-256x64": dict(B=256, max_nodes=64, topk=4, depth=6, V=128256, dtype="bf16", sigma=3.0, lead=30.0,
+                        p_follow=0.5, seed=22),
+}
+
+
+def generate_tree(spec: dict | str, seed: int | None = None) -> dict:
+    """Draft trees with one target row per node.
+
+    Each node row is N(0, sigma^2) with one planted lead token set to ``lead`` (10 sigma:
+    the row's largest logit by construction); a child's token is its parent's lead token
+    with probability ``p_follow``, else uniform, so walks go several levels deep.  Nodes are
+    in topological order with node 0 of each request its root (parent -1, token 0).
+    """
+    if isinstance(spec, str):
+        spec = TREE_CONFIGS[spec]
+    spec = dict(spec)
+    seed = spec["seed"] if seed is None else seed
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    B, V = spec["B"], spec["V"]
+    parents, toks, cu = [], [], [0]
+    for _ in range(B):
+        par, lvl = [-1], [0]
+        i = 0
+        while i < len(par) and len(par) < spec["max_nodes"]:
+            if lvl[i] < spec["depth"]:
+                for _c in range(int(rng.integers(1, spec["topk"] + 1))):
+                    if len(par) >= spec["max_nodes"]:
+                        break
+                    par.append(i)
+                    lvl.append(lvl[i] + 1)
+            i += 1
+        parents.append(np.array(par, np.int32))
+        cu.append(cu[-1] + len(par))
+    N = cu[-1]
+    lead = rng.integers(0, V, size=N).astype(np.int32)
+    node_tokens = np.zeros(N, np.int32)
+    for r in range(B):
+        base = cu[r]
+        par = parents[r]
+        for j in range(1, len(par)):
+            follow = rng.random() < spec["p_follow"]
+            node_tokens[base + j] = lead[base + par[j]] if follow else int(rng.integers(0, V))
+    bf16 = spec["dtype"] == "bf16"
+    logits = np.empty((N, V), np.uint16 if bf16 else np.float32)
+
+    def fill(b0):
+        b1 = min(N, b0 + ROWS_PER_BLOCK)
+        x = (_rng(seed, 40, b0 // ROWS_PER_BLOCK).standard_normal((b1 - b0, V)) * spec["sigma"]).astype(np.float32)
+        x[np.arange(b1 - b0), lead[b0:b1]] = spec["lead"]
+        logits[b0:b1] = f32_to_bf16_bits(x) if bf16 else x
+
+    with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(0, N, ROWS_PER_BLOCK)))
+    parent = np.concatenate(parents).astype(np.int32)
+    return dict(logits=logits, parent=parent, node_tokens=node_tokens, cu_nodes=np.array(cu, np.int32), B=B, N=N,
+                V=V, dtype=spec["dtype"], spec=spec)
+
+
+# Token contexts for the n-gram proposer: random tokens with planted repeats of earlier spans,
+# so that the final n-gram often occurs earlier in the context.
+NGRAM_CONFIGS = {
+    "ngram-1024x4096": dict(B=1024, L=4096, vocab=32000, span=(4, 64), p_copy=0.3, min_n=2, max_n=5, k=8, seed=31),
+}
+
+
+def generate_ngram(spec: dict | str, seed: int | None = None) -> dict:
+    """B contexts of L tokens: spans of fresh tokens, and with probability ``p_copy`` copies
+    of an earlier span of the same context."""
+    if isinstance(spec, str):
+        spec = NGRAM_CONFIGS[spec]
+    spec = dict(spec)
+    seed = spec["seed"] if seed is None else seed
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 9]))
+    B, L = spec["B"], spec["L"]
+    lo, hi = spec["span"]
+    out = np.empty(B * L, np.int32)
+    for r in range(B):
+        ctx = np.empty(L, np.int32)
+        n = 0
+        while n < L:
+            m = int(min(L - n, rng.integers(lo, hi + 1)))
+            if n > hi and rng.random() < spec["p_copy"]:
+                s = int(rng.integers(0, n - m + 1))
+                ctx[n:n + m] = ctx[s:s + m]
+            else:
+                ctx[n:n + m] = rng.integers(0, spec["vocab"], size=m)
+            n += m
+        out[r * L:(r + 1) * L] = ctx
+    cu = (np.arange(B + 1, dtype=np.int64) * L)
+    return dict(tokens=out, cu_tokens=cu, B=B, L=L, min_n=spec["min_n"], max_n=spec["max_n"], k=spec["k"], spec=spec)
