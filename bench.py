@@ -304,6 +304,15 @@ def bench_other_path(args):
                             "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
                             "frac": round(achieved / peak, 6), "peak_kind": peak_kind, "traffic": None,
                             "algorithmic_bytes_per_launch": nbytes}
+        # the fused form: the same counters added inside the sampler's finalize pass
+        wl = W.generate("large-128")
+        dd = binding.to_device(wl, dev)
+        bufs = binding.make_buffers(wl["B"], wl["T"], wl["V"], binding.BF16, dd["draft_probs"] is not None, dev)
+        plain_ms, _, _ = time_calls(lambda: binding.sample_ex(**dd, buffers=bufs), args.steps, args.warmup, dev)
+        fused_ms, _, _ = time_calls(lambda: binding.sample_ex(**dd, counters=ctr, buffers=bufs), args.steps,
+                                    args.warmup, dev)
+        line["fused"] = {"workload": "large-128 sampler call", "call_ms_without_counters": round(plain_ms, 4),
+                         "call_ms_with_counters": round(fused_ms, 4), "extra_launches": 0}
         if not args.no_cpu:
             from oracle import closed_forms as cf
             n, dt = bounded(lambda n: [cf.acceptance_counters(cu_h, acc_h) for _ in range(n)], 1, 10 ** 6, 4.0)

@@ -183,6 +183,38 @@ spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype log
                                        float *p_draft, float *z_out);
 
 /*
+ * Options of spec_reject_sample_ex(); a NULL pointer switches the option off, and a NULL
+ * options pointer is spec_reject_sample().
+ *   top_k, top_p       device int32 [B] / fp32 [B]: top-k / top-p on the target, exactly as
+ *                      spec_reject_sample_filtered() (same readings and limits)
+ *   counters           device int64 [SPEC_METRIC_COUNT], 8-byte aligned: this call's acceptance
+ *                      counters are added to it inside the per-request finalize pass (no extra
+ *                      launch), with the definitions and the result of
+ *                      spec_reject_metrics_update() on the call's outputs (vLLM's spec_decode_*
+ *                      counters of "第12章 投机解码：以小博大" §12.7.5)
+ *   row_sum, p_draft   diagnostics as in spec_reject_sample_filtered()
+ */
+typedef struct spec_reject_options {
+    const int32_t *top_k;
+    const float *top_p;
+    int64_t *counters;
+    float *row_sum;
+    float *p_draft;
+} spec_reject_options;
+
+/*
+ * spec_reject_sample() with options (see spec_reject_options).  Same arguments, workspace,
+ * errors and asynchrony as spec_reject_sample(); a misaligned counters pointer is
+ * SPEC_ERR_INVALID_ARG.
+ */
+spec_status spec_reject_sample_ex(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                  int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                  const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                  const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                  int32_t *out_num_accepted, void *workspace, size_t workspace_bytes, void *stream,
+                                  const spec_reject_options *options);
+
+/*
  * Measurement form of spec_reject_sample() / spec_reject_sample_filtered() (top_k and top_p
  * may be NULL): identical work, plus cudaEventRecord of caller-created events (cudaEvent_t
  * handles) on `stream`: stage_events[0] before the first kernel, then one after each kernel

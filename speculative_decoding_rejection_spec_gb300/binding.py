@@ -25,8 +25,14 @@ EXPORTED = [
     "spec_reject_host_arena_size", "spec_reject_sample_host", "spec_reject_debug_rowstats",
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
     "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
-    "spec_tree_workspace_size", "spec_tree_verify_greedy", "spec_reject_sample_filtered",
+    "spec_tree_workspace_size", "spec_tree_verify_greedy", "spec_reject_sample_filtered", "spec_reject_sample_ex",
 ]
+
+
+class Options(ctypes.Structure):
+    """spec_reject_options (device pointers; None = off)."""
+    _fields_ = [("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p), ("counters", ctypes.c_void_p),
+                ("row_sum", ctypes.c_void_p), ("p_draft", ctypes.c_void_p)]
 METRIC_NUM_DRAFTS, METRIC_NUM_DRAFT_TOKENS, METRIC_NUM_ACCEPTED_TOKENS, METRIC_NUM_VERIFIES = 0, 1, 2, 3
 METRIC_ACCEPTED_PER_POS = 4
 METRIC_COUNT = 4 + MAX_SPEC_LEN
@@ -81,6 +87,8 @@ def load():
     lib.spec_reject_sample_filtered.restype = ctypes.c_int
     lib.spec_reject_sample_filtered.argtypes = [P, ctypes.c_int, i64, i32, i64, P, i64, P, P, i32, P, P, P, P, P, P,
                                                 P, sz, P, P, P]
+    lib.spec_reject_sample_ex.restype = ctypes.c_int
+    lib.spec_reject_sample_ex.argtypes = sample_args + [P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int]
     _lib = lib
@@ -332,6 +340,33 @@ def sample_filtered(target_logits, draft_ids, cu_num_draft, uniforms, temperatur
         int(buffers.workspace.numel()), _stream(stream), _ptr(rs), _ptr(pdr))
     if st != 0:
         raise SpecRejectError(st, "spec_reject_sample_filtered")
+    return buffers.out_tokens, buffers.out_num_accepted
+
+
+def sample_ex(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *, top_k=None,
+              top_p=None, counters=None, buffers: Buffers | None = None, stream=None, debug: dict | None = None):
+    """``sample`` with options: top-k / top-p as ``sample_filtered`` and ``counters`` (device int64
+    [METRIC_COUNT]) to which this call's acceptance counters are added inside the finalize pass."""
+    import torch
+    T, V = int(target_logits.shape[0]), int(target_logits.shape[1])
+    B = int(cu_num_draft.shape[0]) - 1
+    dt = _dtype_code(target_logits)
+    if buffers is None:
+        buffers = make_buffers(B, T, V, dt, draft_probs is not None, target_logits.device)
+    qs = 0 if draft_probs is None else _row_stride(draft_probs)
+    rs = pdr = None
+    if debug is not None:
+        rs = torch.full((T,), float("nan"), device=target_logits.device)
+        pdr = torch.full((max(T - B, 0),), float("nan"), device=target_logits.device)
+        debug.update(row_sum=rs, p_draft=pdr)
+    opts = Options(_ptr(top_k), _ptr(top_p), _ptr(counters), _ptr(rs), _ptr(pdr))
+    st = load().spec_reject_sample_ex(
+        _ptr(target_logits), dt, T, V, _row_stride(target_logits), _ptr(draft_probs), qs, _ptr(draft_ids),
+        _ptr(cu_num_draft), B, _ptr(uniforms), _ptr(temperature), _ptr(buffers.out_tokens),
+        _ptr(buffers.out_num_accepted), _ptr(buffers.workspace), int(buffers.workspace.numel()), _stream(stream),
+        ctypes.byref(opts))
+    if st != 0:
+        raise SpecRejectError(st, "spec_reject_sample_ex")
     return buffers.out_tokens, buffers.out_num_accepted
 
 

@@ -121,6 +121,7 @@ struct Params {
     // top-k / top-p restriction of the target (all null without filters)
     const int32_t *top_k;  // [B]
     const float *top_p;    // [B]
+    unsigned long long *counters;  // [SPEC_METRIC_COUNT] acceptance counters to add to, or null
     uint32_t *thr;         // [T] order key below which a token is cut (0 = none)
     // diagnostics (all may be null)
     float *dbg_pdraft;
@@ -2029,6 +2030,18 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
         if (P.dbg_z && !pending)
             P.dbg_z[r] = zdbg;
     }
+    if (P.counters) {  // this request's share of the acceptance counters (integer sums: order-free)
+        unsigned long long *C = P.counters;
+        if (lane == 0) {
+            if (k > 0)
+                atomicAdd(C + SPEC_METRIC_NUM_DRAFTS, 1ull);
+            atomicAdd(C + SPEC_METRIC_NUM_DRAFT_TOKENS, (unsigned long long)k);
+            atomicAdd(C + SPEC_METRIC_NUM_ACCEPTED_TOKENS, (unsigned long long)j);
+            atomicAdd(C + SPEC_METRIC_NUM_VERIFIES, 1ull);
+        }
+        if (lane < j)
+            atomicAdd(C + SPEC_METRIC_ACCEPTED_PER_POS + lane, 1ull);
+    }
     for (int i = lane; i <= k; i += 32) {
         if (i == j && pending)
             continue;
@@ -2491,7 +2504,8 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 int64_t qstride, const int32_t *ids, const int32_t *cu, int32_t B, const float *uni,
                 const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
                 cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
-                cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr)
+                cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr,
+                int64_t *counters = nullptr)
 {
     spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
     if (st != SPEC_OK)
@@ -2529,6 +2543,9 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     P.chunk = pl.chunk;
     P.nchunks = pl.nchunks;
     P.dbg_pdraft = dbg_pd;
+    if (counters && !aligned(counters, 8))
+        return SPEC_ERR_INVALID_ARG;
+    P.counters = reinterpret_cast<unsigned long long *>(counters);
     P.dbg_z = dbg_z;
     const bool filtered = top_k || top_p;
     if (filtered) {
@@ -2639,6 +2656,21 @@ spec_status spec_reject_sample_filtered(const void *target_logits, spec_dtype lo
                cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
                static_cast<cudaStream_t>(stream), nullptr, row_sum, nullptr, p_draft, nullptr, nullptr, 0, top_k,
                top_p);
+}
+
+spec_status spec_reject_sample_ex(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                  int64_t logits_row_stride, const float *draft_probs, int64_t q_row_stride,
+                                  const int32_t *draft_ids, const int32_t *cu_num_draft, int32_t B,
+                                  const float *uniforms, const float *temperature, int32_t *out_tokens,
+                                  int32_t *out_num_accepted, void *workspace, size_t workspace_bytes, void *stream,
+                                  const spec_reject_options *options)
+{
+    const spec_reject_options none = {};
+    const spec_reject_options &o = options ? *options : none;
+    return run(target_logits, logits_dtype, T, V, logits_row_stride, draft_probs, q_row_stride, draft_ids,
+               cu_num_draft, B, uniforms, temperature, out_tokens, out_num_accepted, workspace, workspace_bytes,
+               static_cast<cudaStream_t>(stream), nullptr, o.row_sum, nullptr, o.p_draft, nullptr, nullptr, 0,
+               o.top_k, o.top_p, o.counters);
 }
 
 spec_status spec_reject_debug_rowstats(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,

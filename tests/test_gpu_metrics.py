@@ -48,3 +48,41 @@ def test_metrics_of_sampler_outputs_match_oracle(name):
     diff = np.abs(np.array(got) - np.array(want))
     assert diff.sum() <= 2 * int((gpu["acc"] != ref.num_accepted).sum()) * 33, (got, want)
     assert got == cf.acceptance_counters(w["cu_num_draft"], gpu["acc"])
+
+
+@pytest.mark.parametrize("name,filters", [("deterministic", None), ("large-128", None), ("large-128", (50, 0.9)),
+                                          ("greedy", None), ("tiny", None)])
+def test_counters_fused_into_the_call(name, filters):
+    """spec_reject_sample_ex with counters: the finalize pass adds exactly what
+    spec_reject_metrics_update computes from the call's outputs (and the oracle's counters on them)."""
+    import torch
+    w = W.generate(name) if filters is None else W.generate(name, top_k=filters[0], top_p=filters[1])
+    d = binding.to_device(w, "cuda")
+    kw = {}
+    if filters is not None:
+        kw = dict(top_k=torch.from_numpy(w["top_k"]).cuda(), top_p=torch.from_numpy(w["top_p"]).cuda())
+    fused = torch.zeros(binding.METRIC_COUNT, dtype=torch.int64, device="cuda")
+    fused[:] = 7  # accumulates onto what is there
+    tok, acc = binding.sample_ex(**d, counters=fused, **kw)
+    separate = torch.full((binding.METRIC_COUNT,), 7, dtype=torch.int64, device="cuda")
+    binding.metrics_update(d["cu_num_draft"], acc, separate)
+    assert fused.cpu().tolist() == separate.cpu().tolist()
+    want = [x + 7 for x in cf.acceptance_counters(w["cu_num_draft"], acc.cpu().numpy())]
+    assert fused.cpu().tolist() == want
+    # the same tokens as the call without counters
+    ref_tok, ref_acc = binding.sample_ex(**d, **kw)
+    assert torch.equal(tok, ref_tok) and torch.equal(acc, ref_acc)
+
+
+def test_counters_skip_invalid_requests():
+    import torch
+    w = W.generate("tiny")
+    ids = w["draft_ids"].copy()
+    ids[0] = w["V"] + 5  # request 0 invalid
+    w = dict(w, draft_ids=ids)
+    d = binding.to_device(w, "cuda")
+    fused = torch.zeros(binding.METRIC_COUNT, dtype=torch.int64, device="cuda")
+    tok, acc = binding.sample_ex(**d, counters=fused)
+    a = acc.cpu().numpy()
+    assert a[0] == -1
+    assert fused.cpu().tolist() == cf.acceptance_counters(w["cu_num_draft"], a)
