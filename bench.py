@@ -489,11 +489,25 @@ def e2e(w, dev, args):
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / steps
-    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if not k.startswith("out_"))
+    # bytes that cross the host link per step: every input copied, except pinned draft
+    # probabilities, which the kernels read in place (one 32-byte sector per q(x*) gather and
+    # the whole row at each rejecting request's first rejection)
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items()
+              if not k.startswith("out_") and k != "draft_probs")
+    q_note = None
+    if has_q:
+        acc = host["out_num_accepted"].numpy()
+        ks = np.diff(w["cu_num_draft"])
+        rejecting = int(((acc >= 0) & (acc < ks)).sum())
+        h2d += rejecting * w["V"] * 4 + 32 * (w["T"] - w["B"])
+        q_note = f"draft probabilities read in place from pinned memory: {rejecting} rows + {w['T'] - w['B']} gathers"
     d2h = 4 * (w["T"] + w["B"])
     from speculative_decoding_rejection_spec_gb300 import workloads as W
-    return {"value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+    out = {"value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+    if q_note:
+        out["note"] = q_note
+    return out
 
 
 if __name__ == "__main__":

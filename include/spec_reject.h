@@ -153,7 +153,10 @@ spec_status spec_reject_last_device_error(const void *workspace, void *stream, i
  * caller-provided device arena, runs the sampler and copies out_tokens and
  * out_num_accepted back.  Synchronous: returns after the host outputs are
  * written (or on the first error).  Host pointers may be pageable or pinned;
- * pinned memory copies fastest.  Rows are passed with the same strides as the
+ * pinned memory copies fastest.  draft_probs in pinned (page-locked, device-mapped)
+ * memory is not copied: the kernels read in place, over the host link, only what the
+ * method needs (q(x*) of each verify row and the row at each request's first
+ * rejection); pageable draft_probs is copied whole.  Rows are passed with the same strides as the
  * device form (0 = aliasing is not allowed here: strides must be >= V).
  * `device_arena` must hold spec_reject_host_arena_size() bytes.
  */

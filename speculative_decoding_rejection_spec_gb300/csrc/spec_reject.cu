@@ -2774,6 +2774,18 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     const size_t ws_bytes = arena_bytes - (size_t)(d_ws - reinterpret_cast<char *>(device_arena));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Draft probabilities in pinned, mapped host memory are read in place over the host link:
+    // the kernels touch only q(x*) of each verify row and the row at each request's first
+    // rejection, a small part of the [T - B, V] array.  Pageable memory is copied whole.
+    const float *q_in_place = nullptr;
+    if (has_q) {
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, draft_probs) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer)
+            q_in_place = static_cast<const float *>(pa.devicePointer);
+        else
+            (void)cudaGetLastError();
+    }
     // one cudaMemcpyAsync per buffer
     const struct {
         void *dst;
@@ -2781,7 +2793,7 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
         size_t bytes;
     } in[] = {
         {d_logits, target_logits, es * (size_t)T * (size_t)V},
-        {d_q, draft_probs, has_q ? 4 * (size_t)(T - B) * (size_t)V : 0},
+        {d_q, draft_probs, has_q && !q_in_place ? 4 * (size_t)(T - B) * (size_t)V : 0},
         {d_ids, draft_ids, 4 * (size_t)(T - B)},
         {d_cu, cu_num_draft, 4 * (size_t)(B + 1)},
         {d_uni, uniforms, 8 * (size_t)T},
@@ -2790,8 +2802,8 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     for (const auto &c : in)
         if (c.bytes && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return SPEC_ERR_CUDA;
-    spec_status st = spec_reject_sample(d_logits, logits_dtype, T, V, V, has_q ? d_q : nullptr, V, d_ids, d_cu, B,
-                                        d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, stream);
+    spec_status st = spec_reject_sample(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr,
+                                        V, d_ids, d_cu, B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, stream);
     if (st != SPEC_OK)
         return st;
     if ((T && cudaMemcpyAsync(out_tokens, d_tok, 4 * (size_t)T, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||

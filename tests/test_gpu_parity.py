@@ -276,3 +276,34 @@ def test_host_entry_matches_device_entry():
         tok, acc = binding.sample_host(w["logits"], w["draft_ids"], w["cu_num_draft"], w["uniforms"],
                                        w["temperature"], w["draft_probs"], arena)
         assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "large-128"])
+def test_host_entry_reads_pinned_draft_probs_in_place(name):
+    """Pinned draft probabilities are read in place by the kernels (no copy): the result is
+    the device entry's, bit for bit, and the oracle's on unflagged requests."""
+    import torch
+    w = W.generate(name)
+    dev = PT.run_gpu(w)
+
+    def pinned(a):
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+
+    host = {k: pinned(w[k]) for k in ("logits", "draft_probs", "draft_ids", "cu_num_draft", "uniforms",
+                                      "temperature")}
+    host["out_tokens"] = torch.full((w["T"],), -7, dtype=torch.int32).pin_memory()
+    host["out_num_accepted"] = torch.full((w["B"],), -7, dtype=torch.int32).pin_memory()
+    ptrs = {k: v.data_ptr() for k, v in host.items()}
+    dt = PT.dtype_code(w)
+    arena = torch.full((binding.host_arena_size(w["B"], w["T"], w["V"], dt, True),), 0xA5, dtype=torch.uint8,
+                       device="cuda")
+    binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena)
+    tok, acc = host["out_tokens"].numpy(), host["out_num_accepted"].numpy()
+    assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
+    # the arena's region for a copy of q (right after the logits, 256-byte aligned) was never
+    # written: the kernels read q in place
+    es = 2 if w["dtype"] == "bf16" else 4
+    base = (-arena.data_ptr()) % 256
+    q0 = base + ((es * w["T"] * w["V"] + 255) // 256) * 256
+    qregion = arena[q0:q0 + 4 * (w["T"] - w["B"]) * w["V"]]
+    assert bool((qregion == 0xA5).all())
