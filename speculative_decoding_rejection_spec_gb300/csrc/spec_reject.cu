@@ -2156,6 +2156,53 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
 }
 
 // ---------------------------------------------------------------------------------------
+// Staging of the draft rows the residual pass reads, when q lives in host memory
+// ---------------------------------------------------------------------------------------
+
+// For every request r whose explicit-q recovery is pending (rstate[r] = j >= 0), copies draft
+// row d = cu[r] + j of q (host memory, read over the host link) to row d of `stage` (device
+// memory, row stride V).  Warps over (request, 16 KB piece) units with eight 16-byte loads in
+// flight per lane: one streaming pass over exactly the rows K3 reads.  K3 reading q in place
+// interleaves those host loads with its own arithmetic and moves half the bandwidth.
+__global__ void __launch_bounds__(kThreads) stage_rows_kernel(Params P, float *stage)
+{
+    constexpr int kPiece = 4096;  // floats per unit
+    constexpr int kUnroll = 8;
+    const int lane = threadIdx.x & 31;
+    const int per = (P.V + kPiece - 1) / kPiece;
+    const int64_t nunits = (int64_t)P.B * per;
+    const bool vec = ((reinterpret_cast<uintptr_t>(P.q) | reinterpret_cast<uintptr_t>(stage)) & 15) == 0 &&
+                     (P.qstride & 3) == 0 && (P.V & 3) == 0;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < nunits; u += (int64_t)gridDim.x * kWarps) {
+        const int r = (int)(u / per);
+        const int c = (int)(u - (int64_t)r * per);
+        const int j = P.rstate[r];
+        if (j < 0)
+            continue;
+        const int64_t d = (int64_t)P.cu[r] + j;
+        const float *src = P.q + d * P.qstride;
+        float *dst = stage + d * (int64_t)P.V;
+        const int v0 = c * kPiece, v1 = min(P.V, v0 + kPiece);
+        if (vec) {
+            for (int v = v0 + 4 * lane; v < v1; v += 4 * 32 * kUnroll) {
+                uint4 x[kUnroll];
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k)
+                    if (v + 128 * k < v1)
+                        x[k] = ld_stream(src + v + 128 * k);
+#pragma unroll
+                for (int k = 0; k < kUnroll; ++k)
+                    if (v + 128 * k < v1)
+                        *reinterpret_cast<uint4 *>(dst + v + 128 * k) = x[k];
+            }
+        } else {
+            for (int v = v0 + lane; v < v1; v += 32)
+                dst[v] = __ldg(src + v);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // Acceptance counters (vLLM's spec_decode_* counters, SGLang's accept rate / length)
 // ---------------------------------------------------------------------------------------
 
@@ -2505,7 +2552,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
                 cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
                 cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr,
-                int64_t *counters = nullptr)
+                int64_t *counters = nullptr, float *q_stage = nullptr)
 {
     spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
     if (st != SPEC_OK)
@@ -2596,13 +2643,21 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             (F ? finalize_kernel<0, true> : finalize_kernel<0, false>)<<<gridB, kThreads, 0, stream>>>(P);
         mark();
         if (q) {
+            Params P3 = P;
+            if (q_stage) {  // q in host memory: stage the rows K3 reads into device memory first
+                const int64_t sunits = (int64_t)B * ((V + 4095) / 4096);
+                const int gridS = (int)clamp_grid((int64_t)di->sms * 8, (sunits + kWarps - 1) / kWarps);
+                stage_rows_kernel<<<gridS, kThreads, 0, stream>>>(P, q_stage);
+                P3.q = q_stage;
+                P3.qstride = V;
+            }
             const int64_t runits = (int64_t)B * pl.nchunks;
             const int64_t rfull = (int64_t)di->sms * (di->blocks_residual[DT] > 0 ? di->blocks_residual[DT] : 1);
             const int gridC = (int)clamp_grid(rfull, (runits + kWarps - 1) / kWarps);
             if (DT)
-                (F ? residual_kernel<1, true> : residual_kernel<1, false>)<<<gridC, kThreads, 0, stream>>>(P);
+                (F ? residual_kernel<1, true> : residual_kernel<1, false>)<<<gridC, kThreads, 0, stream>>>(P3);
             else
-                (F ? residual_kernel<0, true> : residual_kernel<0, false>)<<<gridC, kThreads, 0, stream>>>(P);
+                (F ? residual_kernel<0, true> : residual_kernel<0, false>)<<<gridC, kThreads, 0, stream>>>(P3);
             mark();
         }
     }
@@ -2802,8 +2857,11 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     for (const auto &c : in)
         if (c.bytes && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
             return SPEC_ERR_CUDA;
-    spec_status st = spec_reject_sample(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr,
-                                        V, d_ids, d_cu, B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, stream);
+    // q in place: K2 reads q(x*) over the link, then the rows K3 needs are staged into the
+    // arena's q region (the rest of it stays unwritten)
+    spec_status st = run(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr, V, d_ids,
+                         d_cu, B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, nullptr, 0, nullptr, nullptr, nullptr, q_in_place ? d_q : nullptr);
     if (st != SPEC_OK)
         return st;
     if ((T && cudaMemcpyAsync(out_tokens, d_tok, 4 * (size_t)T, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||

@@ -300,10 +300,15 @@ def test_host_entry_reads_pinned_draft_probs_in_place(name):
     binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena)
     tok, acc = host["out_tokens"].numpy(), host["out_num_accepted"].numpy()
     assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
-    # the arena's region for a copy of q (right after the logits, 256-byte aligned) was never
-    # written: the kernels read q in place
+    # q was not copied: the arena's region for a copy of q (right after the logits, 256-byte
+    # aligned) holds only the rows staged for the residual pass, at most one per request, each
+    # equal to its row of q
     es = 2 if w["dtype"] == "bf16" else 4
     base = (-arena.data_ptr()) % 256
     q0 = base + ((es * w["T"] * w["V"] + 255) // 256) * 256
-    qregion = arena[q0:q0 + 4 * (w["T"] - w["B"]) * w["V"]]
-    assert bool((qregion == 0xA5).all())
+    nd, V = w["T"] - w["B"], w["V"]
+    qregion = arena[q0:q0 + 4 * nd * V].view(nd, 4 * V)
+    written = torch.nonzero((qregion != 0xA5).any(dim=1)).flatten().cpu().numpy()
+    assert 0 < len(written) <= w["B"]
+    qbytes = torch.from_numpy(w["draft_probs"].view(np.uint8).reshape(nd, 4 * V)[written]).cuda()
+    assert torch.equal(qregion[torch.from_numpy(written).cuda()], qbytes)
