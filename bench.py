@@ -53,8 +53,13 @@ def peaks():
 
 
 def source_sha():
+    """Hash of the kernel source up to the end of the row-statistics kernel (K1 and everything
+    it can use are defined before that point; later code cannot change it)."""
     with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+        src = f.read()
+    marker = b"// K1F: top-k / top-p cut"
+    cut = src.find(marker)
+    return hashlib.sha256(src if cut < 0 else src[:cut]).hexdigest()[:16]
 
 
 def traffic_for(workload):
