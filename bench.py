@@ -52,13 +52,14 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_sha():
-    """Hash of the kernel source up to the end of the row-statistics kernel (K1 and everything
-    it can use are defined before that point; later code cannot change it)."""
+def source_sha(full=False):
+    """Hash of the kernel source: by default up to the end of the row-statistics kernel (K1 and
+    everything it can use are defined before that point; later code cannot change it), with
+    full=True the whole file."""
     with open(KERNEL_SOURCE, "rb") as f:
         src = f.read()
     marker = b"// K1F: top-k / top-p cut"
-    cut = src.find(marker)
+    cut = -1 if full else src.find(marker)
     return hashlib.sha256(src if cut < 0 else src[:cut]).hexdigest()[:16]
 
 
@@ -74,6 +75,19 @@ def traffic_for(workload):
         return None
     per_unit = e.get("dram_bytes_per_row")
     return None if per_unit is None else per_unit
+
+
+def traffic_lazy_for(workload):
+    """DRAM bytes per launch of KL on this workload from the committed ncu summary, only if it
+    was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get("lazy", {})
+    if e.get("source_sha") != source_sha(full=True):
+        return None
+    return e.get("dram_bytes_per_launch", {}).get(workload)
 
 
 class ClockSampler:
@@ -381,7 +395,8 @@ def main():
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, has_q, dev)
     tk = None if w.get("top_k") is None else torch.from_numpy(w["top_k"]).to(dev)
     tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).to(dev)
-    nk = binding.num_kernels(has_q, filtered)
+    nk = binding.num_kernels(w["B"], has_q, filtered)
+    lazy = binding.reads_to_first_rejection(w["B"], filtered)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in ev:
@@ -416,40 +431,57 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms = total_ms / args.steps
-    k1 = [row[0].elapsed_time(row[1]) for row in ev]
     stage_ms = [statistics.mean(row[i].elapsed_time(row[i + 1]) for row in ev) for i in range(nk)]
     positions = W.total_drafts(w)
     value = positions * world / (ms / 1e3)
 
-    # roofline of the dominant kernel (row statistics: every target logit read once)
     es = 2 if w["dtype"] == "bf16" else 4
-    k1_bytes = w["T"] * w["V"] * es + 4 * (w["T"] - w["B"])
-    k1_s = statistics.mean(k1) / 1e3
-    peak, peak_kind = peaks()
-    achieved = k1_bytes / k1_s / 1e9
-    tr = traffic_for(args.workload)
-    roofline = {"bound": "hbm", "kernel": "row statistics (K1: rowstats_wr_kernel, warp-private TMA pipelines)",
-                "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                "traffic": None if tr is None else int(tr * w["T"]),
-                "algorithmic_bytes_per_launch": k1_bytes, "ms_per_launch": round(1e3 * k1_s, 4),
-                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
-    # whole-call algorithmic bytes (logits once + q rows at rejected positions + small vectors)
     acc = buf.out_num_accepted.cpu().numpy()
     ks = np.diff(w["cu_num_draft"])
-    rejecting = int(((acc >= 0) & (acc < ks)).sum()) if has_q else 0
-    call_bytes = (w["T"] * w["V"] * es + rejecting * w["V"] * 4 + 8 * (w["T"] - w["B"]) + 12 * w["T"]
-                  + 4 * (2 * w["B"] + 1))
+    valid = acc >= 0
+    rejecting = int((valid & (acc < ks)).sum()) if has_q else 0
+    small = 8 * (w["T"] - w["B"]) + 12 * w["T"] + 4 * (2 * w["B"] + 1)
+    all_rows_bytes = w["T"] * w["V"] * es + rejecting * w["V"] * 4 + small  # every target row once
+    peak, peak_kind = peaks()
+    if not lazy:
+        # K1 reads every target row (and with cuts, the cut kernel re-reads the filtered ones)
+        stages = (["rowstats"] + (["topk_topp_cut"] if filtered else []) + ["finalize"]
+                  + (["residual"] if has_q else []))
+        dom = 0
+        dom_bytes = w["T"] * w["V"] * es + 4 * (w["T"] - w["B"])
+        dom_name = "row statistics (K1: rowstats_wr_kernel, warp-private TMA pipelines)"
+        tr = traffic_for(args.workload)
+        traffic = None if tr is None else int(tr * w["T"])
+        call_bytes = all_rows_bytes
+    else:
+        # KL reads each request's target rows up to its output row (the first rejection, or the
+        # bonus row) and, on an explicit-q rejection, that draft row
+        stages = ["layout_check", "rows_to_first_rejection"]
+        dom = 1
+        rows_read = int((acc[valid] + 1).sum())
+        dom_bytes = rows_read * w["V"] * es + rejecting * w["V"] * 4 + small
+        dom_name = ("KL: lazy_kernel (request queue, rows streamed through warp-private TMA rings up to "
+                    "the first rejection, draw in the same block)")
+        traffic = traffic_lazy_for(args.workload)
+        call_bytes = dom_bytes
+    dom_s = statistics.mean(row[dom].elapsed_time(row[dom + 1]) for row in ev) / 1e3
+    achieved = dom_bytes / dom_s / 1e9
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": round(1e3 * dom_s, 4),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
             "hbm_gbs_effective": round(call_bytes / (ms / 1e3) / 1e9, 1),
-            "stage_ms": [round(x, 4) for x in stage_ms],
-            "stages": ["rowstats"] + (["topk_topp_cut"] if filtered else []) + ["finalize"]
-                      + (["residual"] if has_q else []),
+            "all_rows_gbs_equivalent": round(all_rows_bytes / (ms / 1e3) / 1e9, 1),
+            "stage_ms": [round(x, 4) for x in stage_ms], "stages": stages,
             "rows_per_s": w["T"] * world / (ms / 1e3),
             "roofline": roofline, "gpu_launches": nk * args.steps, "clocks": clocks}
+    if lazy:
+        line["rows_read_per_step"] = rows_read
+        line["rows_total"] = int(w["T"])
 
     if not args.no_e2e and not filtered:  # the host-buffer entry point takes no filters
         line["e2e"] = e2e(w, dev, args)

@@ -221,9 +221,12 @@ spec_status spec_reject_sample_ex(const void *target_logits, spec_dtype logits_d
  * Measurement form of spec_reject_sample() / spec_reject_sample_filtered() (top_k and top_p
  * may be NULL): identical work, plus cudaEventRecord of caller-created events (cudaEvent_t
  * handles) on `stream`: stage_events[0] before the first kernel, then one after each kernel
- * launched, in order: row statistics, the top-k / top-p cut (filtered calls only), the
- * per-request finalize, the residual / recovery pass (with draft_probs only).  Entries
- * beyond num_events, or NULL entries, are skipped.
+ * launched, in order.  Calls without cuts of at least 64 requests on 16-byte-aligned rows: the
+ * layout check, then the pass that reads rows up to each first rejection and draws the
+ * outputs.  Otherwise: row
+ * statistics, the top-k / top-p cut (filtered calls only), the per-request finalize, the
+ * residual / recovery pass (with draft_probs only).  Entries beyond num_events, or NULL
+ * entries, are skipped.
  * The pages have no counterpart: this exists to time each kernel on its own stream.
  */
 spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
@@ -338,8 +341,11 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
                                int32_t max_n, int32_t k, int64_t max_model_len, int32_t *out_drafts,
                                int32_t *out_num_drafts, void *stream);
 
-/* Kernels one call launches: 2, plus 1 with draft probabilities, plus 1 with top-k / top-p. */
-int spec_reject_num_kernels(int has_draft_probs, int has_filters);
+/* Kernels one call of B requests on 16-byte-aligned rows launches: 2 without top-k / top-p
+ * when B >= 64 (the layout check, then the pass that reads rows up to each first rejection);
+ * otherwise row statistics and the finalize (2), plus the top-k / top-p cut with filters, plus
+ * the residual pass with draft probabilities. */
+int spec_reject_num_kernels(int32_t B, int has_draft_probs, int has_filters);
 
 /* Static description of a status code. */
 const char *spec_reject_status_string(spec_status status);

@@ -90,7 +90,7 @@ def load():
     lib.spec_reject_sample_ex.restype = ctypes.c_int
     lib.spec_reject_sample_ex.argtypes = sample_args + [P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
-    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int32, ctypes.c_int, ctypes.c_int]
     _lib = lib
     return lib
 
@@ -310,8 +310,15 @@ def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None
     return out, acc, last, ws
 
 
-def num_kernels(has_draft_probs: bool, has_filters: bool = False) -> int:
-    return int(load().spec_reject_num_kernels(int(bool(has_draft_probs)), int(bool(has_filters))))
+def num_kernels(B: int, has_draft_probs: bool, has_filters: bool = False) -> int:
+    """Kernels one call of B requests launches (16-byte-aligned rows)."""
+    return int(load().spec_reject_num_kernels(int(B), int(bool(has_draft_probs)), int(bool(has_filters))))
+
+
+def reads_to_first_rejection(B: int, has_filters: bool = False) -> bool:
+    """Whether a call of B requests takes the pass that reads rows up to each first rejection."""
+    return not has_filters and int(load().spec_reject_num_kernels(int(B), 0, 0)) == 2 and \
+        int(load().spec_reject_num_kernels(int(B), 1, 0)) == 2
 
 
 def sample_filtered(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *,

@@ -614,6 +614,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return false;
 }
 
+
 // One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), its
 // completion counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -629,8 +630,8 @@ constexpr int kVecPerLane = kUnitBytes / 16 / 32;  // 16-byte vectors of a unit 
 // Softmax partial of a unit held in registers: v[k] is body vector k * 32 + lane (slots
 // past the body hold -inf), the scalar tail comes from global memory.
 template <int DT>
-__device__ __forceinline__ void softmax_regs(const Params &P, int64_t t, int c, float cs, int lane,
-                                             const uint4 (&v)[kVecPerLane], const UnitRange &R, const char *row)
+__device__ __forceinline__ void softmax_regs(float2 *out, float cs, int lane, const uint4 (&v)[kVecPerLane],
+                                             const UnitRange &R, const char *row)
 {
     constexpr int VEC = Elem<DT>::kVec;
     float xt = -INFINITY;
@@ -668,7 +669,7 @@ __device__ __forceinline__ void softmax_regs(const Params &P, int64_t t, int c, 
     const float sl = (m == -INFINITY) ? 0.f : s * ex2(M - Mw);
     const float sw = warp_sum(sl);
     if (lane == 0)
-        P.part[t * P.nchunks + c] = make_float2(mw, mw == -INFINITY ? 0.f : sw);
+        *out = make_float2(mw, mw == -INFINITY ? 0.f : sw);
 }
 
 // Greedy rows: (max, lowest index of the max) of one unit held in registers.  Two passes with
@@ -676,8 +677,8 @@ __device__ __forceinline__ void softmax_regs(const Params &P, int64_t t, int c, 
 // compare-and-select chain over 128 elements would serialise on its own latency).  A unit of
 // -inf only keeps the index unset (INT_MAX), as a running "x > best" scan would.
 template <int DT>
-__device__ __forceinline__ void argmax_regs(const Params &P, int64_t t, int c, int lane, const uint4 (&v)[kVecPerLane],
-                                            const UnitRange &R, const char *row)
+__device__ __forceinline__ void argmax_regs(float2 *out, int lane, const uint4 (&v)[kVecPerLane], const UnitRange &R,
+                                            const char *row)
 {
     constexpr int VEC = Elem<DT>::kVec;
     const bool has_tail = lane < R.hi - R.vhi;
@@ -705,7 +706,7 @@ __device__ __forceinline__ void argmax_regs(const Params &P, int64_t t, int c, i
     for (int o = 16; o > 0; o >>= 1)
         idx = min(idx, __shfl_xor_sync(kFull, idx, o));
     if (lane == 0)
-        P.part[t * P.nchunks + c] = make_float2(mw, __int_as_float(idx));
+        *out = make_float2(mw, __int_as_float(idx));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -821,9 +822,9 @@ __global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_ke
         }
         const char *row = row_ptr<DT>(P, t);
         if (greedy)
-            argmax_regs<DT>(P, t, c, lane, v, R, row);
+            argmax_regs<DT>(P.part + t * P.nchunks + c, lane, v, R, row);
         else
-            softmax_regs<DT>(P, t, c, cs, lane, v, R, row);
+            softmax_regs<DT>(P.part + t * P.nchunks + c, cs, lane, v, R, row);
         if (++c == P.nchunks) {
             c = 0;
             ++t;
@@ -878,6 +879,9 @@ constexpr int kFList = 2048;                  // candidate list entries (per blo
 constexpr int kFWindow = 512;                 // tokens of one bin ranked directly
 #ifndef SPEC_FILTER_KEYS
 #define SPEC_FILTER_KEYS 512
+#endif
+#ifndef SPEC_FILTER_LOADS
+#define SPEC_FILTER_LOADS 4  // 16-byte loads in flight per lane in the one-pass count
 #endif
 constexpr int kFKeys = SPEC_FILTER_KEYS;      // bf16 one-pass window: the largest keys counted
 static_assert(kFBins == 4 * kFilterThreads, "bins are owned four per thread");
@@ -1190,15 +1194,16 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(Params P, int
             };
             int tail0 = e0;
             if (slice.vec) {
+                constexpr int NL = SPEC_FILTER_LOADS;
                 const int v1 = e1 / 8;
-                for (int v = e0 / 8 + lane; v < v1; v += 4 * 32) {  // four 16-byte loads in flight
-                    uint4 w[4];
+                for (int v = e0 / 8 + lane; v < v1; v += NL * 32) {  // NL 16-byte loads in flight
+                    uint4 w[NL];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < NL; ++u)
                         if (v + 32 * u < v1)
                             w[u] = ld_stream(slice.p + (size_t)(v + 32 * u) * 16);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < NL; ++u)
                         if (v + 32 * u < v1)
                             count8(w[u]);
                 }
@@ -1225,6 +1230,39 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(Params P, int
             U.k.bh[o] = tot;
         }
         __syncthreads();
+#ifdef SPEC_FILTER_BLOCK_SELECT
+        {
+            bool ok = true;
+            int pcut = kFKeys - 1;
+            if (use_k) {
+                find_crossing(S, kFKeys, 0ull, (unsigned long long)tk,
+                              [&](int o) { return (unsigned long long)U.k.bh[o]; });
+                ok = S.pos >= 0;
+                pcut = S.pos;
+            }
+            if (ok && use_p) {
+                unsigned long long target;
+                const int pk = pcut;
+                if (use_k) {
+                    unsigned long long sk = 0;
+                    for (int o = threadIdx.x; o <= pk; o += blockDim.x)
+                        sk += (unsigned long long)U.k.bh[o] * U.k.km[o];
+                    target = (unsigned long long)ceil((double)tp * (double)block_sum_u64(S, sk));
+                } else {
+                    target = (unsigned long long)ceil((double)tp * S.z);
+                }
+                find_crossing(S, kFKeys, 0ull, target,
+                              [&](int o) { return o <= pk ? (unsigned long long)U.k.bh[o] * U.k.km[o] : 0ull; });
+                if (S.pos >= 0)
+                    pcut = S.pos;
+                else
+                    ok = use_k;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0)
+                S.pos = ok ? pcut : -1;
+        }
+#else
         // selection by warp 0 alone (lanes own 16 consecutive offsets), published by one barrier
         if (warp == 0) {
             constexpr int PER = kFKeys / 32;
@@ -1283,6 +1321,7 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(Params P, int
             if (lane == 0)
                 S.pos = ok ? pcut : -1;
         }
+#endif
         __syncthreads();
         const int pcut = S.pos;
         if (pcut >= 0) {
@@ -1592,11 +1631,11 @@ __device__ __forceinline__ int lane_combine_argmax(const Params &P, int64_t t, f
 }
 
 // Warp combine of one row's softmax partials (lanes over chunks).
-__device__ __forceinline__ void warp_combine_soft(const Params &P, int64_t t, float cs, int lane, float &M, float &S)
+__device__ __forceinline__ void warp_combine_soft(const float2 *pp, int nchunks, float cs, int lane, float &M,
+                                                  float &S)
 {
-    const float2 *pp = P.part + t * P.nchunks;
     float m = -INFINITY;
-    for (int c = lane; c < P.nchunks; c += 32) {
+    for (int c = lane; c < nchunks; c += 32) {
         const float x = pp[c].x;
         m = fmaxf(m, x);
     }
@@ -1604,7 +1643,7 @@ __device__ __forceinline__ void warp_combine_soft(const Params &P, int64_t t, fl
     M = m * cs;
     float s = 0.f;
     if (m > -INFINITY) {
-        for (int c = lane; c < P.nchunks; c += 32) {
+        for (int c = lane; c < nchunks; c += 32) {
             const float2 pc = pp[c];
             if (pc.x != -INFINITY)
                 s += pc.y * ex2(pc.x * cs - M);
@@ -1613,12 +1652,11 @@ __device__ __forceinline__ void warp_combine_soft(const Params &P, int64_t t, fl
     S = warp_sum(s);
 }
 
-__device__ __forceinline__ int warp_combine_argmax(const Params &P, int64_t t, int lane)
+__device__ __forceinline__ int warp_combine_argmax(const float2 *pp, int nchunks, int lane)
 {
-    const float2 *pp = P.part + t * P.nchunks;
     float best = -INFINITY;
     int idx = INT_MAX;
-    for (int c = lane; c < P.nchunks; c += 32) {
+    for (int c = lane; c < nchunks; c += 32) {
         const float2 pc = pp[c];
         const int i = __float_as_int(pc.y);
         if (pc.x > best || (pc.x == best && i < idx)) {
@@ -1653,6 +1691,7 @@ template <int DT, bool F> struct TargetMass {
         int64_t v = v0;
         const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0);
         if (aligned) {
+#pragma unroll 8
             for (; v + VEC <= v1; v += VEC) {
                 float x[VEC];
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
@@ -1690,6 +1729,7 @@ template <int DT, bool F> struct ResidualMass {
         const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0) &&
                              ((reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0);
         if (aligned) {
+#pragma unroll 8
             for (; v + VEC <= v1; v += VEC) {
                 float x[VEC];
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
@@ -1974,14 +2014,14 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
     bool pending = false;
     float zdbg = 0.f;
     if (greedy) {
-        token = (j < k) ? __shfl_sync(kFull, am, j) : warp_combine_argmax(P, tj, lane);
+        token = (j < k) ? __shfl_sync(kFull, am, j) : warp_combine_argmax(P.part + tj * P.nchunks, P.nchunks, lane);
     } else {
         const float us = P.uni[2 * tj + 1];
         const char *row = row_ptr<DT>(P, tj);
         const uint32_t thr = P.thr ? P.thr[tj] : 0u;
         if (j == k) {  // bonus: draw from p
             float M, S;
-            warp_combine_soft(P, tj, cs, lane, M, S);
+            warp_combine_soft(P.part + tj * P.nchunks, P.nchunks, cs, lane, M, S);
             ChunkMassFromPartials cm{P.part + tj * P.nchunks, cs, M, -1, 0.f};
             const float Z = chunk_total(cm, P.nchunks, lane);
             float th;
@@ -2055,7 +2095,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 
 // Residual mass sum max(0, p(v) - q(v)) over the chunk [lo, hi) by one warp: lane-strided
 // 16-byte groups of target logits and draft probabilities, four groups in flight per lane.
-template <int DT, bool F>
+template <int DT, bool F, int U = 4>
 __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &f, int64_t lo, int64_t hi, int lane)
 {
     constexpr int VEC = Elem<DT>::kVec;
@@ -2064,7 +2104,7 @@ __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &
     int64_t tail = lo;
     if (((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo)) & 15) == 0) {
         const int64_t ng = (hi - lo) / VEC;
-#pragma unroll 4
+#pragma unroll(U)
         for (int64_t g = lane; g < ng; g += 32) {
             const int64_t v = lo + g * VEC;
             float x[VEC];
@@ -2153,6 +2193,343 @@ __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
                 P.dbg_z[r] = Z > 0.f ? Z : 0.f;
         }
     }
+}
+
+// ---------------------------------------------------------------------------------------
+// KL: calls without top-k / top-p, target rows read only up to each request's first rejection
+// ---------------------------------------------------------------------------------------
+//
+// The acceptance test at draft position i needs target row t_i alone, and the test stops at
+// the first rejection, so no row after it can change the result.  KL walks each request's
+// rows in order: a block takes the next request from a queue, streams row t_i through its
+// warps' TMA rings into chunk partials in shared memory (K1's per-unit reduction), decides
+// position i with K2's arithmetic, and stops at the first rejection (or, every draft
+// accepted, after the bonus row).  The output token is drawn in the same block: K2's chunk
+// scan and warp descent, and for explicit draft probabilities K3's residual chunk masses over
+// the rejected row, by all warps.  A request costs j + 1 target rows (j = its output
+// position) and, on an explicit-q rejection, one draft row, where K1 / K3 read all k + 1
+// target rows.  Every value that decides a token comes from the same functions as in K1, K2
+// and K3, so the results are the same bit for bit.  Blocks never wait for one another.
+
+constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnitBytes;
+#ifndef SPEC_KL_WARPS
+#define SPEC_KL_WARPS 8       // warps per block, each with its own ring
+#endif
+#ifndef SPEC_KL_STAGES
+#define SPEC_KL_STAGES 1      // ring slots per warp (8 warps x 2 blocks: 16 units in flight per SM)
+#endif
+#ifndef SPEC_KL_MIN_REQUESTS
+#define SPEC_KL_MIN_REQUESTS 64  // smaller batches: each request's chain of rows would set the time
+#endif
+#ifndef SPEC_KL_RESIDUAL_UNROLL
+#define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass
+#endif
+#ifndef SPEC_KL_MIN_BLOCKS
+#define SPEC_KL_MIN_BLOCKS 2  // blocks per SM
+#endif
+constexpr int kLWarps = SPEC_KL_WARPS;
+constexpr int kLStages = SPEC_KL_STAGES;
+constexpr int kLThreads = kLWarps * 32;
+constexpr size_t kLSmem = (size_t)kLWarps * kLStages * kUnitBytes;
+
+// Layout check and request-queue reset before KL (one block).
+__global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
+{
+    validate_layout(P);
+    if (threadIdx.x == 0)
+        P.err[2] = 0;  // next request to hand out
+}
+
+struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
+    const float *z;
+    __device__ __forceinline__ float operator()(int c) const { return z[c]; }
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Params P)
+{
+    constexpr int ES = Elem<DT>::kSize;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kLWarps * kLStages];
+    __shared__ float2 spart[kLMaxChunks];  // chunk partials of the row just streamed
+    __shared__ float srm[kLMaxChunks];     // residual chunk masses (explicit q)
+    __shared__ int s_r, s_go, s_abort;
+    __shared__ float s_M, s_S;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (P.err[0] & SPEC_DEVERR_LAYOUT) {  // the whole batch is invalid (as K2 reports it)
+        for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < P.B; r += gridDim.x * blockDim.x)
+            P.out_acc[r] = -1;
+        return;
+    }
+    if (threadIdx.x < kLWarps * kLStages)
+        mbar_init(&full[threadIdx.x], 1);
+    mbar_fence_init();
+    if (threadIdx.x == 0)
+        s_abort = 0;
+    __syncthreads();
+    unsigned char *slots = ring + (size_t)warp * kLStages * kUnitBytes;
+    uint64_t *bars = full + warp * kLStages;
+    int64_t qi = 0, qc = 0;  // this warp's units issued (lane 0) and consumed; slot = count % stages
+
+    auto issue = [&](const char *row, int c) {
+        const int s = (int)(qi % kLStages);
+        const int64_t lo = (int64_t)c * P.chunk;
+        const int64_t hi = min((int64_t)P.V, lo + P.chunk);
+        const uint32_t bytes = (uint32_t)((hi - lo) * ES) & ~15u;
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        if (bytes)
+            bulk_g2s(slots + (size_t)s * kUnitBytes, row + lo * ES, bytes, &bars[s]);
+        ++qi;
+    };
+
+    for (;;) {
+        if (threadIdx.x == 0)
+            s_r = atomicAdd(P.err + 2, 1);
+        __syncthreads();
+        const int r = s_r;
+        if (r >= P.B || s_abort)
+            break;  // uniform
+        const int cu0 = P.cu[r];
+        const int k = P.cu[r + 1] - cu0;
+        const int64_t tb = (int64_t)cu0 + r;
+        const int64_t db = cu0;
+        // per-request checks, as K2 (every warp reads the same ids, so every warp agrees)
+        const bool too_long = k > SPEC_REJECT_MAX_SPEC_LEN;
+        int xs = -1;
+        if (!too_long && lane < k)
+            xs = P.ids[db + lane];
+        const unsigned badid = __ballot_sync(kFull, !too_long && lane < k && (xs < 0 || xs >= P.V));
+        if (too_long || badid) {
+            if (warp == 0) {
+                for (int64_t i = lane; i <= k; i += 32)
+                    P.out_tokens[tb + i] = -1;
+                if (lane == 0) {
+                    P.out_acc[r] = -1;
+                    atomicOr(P.err, too_long ? SPEC_DEVERR_SPEC_LEN : SPEC_DEVERR_DRAFT_ID);
+                    atomicMin(P.err + 1, r);
+                }
+            }
+            __syncthreads();  // s_r is rewritten for the next request
+            continue;
+        }
+        const float temp = P.temp[r];
+        const bool greedy = !(temp > 0.f);
+        const float cs = greedy ? 0.f : kLog2e / temp;
+        // inputs of the acceptance test of draft position `lane` (warp 0), issued first
+        float ls = 0.f, qs = 1.f, ua = 0.f, usl = 0.f;
+        if (warp == 0 && !greedy) {
+            if (lane < k) {
+                ls = load1<DT>(row_ptr<DT>(P, tb + lane), xs);
+                if (P.q)
+                    qs = __ldg(P.q + (db + lane) * P.qstride + xs);
+                ua = P.uni[2 * (tb + lane)];
+            }
+            if (lane <= k)
+                usl = P.uni[2 * (tb + lane) + 1];  // the sampling draw, wherever the output lands
+        }
+        const float us32 = (warp == 0 && !greedy && k == 32) ? P.uni[2 * (tb + 32) + 1] : 0.f;
+
+        int j = k;       // output position: the first rejection, else the bonus row
+        int am = 0;      // argmax of the latest row (greedy)
+        float Mi = 0.f, Si = 0.f;
+        for (int i = 0; i <= k; ++i) {
+            const char *row = row_ptr<DT>(P, tb + i);
+            // ---- stream row t_i: this warp's units c = warp, warp + kLWarps, ...
+            int ci = warp;
+            if (lane == 0)
+                for (int s = 0; s < kLStages && ci < P.nchunks; ++s, ci += kLWarps)
+                    issue(row, ci);
+            bool ok = true;
+            for (int c = warp; c < P.nchunks; c += kLWarps) {
+                const int s = (int)(qc % kLStages);
+                if (!__all_sync(kFull, mbar_wait(&bars[s], (uint32_t)(qc / kLStages) & 1, P.err))) {
+                    ok = false;
+                    break;
+                }
+                UnitRange R;
+                R.lo = (int64_t)c * P.chunk;
+                R.hi = min((int64_t)P.V, R.lo + P.chunk);
+                R.vlo = R.lo;
+                R.nvec = ((R.hi - R.lo) * ES) / 16;
+                R.vhi = R.vlo + R.nvec * Elem<DT>::kVec;
+                const uint4 *stage = reinterpret_cast<const uint4 *>(slots + (size_t)s * kUnitBytes);
+                uint4 v[kVecPerLane];
+#pragma unroll
+                for (int kk = 0; kk < kVecPerLane; ++kk) {
+                    const int vi = kk * 32 + lane;
+                    v[kk] = (vi < R.nvec) ? stage[vi] : neg_inf_vec<DT>();
+                }
+                __syncwarp();
+                ++qc;
+                if (lane == 0 && ci < P.nchunks) {  // the slot is in registers: refill it
+                    issue(row, ci);
+                    ci += kLWarps;
+                }
+                if (greedy)
+                    argmax_regs<DT>(&spart[c], lane, v, R, row);
+                else
+                    softmax_regs<DT>(&spart[c], cs, lane, v, R, row);
+            }
+            if (!ok && lane == 0)
+                s_abort = 1;
+            __syncthreads();  // the row's chunk partials are in spart
+            if (s_abort)
+                break;
+            // ---- the row's statistics (K2's per-row combine) and, on a draft row, the test
+            if (warp == 0) {
+                float m = -INFINITY, sv = 0.f, best = -INFINITY;
+                int idx = INT_MAX;
+                for (int c = lane; c < P.nchunks; c += 32) {
+                    const float2 pc = spart[c];
+                    if (greedy) {
+                        const int cix = __float_as_int(pc.y);
+                        if (pc.x > best || (pc.x == best && cix < idx)) {
+                            best = pc.x;
+                            idx = cix;
+                        }
+                    } else if (pc.x != -INFINITY) {
+                        const float Mc = pc.x * cs;
+                        if (Mc > m) {
+                            sv = (m == -INFINITY) ? pc.y : sv * ex2(m - Mc) + pc.y;
+                            m = Mc;
+                        } else {
+                            sv += pc.y * ex2(Mc - m);
+                        }
+                    }
+                }
+                bool go = false;
+                if (greedy) {
+                    warp_argmax(best, idx);
+                    am = idx == INT_MAX ? 0 : idx;
+                    go = i < k && __shfl_sync(kFull, xs, i) == am;
+                } else {
+                    const float mw = warp_max(m);
+                    const float sw = warp_sum(m == -INFINITY ? 0.f : sv * ex2(m - mw));
+                    Mi = mw;
+                    Si = sw;
+                    bool accept = true;
+                    if (lane == i && i < k) {
+                        const float e = fmaf(ls, cs, -Mi);
+                        const float wstar = ex2(e);
+                        const double lhs = (double)ua * (double)qs;  // exact
+                        const float ps = wstar / Si;
+                        if (ps > 1e-30f || wstar == 0.f)
+                            accept = lhs < (double)ps;
+                        else  // below fp32's normal range: form p(x*) in double
+                            accept = lhs < exp2((double)e) / (double)Si;
+                    }
+                    go = i < k && __shfl_sync(kFull, accept, i & 31);
+                }
+                if (lane == 0) {
+                    s_go = go;
+                    s_M = Mi;
+                    s_S = Si;
+                }
+            }
+            __syncthreads();
+            if (!s_go) {
+                j = i;
+                break;
+            }
+        }
+        if (s_abort)
+            break;
+
+        // ---- the output token at row t_j (K2 / K3 arithmetic)
+        const int64_t tj = tb + j;
+        const char *rowj = row_ptr<DT>(P, tj);
+        int token = -1;
+        const bool residual = !greedy && j < k && P.q;
+        if (residual) {  // explicit q: residual chunk masses of row t_j by every warp (K3)
+            const float Mj = s_M, Sj = s_S;
+            const ResidualMass<DT, false> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, 0u};
+            for (int c = warp; c < P.nchunks; c += kLWarps) {
+                const float z = warp_residual_chunk<DT, false, SPEC_KL_RESIDUAL_UNROLL>(
+                    f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), lane);
+                if (lane == 0)
+                    srm[c] = z;
+            }
+            __syncthreads();
+        }
+        if (warp == 0) {
+            const float us = greedy ? 0.f : (j < 32 ? __shfl_sync(kFull, usl, j & 31) : us32);
+            if (greedy) {
+                token = am;  // the argmax of row t_j: the first mismatch, or the bonus row
+            } else if (j == k) {  // bonus: draw from p
+                float M, S;
+                warp_combine_soft(spart, P.nchunks, cs, lane, M, S);
+                ChunkMassFromPartials cm{spart, cs, M, -1, 0.f};
+                const float Z = chunk_total(cm, P.nchunks, lane);
+                float th;
+                const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
+                TargetMass<DT, false> f{rowj, cs, M, -1, 0u};
+                token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
+                                       lane);
+            } else if (!residual) {  // one-hot draft: residual = p without x*
+                const float Mj = Mi;
+                const int xj = __shfl_sync(kFull, xs, j & 31);
+                const int cx = xj / P.chunk;
+                TargetMass<DT, false> fx{rowj, cs, Mj, xj, 0u};
+                const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
+                                                 min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
+                ChunkMassFromPartials cm{spart, cs, Mj, cx, mx};
+                float Z = chunk_total(cm, P.nchunks, lane);
+                int64_t excl = xj;
+                if (!(Z > 0.f)) {  // empty residual: draw from p itself
+                    cm.override_chunk = -1;
+                    Z = chunk_total(cm, P.nchunks, lane);
+                    excl = -1;
+                }
+                float th;
+                const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
+                TargetMass<DT, false> f{rowj, cs, Mj, excl, 0u};
+                token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
+                                       lane);
+            } else {  // explicit q: locate in the residual (K3)
+                const float Mj = s_M, Sj = s_S;
+                const ChunkMassFromShared cmz{srm};
+                const float Z = chunk_total(cmz, P.nchunks, lane);
+                if (Z > 0.f) {
+                    float th;
+                    const int cc = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
+                    const ResidualMass<DT, false> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, 0u};
+                    token = (int)warp_find(f, (int64_t)cc * P.chunk,
+                                           min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
+                } else {  // empty residual: draw from p itself
+                    const ChunkMassFromPartials cm{spart, cs, Mj, -1, 0.f};
+                    const float Zp = chunk_total(cm, P.nchunks, lane);
+                    float th;
+                    const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
+                    const TargetMass<DT, false> ft{rowj, cs, Mj, -1, 0u};
+                    token = (int)warp_find(ft, (int64_t)cc * P.chunk,
+                                           min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
+                }
+            }
+            // ---- outputs
+            if (lane == 0)
+                P.out_acc[r] = j;
+            for (int i = lane; i <= k; i += 32)
+                P.out_tokens[tb + i] = (i < j) ? xs : (i == j ? token : -1);
+            if (P.counters) {
+                unsigned long long *C = P.counters;
+                if (lane == 0) {
+                    if (k > 0)
+                        atomicAdd(C + SPEC_METRIC_NUM_DRAFTS, 1ull);
+                    atomicAdd(C + SPEC_METRIC_NUM_DRAFT_TOKENS, (unsigned long long)k);
+                    atomicAdd(C + SPEC_METRIC_NUM_ACCEPTED_TOKENS, (unsigned long long)j);
+                    atomicAdd(C + SPEC_METRIC_NUM_VERIFIES, 1ull);
+                }
+                if (lane < j)
+                    atomicAdd(C + SPEC_METRIC_ACCEPTED_PER_POS + lane, 1ull);
+            }
+        }
+        __syncthreads();  // spart, srm and the shared scalars are reused by the next request
+    }
+    // gave up on a wait: let this warp's copies still in flight land before exiting
+    if (lane == 0)
+        for (int64_t q2 = qc; q2 < qi; ++q2)
+            mbar_wait(&bars[q2 % kLStages], (uint32_t)(q2 / kLStages) & 1, P.err);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -2276,7 +2653,7 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(Params P, const int
     }
     int cur = 0, acc = 0;
     for (int step = 0; step < n; ++step) {
-        const int am = warp_combine_argmax(P, (int64_t)n0 + cur, lane);
+        const int am = warp_combine_argmax(P.part + ((int64_t)n0 + cur) * P.nchunks, P.nchunks, lane);
         int child = INT_MAX;
         for (int i = 1 + lane; i < n; i += 32)
             if (parent[n0 + i] == cur && tok[n0 + i] == am)
@@ -2375,7 +2752,7 @@ __global__ void __launch_bounds__(kThreads) debug_soft_kernel(Params P, float *r
         return;  // greedy rows: filled from the argmax pass
     const float cs = kLog2e / temp;
     float M, S;
-    warp_combine_soft(P, t, cs, lane, M, S);
+    warp_combine_soft(P.part + t * P.nchunks, P.nchunks, cs, lane, M, S);
     float m = -INFINITY;
     for (int c = lane; c < P.nchunks; c += 32)
         m = fmaxf(m, P.part[t * P.nchunks + c].x);
@@ -2396,7 +2773,7 @@ __global__ void __launch_bounds__(kThreads) debug_argmax_kernel(Params P, float 
     const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= P.T || P.B == 0 || (P.err[0] & SPEC_DEVERR_LAYOUT))
         return;
-    const int idx = warp_combine_argmax(P, t, lane);
+    const int idx = warp_combine_argmax(P.part + t * P.nchunks, P.nchunks, lane);
     if (lane == 0) {
         if (row_argmax)
             row_argmax[t] = idx;
@@ -2424,6 +2801,7 @@ struct DeviceInfo {
     int blocks_rowstats[2] = {0, 0};
     int blocks_residual[2] = {0, 0};
     int blocks_wr[2] = {0, 0};
+    int blocks_lazy[2] = {0, 0};
 };
 
 constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
@@ -2444,6 +2822,10 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
         return e;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
+        return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT>, kLThreads, kLSmem)))
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
@@ -2620,6 +3002,21 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             cudaEventRecord(ev[evi], stream);
         ++evi;
     };
+    // calls without cuts or diagnostics: KL reads rows only up to each request's first rejection
+    const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
+    if (!filtered && !debug && !q_stage && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
+        di->blocks_lazy[DT] > 0) {
+        mark();
+        lazy_init_kernel<<<1, 256, 0, stream>>>(P);
+        mark();
+        const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
+        if (DT)
+            lazy_kernel<1><<<gridL, kLThreads, kLSmem, stream>>>(P);
+        else
+            lazy_kernel<0><<<gridL, kLThreads, kLSmem, stream>>>(P);
+        mark();
+        return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    }
     mark();
     launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
     mark();
@@ -3043,9 +3440,11 @@ const char *spec_reject_status_string(spec_status status)
 
 int spec_reject_version(void) { return 100; }
 
-int spec_reject_num_kernels(int has_draft_probs, int has_filters)
+int spec_reject_num_kernels(int32_t B, int has_draft_probs, int has_filters)
 {
-    return 2 + (has_draft_probs ? 1 : 0) + (has_filters ? 1 : 0);
+    if (!has_filters && B >= SPEC_KL_MIN_REQUESTS)
+        return 2;  // layout check, then the pass up to each first rejection
+    return (has_filters ? 3 : 2) + (has_draft_probs ? 1 : 0);
 }
 
 }  // extern "C"

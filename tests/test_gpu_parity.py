@@ -312,3 +312,36 @@ def test_host_entry_reads_pinned_draft_probs_in_place(name):
     assert 0 < len(written) <= w["B"]
     qbytes = torch.from_numpy(w["draft_probs"].view(np.uint8).reshape(nd, 4 * V)[written]).cuda()
     assert torch.equal(qregion[torch.from_numpy(written).cuda()], qbytes)
+
+
+# ---------------------------------------------------------------------------- rows read up to the first rejection
+
+@pytest.mark.parametrize("name,over", [("tiny", dict(B=96)), ("greedy", {}), ("probabilistic", dict(B=80)),
+                                       ("deterministic", {}), ("large-128", {})])
+def test_first_rejection_pass_equals_full_pass(name, over):
+    """Calls without cuts or diagnostics on 64 or more requests read each request's rows only up
+    to its first rejection (KL); the diagnostic entry still runs the full pass over every row
+    (K1, K2, K3).  Both take every decision with the same arithmetic, so the outputs are the same
+    bit for bit (fp32 and bf16 rows, explicit and one-hot drafts, greedy requests)."""
+    w = W.generate(name, **over)
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+
+
+def test_first_rejection_pass_long_chains_and_counters():
+    """Requests that accept every draft walk all k + 1 rows (up to 32 drafts), and the counters
+    added inside the pass match the standalone update."""
+    import torch
+    B, K = 72, 32
+    w = W.generate(dict(B=B, K=K, V=5003, dtype="bf16", sigma=2.0, temperature=0.9, draft="target_q", seed=44),
+                   name="long-chains")
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    assert (lazy["acc"] == K).any()  # q = p accepts every draft
+    d = binding.to_device(w, "cuda")
+    ctr = torch.zeros(binding.METRIC_COUNT, dtype=torch.int64, device="cuda")
+    tok, acc = binding.sample_ex(**d, counters=ctr)
+    from oracle import closed_forms as cf
+    assert ctr.cpu().tolist() == cf.acceptance_counters(w["cu_num_draft"], acc.cpu().numpy())

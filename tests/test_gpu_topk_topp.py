@@ -86,7 +86,7 @@ def test_profiled_entry_with_filters_matches_filtered_entry():
     d = binding.to_device(w, dev)
     dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, d["draft_probs"] is not None, dev)
-    nk = binding.num_kernels(d["draft_probs"] is not None, True)
+    nk = binding.num_kernels(w["B"], d["draft_probs"] is not None, True)
     assert nk == 3 + (d["draft_probs"] is not None)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
     stream = torch.cuda.current_stream()
