@@ -526,18 +526,27 @@ def e2e(w, dev, args):
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / steps
-    # bytes that cross the host link per step: every input copied, except pinned draft
-    # probabilities, which the kernels read in place (one 32-byte sector per q(x*) gather and
-    # the whole row at each rejecting request's first rejection)
+    # bytes that cross the host link per step (the algorithmic ones): the small inputs are copied;
+    # pinned draft probabilities are read in place (one 32-byte sector per q(x*) gather and the
+    # row at each rejecting request's first rejection); pinned target logits of a batch that
+    # takes the first-rejection pass are read in place too, only the rows up to each output row
+    from speculative_decoding_rejection_spec_gb300 import binding as _b
+    acc = host["out_num_accepted"].numpy()
+    ks = np.diff(w["cu_num_draft"])
+    logits_in_place = _b.reads_to_first_rejection(w["B"])
     h2d = sum(v.numel() * v.element_size() for k, v in host.items()
-              if not k.startswith("out_") and k != "draft_probs")
-    q_note = None
+              if not k.startswith("out_") and k != "draft_probs" and not (k == "logits" and logits_in_place))
+    es = 2 if w["dtype"] == "bf16" else 4
+    notes = []
+    if logits_in_place:
+        rows = int((acc[acc >= 0] + 1).sum())
+        h2d += rows * w["V"] * es
+        notes.append(f"target logits read in place from pinned memory: {rows} of {w['T']} rows")
     if has_q:
-        acc = host["out_num_accepted"].numpy()
-        ks = np.diff(w["cu_num_draft"])
         rejecting = int(((acc >= 0) & (acc < ks)).sum())
         h2d += rejecting * w["V"] * 4 + 32 * (w["T"] - w["B"])
-        q_note = f"draft probabilities read in place from pinned memory: {rejecting} rows + {w['T'] - w['B']} gathers"
+        notes.append(f"draft probabilities read in place: {rejecting} rows + {w['T'] - w['B']} gathers")
+    q_note = "; ".join(notes) if notes else None
     d2h = 4 * (w["T"] + w["B"])
     from speculative_decoding_rejection_spec_gb300 import workloads as W
     out = {"value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),

@@ -156,7 +156,10 @@ spec_status spec_reject_last_device_error(const void *workspace, void *stream, i
  * pinned memory copies fastest.  draft_probs in pinned (page-locked, device-mapped)
  * memory is not copied: the kernels read in place, over the host link, only what the
  * method needs (q(x*) of each verify row and the row at each request's first
- * rejection); pageable draft_probs is copied whole.  Rows are passed with the same strides as the
+ * rejection); pageable draft_probs is copied whole.  When the target logits are pinned
+ * too (and draft_probs, if given), the batch has at least 64 requests and rows are
+ * 16-byte aligned, nothing large is copied: the target rows are read in place as well,
+ * only those up to each request's output row.  Rows are passed with the same strides as the
  * device form (0 = aliasing is not allowed here: strides must be >= V).
  * `device_arena` must hold spec_reject_host_arena_size() bytes.
  */

@@ -2245,7 +2245,9 @@ struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
     __device__ __forceinline__ float operator()(int c) const { return z[c]; }
 };
 
-template <int DT>
+// HOST: the target rows live in pinned host memory (read over the host link with 16-byte loads,
+// sixteen in flight per lane) instead of device memory (TMA bulk copies).
+template <int DT, bool HOST>
 __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Params P)
 {
     constexpr int ES = Elem<DT>::kSize;
@@ -2337,10 +2339,31 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             const char *row = row_ptr<DT>(P, tb + i);
             // ---- stream row t_i: this warp's units c = warp, warp + kLWarps, ...
             int ci = warp;
-            if (lane == 0)
+            if (!HOST && lane == 0)
                 for (int s = 0; s < kLStages && ci < P.nchunks; ++s, ci += kLWarps)
                     issue(row, ci);
             bool ok = true;
+            if constexpr (HOST) {
+                for (int c = warp; c < P.nchunks; c += kLWarps) {
+                    UnitRange R;
+                    R.lo = (int64_t)c * P.chunk;
+                    R.hi = min((int64_t)P.V, R.lo + P.chunk);
+                    R.vlo = R.lo;
+                    R.nvec = ((R.hi - R.lo) * ES) / 16;
+                    R.vhi = R.vlo + R.nvec * Elem<DT>::kVec;
+                    const char *u0 = row + R.lo * ES;
+                    uint4 v[kVecPerLane];
+#pragma unroll
+                    for (int kk = 0; kk < kVecPerLane; ++kk) {
+                        const int vi = kk * 32 + lane;
+                        v[kk] = (vi < R.nvec) ? ld_stream(u0 + (size_t)vi * 16) : neg_inf_vec<DT>();
+                    }
+                    if (greedy)
+                        argmax_regs<DT>(&spart[c], lane, v, R, row);
+                    else
+                        softmax_regs<DT>(&spart[c], cs, lane, v, R, row);
+                }
+            } else
             for (int c = warp; c < P.nchunks; c += kLWarps) {
                 const int s = (int)(qc % kLStages);
                 if (!__all_sync(kFull, mbar_wait(&bars[s], (uint32_t)(qc / kLStages) & 1, P.err))) {
@@ -2823,9 +2846,12 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
         return e;
-    if ((e = cudaFuncSetAttribute(lazy_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
         return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT>, kLThreads, kLSmem)))
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
+        return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT, false>, kLThreads,
+                                                           kLSmem)))
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
@@ -2934,7 +2960,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
                 cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
                 cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr,
-                int64_t *counters = nullptr, float *q_stage = nullptr)
+                int64_t *counters = nullptr, float *q_stage = nullptr, bool rows_in_host = false)
 {
     spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
     if (st != SPEC_OK)
@@ -3010,13 +3036,22 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
         mark();
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
-        if (DT)
-            lazy_kernel<1><<<gridL, kLThreads, kLSmem, stream>>>(P);
-        else
-            lazy_kernel<0><<<gridL, kLThreads, kLSmem, stream>>>(P);
+        if (rows_in_host) {
+            if (DT)
+                lazy_kernel<1, true><<<gridL, kLThreads, kLSmem, stream>>>(P);
+            else
+                lazy_kernel<0, true><<<gridL, kLThreads, kLSmem, stream>>>(P);
+        } else {
+            if (DT)
+                lazy_kernel<1, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
+            else
+                lazy_kernel<0, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
+        }
         mark();
         return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
     }
+    if (rows_in_host)
+        return SPEC_ERR_INVALID_ARG;  // only the first-rejection pass reads rows in host memory
     mark();
     launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
     mark();
@@ -3229,22 +3264,26 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     // Draft probabilities in pinned, mapped host memory are read in place over the host link:
     // the kernels touch only q(x*) of each verify row and the row at each request's first
     // rejection, a small part of the [T - B, V] array.  Pageable memory is copied whole.
-    const float *q_in_place = nullptr;
-    if (has_q) {
+    auto mapped = [](const void *p) -> const void * {  // device address of pinned, mapped host memory
         cudaPointerAttributes pa{};
-        if (cudaPointerGetAttributes(&pa, draft_probs) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
-            pa.devicePointer)
-            q_in_place = static_cast<const float *>(pa.devicePointer);
-        else
-            (void)cudaGetLastError();
-    }
+        if (cudaPointerGetAttributes(&pa, p) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer)
+            return pa.devicePointer;
+        (void)cudaGetLastError();
+        return nullptr;
+    };
+    const float *q_in_place = has_q ? static_cast<const float *>(mapped(draft_probs)) : nullptr;
+    // Pinned logits too, and a batch that takes the first-rejection pass: that pass reads the
+    // target rows in place as well, only the rows up to each request's output row.
+    const void *logits_in_place = (T > 0) ? mapped(target_logits) : nullptr;
+    const bool all_in_place = logits_in_place && (!has_q || q_in_place) && B >= SPEC_KL_MIN_REQUESTS &&
+                              aligned(logits_in_place, 16) && ((size_t)V * es) % 16 == 0;
     // one cudaMemcpyAsync per buffer
     const struct {
         void *dst;
         const void *src;
         size_t bytes;
     } in[] = {
-        {d_logits, target_logits, es * (size_t)T * (size_t)V},
+        {d_logits, target_logits, all_in_place ? 0 : es * (size_t)T * (size_t)V},
         {d_q, draft_probs, has_q && !q_in_place ? 4 * (size_t)(T - B) * (size_t)V : 0},
         {d_ids, draft_ids, 4 * (size_t)(T - B)},
         {d_cu, cu_num_draft, 4 * (size_t)(B + 1)},
@@ -3256,9 +3295,14 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
             return SPEC_ERR_CUDA;
     // q in place: K2 reads q(x*) over the link, then the rows K3 needs are staged into the
     // arena's q region (the rest of it stays unwritten)
-    spec_status st = run(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr, V, d_ids,
-                         d_cu, B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr,
-                         nullptr, nullptr, 0, nullptr, nullptr, nullptr, q_in_place ? d_q : nullptr);
+    spec_status st =
+        all_in_place
+            ? run(logits_in_place, logits_dtype, T, V, V, q_in_place, V, d_ids, d_cu, B, d_uni, d_temp, d_tok, d_acc,
+                  d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr,
+                  nullptr, nullptr, true)
+            : run(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr, V, d_ids, d_cu,
+                  B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr,
+                  nullptr, 0, nullptr, nullptr, nullptr, q_in_place ? d_q : nullptr);
     if (st != SPEC_OK)
         return st;
     if ((T && cudaMemcpyAsync(out_tokens, d_tok, 4 * (size_t)T, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||

@@ -278,40 +278,47 @@ def test_host_entry_matches_device_entry():
         assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
 
 
-@pytest.mark.parametrize("name", ["tiny", "large-128"])
-def test_host_entry_reads_pinned_draft_probs_in_place(name):
-    """Pinned draft probabilities are read in place by the kernels (no copy): the result is
-    the device entry's, bit for bit, and the oracle's on unflagged requests."""
+@pytest.mark.parametrize("name", ["tiny", "large-128", "deterministic"])
+def test_host_entry_reads_pinned_inputs_in_place(name):
+    """Pinned inputs are read in place by the kernels: below 64 requests the draft probabilities
+    (the rows the residual pass needs are staged into the arena), from 64 requests the target
+    logits too (the first-rejection pass reads rows over the host link; nothing large is
+    copied).  The result is the device entry's, bit for bit."""
     import torch
     w = W.generate(name)
     dev = PT.run_gpu(w)
+    has_q = w["draft_probs"] is not None
 
     def pinned(a):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
 
-    host = {k: pinned(w[k]) for k in ("logits", "draft_probs", "draft_ids", "cu_num_draft", "uniforms",
-                                      "temperature")}
+    keys = ["logits", "draft_ids", "cu_num_draft", "uniforms", "temperature"] + (["draft_probs"] if has_q else [])
+    host = {k: pinned(w[k]) for k in keys}
     host["out_tokens"] = torch.full((w["T"],), -7, dtype=torch.int32).pin_memory()
     host["out_num_accepted"] = torch.full((w["B"],), -7, dtype=torch.int32).pin_memory()
     ptrs = {k: v.data_ptr() for k, v in host.items()}
     dt = PT.dtype_code(w)
-    arena = torch.full((binding.host_arena_size(w["B"], w["T"], w["V"], dt, True),), 0xA5, dtype=torch.uint8,
+    arena = torch.full((binding.host_arena_size(w["B"], w["T"], w["V"], dt, has_q),), 0xA5, dtype=torch.uint8,
                        device="cuda")
     binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena)
     tok, acc = host["out_tokens"].numpy(), host["out_num_accepted"].numpy()
     assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
-    # q was not copied: the arena's region for a copy of q (right after the logits, 256-byte
-    # aligned) holds only the rows staged for the residual pass, at most one per request, each
-    # equal to its row of q
+    # the arena holds the logits copy first, then the q copy (256-byte aligned regions)
     es = 2 if w["dtype"] == "bf16" else 4
     base = (-arena.data_ptr()) % 256
-    q0 = base + ((es * w["T"] * w["V"] + 255) // 256) * 256
-    nd, V = w["T"] - w["B"], w["V"]
-    qregion = arena[q0:q0 + 4 * nd * V].view(nd, 4 * V)
-    written = torch.nonzero((qregion != 0xA5).any(dim=1)).flatten().cpu().numpy()
-    assert 0 < len(written) <= w["B"]
-    qbytes = torch.from_numpy(w["draft_probs"].view(np.uint8).reshape(nd, 4 * V)[written]).cuda()
-    assert torch.equal(qregion[torch.from_numpy(written).cuda()], qbytes)
+    lbytes = es * w["T"] * w["V"]
+    q0 = base + ((lbytes + 255) // 256) * 256
+    if w["B"] >= 64:  # nothing large was copied
+        assert bool((arena[base:base + lbytes] == 0xA5).all())
+        if has_q:
+            assert bool((arena[q0:q0 + 4 * (w["T"] - w["B"]) * w["V"]] == 0xA5).all())
+    elif has_q:  # only the rows for the residual pass were staged, each equal to its row of q
+        nd, V = w["T"] - w["B"], w["V"]
+        qregion = arena[q0:q0 + 4 * nd * V].view(nd, 4 * V)
+        written = torch.nonzero((qregion != 0xA5).any(dim=1)).flatten().cpu().numpy()
+        assert 0 < len(written) <= w["B"]
+        qbytes = torch.from_numpy(w["draft_probs"].view(np.uint8).reshape(nd, 4 * V)[written]).cuda()
+        assert torch.equal(qregion[torch.from_numpy(written).cuda()], qbytes)
 
 
 # ---------------------------------------------------------------------------- rows read up to the first rejection
