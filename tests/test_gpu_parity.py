@@ -264,6 +264,44 @@ def test_device_errors_layout(which):
     assert ref.status == 1 and (ref.num_accepted == -1).all()
 
 
+@pytest.mark.parametrize("draft", ["noisy_q", "uniform"])
+def test_first_rejection_pass_device_errors_per_request(draft):
+    """The same per-request errors on a batch that takes the first-rejection pass (B >= 64):
+    k > 32 and an out-of-range draft id invalidate only their request; the rest match the full
+    pass bit for bit."""
+    B = 70
+    ks = [3] * B
+    ks[5] = 33
+    w = W.generate(dict(B=B, K=ks, V=500, dtype="f32", sigma=1.0, temperature=1.0, draft=draft, seed=112),
+                   name="bad-many")
+    w["draft_ids"][w["cu_num_draft"][40] + 1] = -3  # request 40: id out of range
+    tok, acc, st, bits, first = _run_raw(w)
+    assert st == 5 and bits == (binding.DEVERR_SPEC_LEN | binding.DEVERR_DRAFT_ID) and first == 5
+    assert acc[5] == -1 and acc[40] == -1
+    cu = w["cu_num_draft"]
+    for r in (5, 40):
+        assert (tok[cu[r] + r:cu[r + 1] + r + 1] == -1).all()
+    full = PT.run_gpu(w, debug=True)
+    assert np.array_equal(tok, full["tokens"]) and np.array_equal(acc, full["acc"])
+    ref = oracle.reject_sample_workload(w)
+    assert (ref.num_accepted[[5, 40]] == -1).all()
+
+
+@pytest.mark.parametrize("which", ["cu0", "decreasing", "total"])
+def test_first_rejection_pass_device_errors_layout(which):
+    w = W.generate(dict(B=80, K=3, V=300, dtype="f32", sigma=1.0, temperature=1.0, draft="uniform", seed=122),
+                   name="layout-many")
+    if which == "cu0":
+        w["cu_num_draft"][0] = 1
+    elif which == "decreasing":
+        w["cu_num_draft"][20] = w["cu_num_draft"][19] - 1
+    else:
+        w["cu_num_draft"][-1] -= 1
+    tok, acc, st, bits, first = _run_raw(w)
+    assert st == 5 and bits & binding.DEVERR_LAYOUT and first == -1
+    assert (acc == -1).all()
+
+
 # ---------------------------------------------------------------------------- host-buffer entry point
 
 def test_host_entry_matches_device_entry():
