@@ -395,8 +395,8 @@ def main():
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, has_q, dev)
     tk = None if w.get("top_k") is None else torch.from_numpy(w["top_k"]).to(dev)
     tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).to(dev)
-    nk = binding.num_kernels(w["B"], has_q, filtered)
-    lazy = binding.reads_to_first_rejection(w["B"], filtered)
+    nk = binding.num_kernels(w["B"], has_q, filtered, dt)
+    lazy = binding.reads_to_first_rejection(w["B"], filtered, dt)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in ev:

@@ -344,11 +344,12 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
                                int32_t max_n, int32_t k, int64_t max_model_len, int32_t *out_drafts,
                                int32_t *out_num_drafts, void *stream);
 
-/* Kernels one call of B requests on 16-byte-aligned rows launches: 2 without top-k / top-p
- * when B >= 64 (the layout check, then the pass that reads rows up to each first rejection);
- * otherwise row statistics and the finalize (2), plus the top-k / top-p cut with filters, plus
- * the residual pass with draft probabilities. */
-int spec_reject_num_kernels(int32_t B, int has_draft_probs, int has_filters);
+/* Kernels one call of B requests on 16-byte-aligned rows in device memory launches: 2 when
+ * B >= 64 and the call has no top-k / top-p or its rows are bf16 (the layout check, then the
+ * pass that reads rows up to each first rejection); otherwise row statistics and the finalize
+ * (2), plus the top-k / top-p cut with filters, plus the residual pass with draft
+ * probabilities. */
+int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters);
 
 /* Static description of a status code. */
 const char *spec_reject_status_string(spec_status status);

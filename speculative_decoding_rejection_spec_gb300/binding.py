@@ -90,7 +90,7 @@ def load():
     lib.spec_reject_sample_ex.restype = ctypes.c_int
     lib.spec_reject_sample_ex.argtypes = sample_args + [P]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
-    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int32, ctypes.c_int, ctypes.c_int]
+    lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int, ctypes.c_int]
     _lib = lib
     return lib
 
@@ -310,15 +310,16 @@ def tree_verify_greedy(target_logits, parent, node_tokens, cu_nodes, stream=None
     return out, acc, last, ws
 
 
-def num_kernels(B: int, has_draft_probs: bool, has_filters: bool = False) -> int:
-    """Kernels one call of B requests launches (16-byte-aligned rows)."""
-    return int(load().spec_reject_num_kernels(int(B), int(bool(has_draft_probs)), int(bool(has_filters))))
+def num_kernels(B: int, has_draft_probs: bool, has_filters: bool = False, dtype: int = BF16) -> int:
+    """Kernels one call of B requests launches (16-byte-aligned rows in device memory)."""
+    return int(load().spec_reject_num_kernels(int(dtype), int(B), int(bool(has_draft_probs)),
+                                              int(bool(has_filters))))
 
 
-def reads_to_first_rejection(B: int, has_filters: bool = False) -> bool:
+def reads_to_first_rejection(B: int, has_filters: bool = False, dtype: int = BF16) -> bool:
     """Whether a call of B requests takes the pass that reads rows up to each first rejection."""
-    return not has_filters and int(load().spec_reject_num_kernels(int(B), 0, 0)) == 2 and \
-        int(load().spec_reject_num_kernels(int(B), 1, 0)) == 2
+    return all(int(load().spec_reject_num_kernels(int(dtype), int(B), q, int(bool(has_filters)))) == 2
+               for q in (0, 1))
 
 
 def sample_filtered(target_logits, draft_ids, cu_num_draft, uniforms, temperature, draft_probs=None, *,

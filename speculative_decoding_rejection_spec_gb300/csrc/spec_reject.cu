@@ -2232,6 +2232,344 @@ constexpr int kLStages = SPEC_KL_STAGES;
 constexpr int kLThreads = kLWarps * 32;
 constexpr size_t kLSmem = (size_t)kLWarps * kLStages * kUnitBytes;
 
+// ---- KL with top-k / top-p (bf16 rows): the cut of one row, by the whole block
+//
+// The same cut as K1F, from the row KL has just streamed (its unfiltered chunk partials are in
+// shared memory; the row is read again, mostly from L2):
+//   1. counts by order-key offset below the maximum's key, over the kFKeys largest keys (one
+//      histogram per warp, a sink per lane for the rest), and one token's fixed-point mass per
+//      offset;
+//   2. warp 0 finds the k-th largest key, S_k and the top-p key from the totals (integer
+//      sums), as K1F's one-pass path;
+//   3. one more pass gives each chunk's partial over the survivors: per element the mass of its
+//      key offset, summed as integers, which is K1F's count x mass sum.
+// A cut outside the window is found by a radix select on the 16-bit order key (two passes of
+// digit histograms per selection) with the partials of K1F's general path.  Either way the cut
+// key and the partials are K1F's, bit for bit.
+
+struct CutSmem {
+    unsigned hw[kLWarps][kFKeys + 32];  // per warp: tokens per key offset, then a sink per lane
+    unsigned bh[kFKeys];                // block totals per key offset
+    unsigned long long km[kFKeys];      // fixed-point mass of one token per key offset
+    float cmx[kLMaxChunks];             // unfiltered chunk maxima
+    unsigned rc[256];                   // radix: tokens per digit
+    unsigned long long rm[256];         // radix: masses per digit
+    unsigned long long red[kLWarps];
+    double z;                           // normaliser (top-p alone), 2^-32 units
+    float m;                            // row maximum
+    int pos;                            // exact path: crossing offset (-1: fall back)
+    int dsel;                           // radix: crossing digit (-1: none)
+    unsigned long long dabove;
+};
+constexpr size_t kLCutSmem = kLSmem + sizeof(CutSmem);
+
+// First position (in order 0, 1, ...) of 256 digit weights w at which above0 + cum >= target,
+// by warp 0 (8 per lane); -1 if the total falls short.  Returns the position and the weight
+// before it through C.dsel / C.dabove.
+template <class WF>
+__device__ __forceinline__ void warp_digit_crossing(CutSmem &C, unsigned long long above0, unsigned long long target,
+                                                    WF w)
+{
+    const int lane = threadIdx.x & 31;
+    const int b0 = lane * 8;
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        mine += w(b0 + k);
+    unsigned long long inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o)
+            inc += y;
+    }
+    unsigned long long c = above0 + inc - mine;
+    int pos = -1;
+    unsigned long long ab = 0;
+    if (c < target && c + mine >= target)
+        for (int k = 0; k < 8; ++k) {
+            const unsigned long long wk = w(b0 + k);
+            if (c + wk >= target) {
+                pos = b0 + k;
+                ab = c;
+                break;
+            }
+            c += wk;
+        }
+    const unsigned found = __ballot_sync(kFull, pos >= 0);
+    if (lane == 0)
+        C.dsel = -1;
+    __syncwarp();
+    if (found && lane == __ffs(found) - 1) {
+        C.dsel = pos;
+        C.dabove = ab;
+    }
+}
+
+// Cut of row `row` (all threads of the block; spart holds the row's unfiltered partials on
+// entry and the partials over the survivors on return).  Returns the cut key (0: no cut).
+template <int DT>
+__device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 *spart, const char *row, float cs,
+                                            int32_t tk, float tp, bool use_k, bool use_p)
+{
+    constexpr int kB = kFKeys;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = (int)(blockDim.x >> 5);
+    constexpr float kTwo32 = 4294967296.0f, kTwoM32f = 2.3283064365386963e-10f;
+
+    // ---- row maximum and (top-p alone) the normaliser from the unfiltered partials (K1F)
+    if (warp == 0) {
+        float mm = -INFINITY;
+        for (int c = lane; c < P.nchunks; c += 32)
+            mm = fmaxf(mm, spart[c].x);
+        mm = warp_max(mm);
+        double z = 0.0;
+        if (!use_k && mm > -INFINITY) {
+            const float Mm = mm * cs;
+            for (int c = lane; c < P.nchunks; c += 32) {
+                const float2 pc = spart[c];
+                if (pc.x != -INFINITY)
+                    z += (double)pc.y * (double)ex2(pc.x * cs - Mm);
+            }
+            z = warp_sum_f64(z);
+        }
+        if (lane == 0) {
+            C.m = mm;
+            C.z = z * 4294967296.0;
+        }
+    }
+    for (int c = threadIdx.x; c < P.nchunks; c += blockDim.x)
+        C.cmx[c] = spart[c].x;
+    for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
+        (&C.hw[0][0])[i] = 0u;
+    __syncthreads();
+    const float m = C.m;
+    if (!(m > -INFINITY))
+        return 0u;  // no finite logit (the same for every thread): no cut
+    const float M = m * cs;
+    auto fx = [&](float x) -> unsigned long long { return __float2ull_rn(ex2(fmaf(x, cs, -M)) * kTwo32); };
+    const uint32_t kmax = key_of<1>(m);
+    const bool plain = kmax >= 0x8000u + (uint32_t)kB;
+    auto offset = [&](uint32_t b16) -> uint32_t {  // key offset below kmax of the bf16 bits b16
+        if (plain)
+            return kmax - 0x8000u - b16;
+        const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
+        return kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
+    };
+    // fn(bits) for every element of chunk c, 16-byte loads (the row is 16-byte aligned here)
+    auto chunk_for_each = [&](int c, auto fn) {
+        const int e0 = c * P.chunk, e1 = min(P.V, e0 + P.chunk);
+        const int v1 = e1 / 8;
+        for (int v = e0 / 8 + lane; v < v1; v += 4 * 32) {
+            uint4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + 32 * u < v1)
+                    w[u] = ld_stream(row + (size_t)(v + 32 * u) * 16);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + 32 * u < v1) {
+                    fn(w[u].x & 0xffffu);
+                    fn(w[u].x >> 16);
+                    fn(w[u].y & 0xffffu);
+                    fn(w[u].y >> 16);
+                    fn(w[u].z & 0xffffu);
+                    fn(w[u].z >> 16);
+                    fn(w[u].w & 0xffffu);
+                    fn(w[u].w >> 16);
+                }
+        }
+        for (int i = v1 * 8 + lane; i < e1; i += 32)
+            fn((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i));
+    };
+
+    // ---- 1. counts by key offset
+    {
+        unsigned *h = C.hw[warp];
+        const uint32_t sink = (uint32_t)kB + (uint32_t)lane;
+        for (int c = warp; c < P.nchunks; c += nw)
+            chunk_for_each(c, [&](uint32_t b16) { atomicAdd(&h[min(offset(b16), sink)], 1u); });
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < kB; o += blockDim.x) {
+        unsigned tot = 0;
+        for (int w = 0; w < nw; ++w)
+            tot += C.hw[w][o];
+        C.bh[o] = tot;
+        C.km[o] = (uint32_t)o < kmax ? fx(x_of<1>(kmax - (uint32_t)o)) : 0ull;
+    }
+    __syncthreads();
+
+    // ---- 2. selection by warp 0 (lanes own 16 consecutive offsets), K1F's one-pass rules
+    if (warp == 0) {
+        constexpr int PER = kB / 32;
+        // first offset o <= olim at which w(0) + ... + w(o) >= target (-1 if never)
+        auto crossing = [&](unsigned long long target, int olim, bool by_mass) -> int {
+            const int b0 = lane * PER;
+            unsigned long long mine = 0;
+#pragma unroll 4
+            for (int k = 0; k < PER; ++k)
+                if (b0 + k <= olim)
+                    mine += by_mass ? (unsigned long long)C.bh[b0 + k] * C.km[b0 + k] : (unsigned long long)C.bh[b0 + k];
+            unsigned long long inc = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o)
+                    inc += y;
+            }
+            unsigned long long c = inc - mine;
+            int pos = -1;
+            if (c < target && inc >= target)
+                for (int k = 0; k < PER; ++k) {
+                    c += by_mass ? (unsigned long long)C.bh[b0 + k] * C.km[b0 + k] : (unsigned long long)C.bh[b0 + k];
+                    if (c >= target) {
+                        pos = b0 + k;
+                        break;
+                    }
+                }
+            const unsigned found = __ballot_sync(kFull, pos >= 0);
+            return found ? __shfl_sync(kFull, pos, __ffs(found) - 1) : -1;
+        };
+        bool ok = true;
+        int pcut = kB - 1;
+        if (use_k) {
+            pcut = crossing((unsigned long long)tk, kB - 1, false);
+            ok = pcut >= 0;  // fewer than k tokens in the window
+        }
+        if (ok && use_p) {
+            unsigned long long target;
+            if (use_k) {
+                unsigned long long sk = 0;
+                for (int o = lane; o <= pcut; o += 32)
+                    sk += (unsigned long long)C.bh[o] * C.km[o];
+                target = (unsigned long long)ceil((double)tp * (double)warp_sum_u64(sk));
+            } else {
+                target = (unsigned long long)ceil((double)tp * C.z);
+            }
+            const int p2 = crossing(target, pcut, true);
+            if (p2 >= 0)
+                pcut = p2;
+            else
+                ok = use_k;  // top-p alone: the cut lies below the window
+        }
+        if (lane == 0)
+            C.pos = ok ? pcut : -1;
+    }
+    __syncthreads();
+    const int pcut = C.pos;
+    if (pcut >= 0) {
+        // ---- 3. chunk partials over the survivors: masses relative to the row maximum, rescaled
+        const uint32_t thr = kmax - (uint32_t)pcut;
+        for (int c = warp; c < P.nchunks; c += nw) {
+            const float mk = C.cmx[c];
+            float mc = -INFINITY, sc = 0.f;
+            if (mk > -INFINITY && key_of<1>(mk) >= thr) {
+                mc = mk;
+                unsigned long long sum = 0;
+                chunk_for_each(c, [&](uint32_t b16) {
+                    const uint32_t o = offset(b16);
+                    if (o <= (uint32_t)pcut)
+                        sum += C.km[o];
+                });
+                sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
+            }
+            if (lane == 0)
+                spart[c] = make_float2(mc, sc);
+        }
+        __syncthreads();
+        return thr;
+    }
+
+    // ---- cut below the window: radix selects on the order key (high byte, then low byte)
+    auto key16 = [](uint32_t b16) -> uint32_t {
+        const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
+        return 0x8000u + (((b16 & 0x7fffu) ^ sg) - sg);
+    };
+    // The largest key K >= lo with (weights of the keys in [K, ...) that are >= lo) >= target,
+    // 0 when the total falls short.  Weights: 1 per token, or its fixed-point mass.  With
+    // p_of_total the target is ceil(tp * total weight), the total taken from the first level.
+    auto select = [&](uint32_t lo, unsigned long long target, bool by_mass, bool p_of_total) -> uint32_t {
+        uint32_t prefix = 0;
+        unsigned long long above = 0;
+        for (int level = 0; level < 2; ++level) {
+            const int shift = level ? 0 : 8;
+            for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
+                (&C.hw[0][0])[i] = 0u;
+            __syncthreads();
+            unsigned *hc = C.hw[warp];
+            unsigned long long *hm = reinterpret_cast<unsigned long long *>(C.hw[warp]);
+            for (int c = warp; c < P.nchunks; c += nw)
+                chunk_for_each(c, [&](uint32_t b16) {
+                    const uint32_t key = key16(b16);
+                    if (key >= lo && (level == 0 || (key >> 8) == (prefix >> 8))) {
+                        const uint32_t d = (key >> shift) & 255u;
+                        if (by_mass) {
+                            const unsigned long long w = fx(__uint_as_float(b16 << 16));
+                            if (w)
+                                atomicAdd(&hm[d], w);
+                        } else {
+                            atomicAdd(&hc[d], 1u);
+                        }
+                    }
+                });
+            __syncthreads();
+            for (int d = threadIdx.x; d < 256; d += blockDim.x) {
+                unsigned long long t = 0;
+                for (int w = 0; w < nw; ++w)
+                    t += by_mass ? reinterpret_cast<const unsigned long long *>(C.hw[w])[d]
+                                 : (unsigned long long)C.hw[w][d];
+                C.rm[d] = t;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                if (level == 0 && p_of_total) {
+                    unsigned long long t = 0;
+                    for (int d = lane; d < 256; d += 32)
+                        t += C.rm[d];
+                    target = (unsigned long long)ceil((double)tp * (double)warp_sum_u64(t));
+                }
+                warp_digit_crossing(C, above, target, [&](int i) { return C.rm[255 - i]; });
+            }
+            __syncthreads();
+            if (C.dsel < 0)
+                return 0u;  // uniform over the block
+            above = C.dabove;
+            prefix |= (255u - (uint32_t)C.dsel) << shift;
+            __syncthreads();  // C.dsel is rewritten by the next level
+        }
+        return prefix;
+    };
+    uint32_t tau = 0, lam = 0;
+    if (use_k)
+        tau = select(0u, (unsigned long long)tk, false, false);
+    if (use_p) {
+        const unsigned long long target = use_k ? 0ull : (unsigned long long)ceil((double)tp * C.z);
+        lam = select(tau, target, true, use_k);
+    }
+    const uint32_t thr = max(max(tau, lam), 1u);
+
+    // ---- chunk partials over the survivors, relative to each chunk's maximum (K1F's general path)
+    for (int c = warp; c < P.nchunks; c += nw) {
+        const float mk = C.cmx[c];
+        float mc = -INFINITY, sc = 0.f;
+        if (mk > -INFINITY && key_of<1>(mk) >= thr) {
+            mc = mk;
+            const float Mc = mc * cs;
+            unsigned long long sum = 0;
+            chunk_for_each(c, [&](uint32_t b16) {
+                if (key16(b16) >= thr)
+                    sum += __float2ull_rn(ex2(fmaf(__uint_as_float(b16 << 16), cs, -Mc)) * kTwo32);
+            });
+            sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f;
+        }
+        if (lane == 0)
+            spart[c] = make_float2(mc, sc);
+    }
+    __syncthreads();
+    return thr;
+}
+
 // Layout check and request-queue reset before KL (one block).
 __global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
 {
@@ -2246,12 +2584,15 @@ struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
 };
 
 // HOST: the target rows live in pinned host memory (read over the host link with 16-byte loads,
-// sixteen in flight per lane) instead of device memory (TMA bulk copies).
-template <int DT, bool HOST>
+// sixteen in flight per lane) instead of device memory (TMA bulk copies).  CUT (bf16 rows in
+// device memory): the call has top-k / top-p cuts, applied to each row as it is reached.
+template <int DT, bool HOST, bool CUT>
 __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Params P)
 {
+    static_assert(!CUT || (DT == 1 && !HOST), "cuts in KL: bf16 rows in device memory");
     constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char ring[];
+    CutSmem &C = *reinterpret_cast<CutSmem *>(ring + kLSmem);  // CUT only: after the rings
     __shared__ __align__(8) uint64_t full[kLWarps * kLStages];
     __shared__ float2 spart[kLMaxChunks];  // chunk partials of the row just streamed
     __shared__ float srm[kLMaxChunks];     // residual chunk masses (explicit q)
@@ -2318,6 +2659,16 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         const float temp = P.temp[r];
         const bool greedy = !(temp > 0.f);
         const float cs = greedy ? 0.f : kLog2e / temp;
+        int32_t tk = 0;
+        float tp = 1.f;
+        if constexpr (CUT) {
+            tk = P.top_k ? P.top_k[r] : 0;
+            tp = P.top_p ? P.top_p[r] : 1.f;
+        }
+        const bool use_k = tk > 0 && tk < P.V;
+        const bool use_p = tp > 0.f && tp < 1.f;
+        const bool cut = CUT && !greedy && (use_k || use_p);  // as K1F: a request's rows all or none
+        uint32_t thr = 0;  // cut key of the latest row (0 = none)
         // inputs of the acceptance test of draft position `lane` (warp 0), issued first
         float ls = 0.f, qs = 1.f, ua = 0.f, usl = 0.f;
         if (warp == 0 && !greedy) {
@@ -2399,6 +2750,9 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             __syncthreads();  // the row's chunk partials are in spart
             if (s_abort)
                 break;
+            if constexpr (CUT)
+                if (cut)  // uniform: the row's cut key, and its partials over the survivors
+                    thr = kl_cut_row<DT>(P, C, spart, row, cs, tk, tp, use_k, use_p);
             // ---- the row's statistics (K2's per-row combine) and, on a draft row, the test
             if (warp == 0) {
                 float m = -INFINITY, sv = 0.f, best = -INFINITY;
@@ -2434,7 +2788,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     bool accept = true;
                     if (lane == i && i < k) {
                         const float e = fmaf(ls, cs, -Mi);
-                        const float wstar = ex2(e);
+                        const float wstar = kept<DT, CUT>(ls, thr) ? ex2(e) : 0.f;
                         const double lhs = (double)ua * (double)qs;  // exact
                         const float ps = wstar / Si;
                         if (ps > 1e-30f || wstar == 0.f)
@@ -2466,9 +2820,9 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         const bool residual = !greedy && j < k && P.q;
         if (residual) {  // explicit q: residual chunk masses of row t_j by every warp (K3)
             const float Mj = s_M, Sj = s_S;
-            const ResidualMass<DT, false> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, 0u};
+            const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
             for (int c = warp; c < P.nchunks; c += kLWarps) {
-                const float z = warp_residual_chunk<DT, false, SPEC_KL_RESIDUAL_UNROLL>(
+                const float z = warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(
                     f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), lane);
                 if (lane == 0)
                     srm[c] = z;
@@ -2486,14 +2840,14 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 const float Z = chunk_total(cm, P.nchunks, lane);
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-                TargetMass<DT, false> f{rowj, cs, M, -1, 0u};
+                TargetMass<DT, CUT> f{rowj, cs, M, -1, thr};
                 token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
                                        lane);
             } else if (!residual) {  // one-hot draft: residual = p without x*
                 const float Mj = Mi;
                 const int xj = __shfl_sync(kFull, xs, j & 31);
                 const int cx = xj / P.chunk;
-                TargetMass<DT, false> fx{rowj, cs, Mj, xj, 0u};
+                TargetMass<DT, CUT> fx{rowj, cs, Mj, xj, thr};
                 const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
                                                  min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
                 ChunkMassFromPartials cm{spart, cs, Mj, cx, mx};
@@ -2506,7 +2860,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 }
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
-                TargetMass<DT, false> f{rowj, cs, Mj, excl, 0u};
+                TargetMass<DT, CUT> f{rowj, cs, Mj, excl, thr};
                 token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
                                        lane);
             } else {  // explicit q: locate in the residual (K3)
@@ -2516,7 +2870,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 if (Z > 0.f) {
                     float th;
                     const int cc = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
-                    const ResidualMass<DT, false> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, 0u};
+                    const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
                     token = (int)warp_find(f, (int64_t)cc * P.chunk,
                                            min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
                 } else {  // empty residual: draw from p itself
@@ -2524,7 +2878,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     const float Zp = chunk_total(cm, P.nchunks, lane);
                     float th;
                     const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
-                    const TargetMass<DT, false> ft{rowj, cs, Mj, -1, 0u};
+                    const TargetMass<DT, CUT> ft{rowj, cs, Mj, -1, thr};
                     token = (int)warp_find(ft, (int64_t)cc * P.chunk,
                                            min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
                 }
@@ -2825,6 +3179,7 @@ struct DeviceInfo {
     int blocks_residual[2] = {0, 0};
     int blocks_wr[2] = {0, 0};
     int blocks_lazy[2] = {0, 0};
+    int blocks_lazy_cut = 0;  // KL with cuts (bf16)
 };
 
 constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
@@ -2846,13 +3201,23 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_wr[DT], rowstats_wr_kernel<DT>, kWrThreads,
                                                            kWrSmem)))
         return e;
-    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kLSmem)))
         return e;
-    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem)))
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kLSmem)))
         return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT, false>, kLThreads,
-                                                           kLSmem)))
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT, false, false>,
+                                                           kLThreads, kLSmem)))
         return e;
+    if constexpr (DT == 1) {
+        if ((e = cudaFuncSetAttribute(lazy_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kLCutSmem)))
+            return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy_cut, lazy_kernel<1, false, true>,
+                                                               kLThreads, kLCutSmem)))
+            return e;
+    }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
 
@@ -3028,24 +3393,32 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             cudaEventRecord(ev[evi], stream);
         ++evi;
     };
-    // calls without cuts or diagnostics: KL reads rows only up to each request's first rejection
+    // calls without diagnostics (and with cuts only on bf16 rows in device memory): KL reads rows
+    // only up to each request's first rejection
     const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
-    if (!filtered && !debug && !q_stage && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
+    const bool cut_ok = !filtered || (DT == 1 && !rows_in_host && di->blocks_lazy_cut > 0);
+    if (cut_ok && !debug && !q_stage && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
         di->blocks_lazy[DT] > 0) {
         mark();
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
         mark();
+        if (filtered) {
+            const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy_cut, B);
+            lazy_kernel<1, false, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
+            mark();
+            return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+        }
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
         if (rows_in_host) {
             if (DT)
-                lazy_kernel<1, true><<<gridL, kLThreads, kLSmem, stream>>>(P);
+                lazy_kernel<1, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
             else
-                lazy_kernel<0, true><<<gridL, kLThreads, kLSmem, stream>>>(P);
+                lazy_kernel<0, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
         } else {
             if (DT)
-                lazy_kernel<1, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
+                lazy_kernel<1, false, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
             else
-                lazy_kernel<0, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
+                lazy_kernel<0, false, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
         }
         mark();
         return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -3484,9 +3857,9 @@ const char *spec_reject_status_string(spec_status status)
 
 int spec_reject_version(void) { return 100; }
 
-int spec_reject_num_kernels(int32_t B, int has_draft_probs, int has_filters)
+int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters)
 {
-    if (!has_filters && B >= SPEC_KL_MIN_REQUESTS)
+    if (B >= SPEC_KL_MIN_REQUESTS && (!has_filters || logits_dtype == SPEC_BF16))
         return 2;  // layout check, then the pass up to each first rejection
     return (has_filters ? 3 : 2) + (has_draft_probs ? 1 : 0);
 }

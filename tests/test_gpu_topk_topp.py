@@ -78,16 +78,18 @@ def test_filters_off_give_the_unfiltered_result():
     assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["acc"], b["acc"])
 
 
-def test_profiled_entry_with_filters_matches_filtered_entry():
+@pytest.mark.parametrize("B", [128, 48])
+def test_profiled_entry_with_filters_matches_filtered_entry(B):
     import torch
-    w = W.generate("large-128", top_k=50, top_p=0.9)
+    w = W.generate("large-128", B=B, top_k=50, top_p=0.9)
     a = PT.run_gpu(w)
     dev = torch.device("cuda", 0)
     d = binding.to_device(w, dev)
     dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, d["draft_probs"] is not None, dev)
-    nk = binding.num_kernels(w["B"], d["draft_probs"] is not None, True)
-    assert nk == 3 + (d["draft_probs"] is not None)
+    nk = binding.num_kernels(w["B"], d["draft_probs"] is not None, True, dt)
+    # bf16 rows: 64 requests or more take the first-rejection pass, fewer the full pass
+    assert nk == (2 if B >= 64 else 3 + (d["draft_probs"] is not None))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
     stream = torch.cuda.current_stream()
     for e in ev:
@@ -98,3 +100,79 @@ def test_profiled_entry_with_filters_matches_filtered_entry():
     assert np.array_equal(buf.out_tokens.cpu().numpy(), a["tokens"])
     assert np.array_equal(buf.out_num_accepted.cpu().numpy(), a["acc"])
     assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(nk))
+
+
+# ---------------------------------------------------------------------------- cuts in the first-rejection pass
+
+FLAT = dict(K=6, V=32000, dtype="bf16", sigma=0.3, temperature=1.0, draft="target_mix", p_match=0.8)
+
+
+@pytest.mark.parametrize("name,over,tk,tp", [
+    ("large-128", {}, 50, 0.9),          # cut inside the 512-key window, explicit q
+    ("large-128", {}, 0, 0.95),          # top-p alone
+    ("large-128", {}, 2000, 1.0),
+    ("deterministic", {}, 0, 0.9),       # one-hot drafts, ragged k
+    ("deterministic", {}, 100, 0.99),
+    ("greedy", {}, 5, 0.5),              # greedy requests take no cut
+    # flat rows (sigma 0.3): the window's 512 keys hold about 40% of the tokens and of the mass
+    (dict(FLAT, B=80, seed=61), {}, 0, 0.9),        # the top-p key lies below the window
+    (dict(FLAT, B=72, seed=62), {}, 20000, 0.95),   # top-k below it too: two radix selects
+    (dict(FLAT, B=64, seed=63, draft="noisy_q", q_sigma=0.3), {}, 700, 0.5),  # inside it
+])
+def test_first_rejection_pass_with_filters_equals_full_pass(name, over, tk, tp):
+    """bf16 calls with cuts on 64 or more requests take the first-rejection pass, which cuts each
+    row as it reaches it; the diagnostic entry runs the full pass (K1, K1F, K2, K3) over every
+    row.  The cut key and the chunk partials come from the same integer sums, so the outputs
+    are the same bit for bit, and they match the oracle."""
+    w = W.generate(name, top_k=tk, top_p=tp, **over) if isinstance(name, str) else \
+        W.generate(dict(name, top_k=tk, top_p=tp), name="flat-filters")
+    assert binding.reads_to_first_rejection(w["B"], True, binding.BF16)
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    assert lazy["status"] == 0 and full["status"] == 0
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
+
+
+def test_first_rejection_pass_mixed_filters_strided_rows():
+    """Per-request cuts with special values, greedy requests, and rows further apart than V with
+    a ragged last chunk (V not a multiple of 8, row stride a multiple of 8)."""
+    import torch
+    B = 96
+    rng = np.random.default_rng(23)
+    tk = rng.choice([0, 1, 5, 40, 7000, 20000], size=B).astype(np.int32)
+    tp = rng.choice([1.0, 0.5, 0.9, 1e-6, 0.999], size=B).astype(np.float32)
+    temps = np.where(np.arange(B) % 5 == 0, 0.0, 0.8).astype(np.float32)
+    w = W.generate(dict(B=B, K="ragged", K_max=6, V=20011, dtype="bf16", sigma=2.0, temperature=temps,
+                        draft="noisy_q", q_sigma=0.5, top_k=tk, top_p=tp, seed=29), name="mixed-filters-strided")
+    d = binding.to_device(w)
+    big = torch.zeros((w["T"], 20016), dtype=torch.bfloat16, device="cuda")
+    big[:, :20011] = d["target_logits"]
+    d["target_logits"] = big[:, :20011]
+    lazy = PT.run_gpu(w, device_tensors=d)
+    full = PT.run_gpu(w, debug=True, device_tensors=d)
+    assert lazy["status"] == 0
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
+
+
+def test_first_rejection_pass_with_filters_fp32_takes_full_pass():
+    """fp32 rows with cuts keep the full pass (the cut in the first-rejection pass is bf16 only)."""
+    assert not binding.reads_to_first_rejection(128, True, binding.F32)
+    assert binding.reads_to_first_rejection(128, False, binding.F32)
+    assert binding.num_kernels(128, True, True, binding.F32) == 4
+
+
+def test_first_rejection_pass_with_filters_on_negative_rows():
+    """Rows whose every logit is negative (the window's order keys below 0x8000 + 512, where a
+    token's key offset comes from its signed magnitude), with cuts inside and below the window."""
+    for seed, tk, tp in [(71, 50, 0.9), (72, 0, 0.95), (73, 20000, 1.0)]:
+        w = W.generate(dict(FLAT, B=64, seed=seed, top_k=tk, top_p=tp), name="negative-rows")
+        x = W.logits_as_f32(w) - np.float32(4.0)
+        w["logits"] = W.f32_to_bf16_bits(x)
+        assert W.logits_as_f32(w).max() < 0
+        lazy = PT.run_gpu(w)
+        full = PT.run_gpu(w, debug=True)
+        assert lazy["status"] == 0
+        assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+        PT.assert_parity(w, lazy)
