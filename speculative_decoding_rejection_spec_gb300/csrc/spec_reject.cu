@@ -2247,19 +2247,35 @@ constexpr size_t kLSmem = (size_t)kLWarps * kLStages * kUnitBytes;
 // digit histograms per selection) with the partials of K1F's general path.  Either way the cut
 // key and the partials are K1F's, bit for bit.
 
+constexpr int kCutHalfBytes = kUnitBytes / 2;  // a pass moves each chunk in two copies of this size
+static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot as two halves");
+
+constexpr int kCutNarrow = 128;       // largest keys counted per chunk first (one binade of bf16)
+constexpr int kCutNarrowChunks = 32;  // chunks (4096 tokens) a row may have for the per-chunk counts
+
 struct CutSmem {
-    unsigned hw[kLWarps][kFKeys + 32];  // per warp: tokens per key offset, then a sink per lane
+    unsigned hw[kLWarps][kFKeys + 32];                // per warp: tokens per key offset, then a sink per lane
+    unsigned short hcc[kCutNarrowChunks][kCutNarrow]; // per chunk: tokens of the kCutNarrow largest keys
     unsigned bh[kFKeys];                // block totals per key offset
     unsigned long long km[kFKeys];      // fixed-point mass of one token per key offset
+    unsigned long long bm[kFKeys];      // block masses per key offset (tokens x km)
+    union {
+        unsigned long long kmc[kFKeys + 1];  // km up to the cut offset, then zeros
+        unsigned long long rm[256];          // radix: weights per digit
+    };
     float cmx[kLMaxChunks];             // unfiltered chunk maxima
-    unsigned rc[256];                   // radix: tokens per digit
-    unsigned long long rm[256];         // radix: masses per digit
     unsigned long long red[kLWarps];
     double z;                           // normaliser (top-p alone), 2^-32 units
     float m;                            // row maximum
     int pos;                            // exact path: crossing offset (-1: fall back)
     int dsel;                           // radix: crossing digit (-1: none)
     unsigned long long dabove;
+    int32_t tk;                         // the current request's top-k and top-p
+    float tp;
+    uint32_t thr;                       // cut key of the latest row (0 = none)
+    int abort;                          // a copy of a pass did not land in time
+    uint64_t bar[kLWarps][2];           // per warp: one mbarrier per half of its ring slot
+    uint32_t ph[kLWarps];               // per warp: the parity each of the two is waiting for
 };
 constexpr size_t kLCutSmem = kLSmem + sizeof(CutSmem);
 
@@ -2306,12 +2322,21 @@ __device__ __forceinline__ void warp_digit_crossing(CutSmem &C, unsigned long lo
     }
 }
 
-// Cut of row `row` (all threads of the block; spart holds the row's unfiltered partials on
-// entry and the partials over the survivors on return).  Returns the cut key (0: no cut).
+// Cut of row `row` of V logits in chunks of `chunk` at scale cs, with the request's top-k and
+// top-p in C (all threads of the block; spart holds the row's unfiltered partials on entry and
+// the partials over the survivors on return).  Leaves the cut key in C.thr (0: no cut).  The
+// request's values stay in shared memory and the dimensions come by value, which keeps the
+// caller's registers free for its streaming loop.
+struct CutDims {
+    int V, chunk, nchunks;
+    int32_t *err;          // error word (a copy that does not land in time)
+    unsigned char *slot;   // the warp's ring slot (free while the row is cut)
+};
 template <int DT>
-__device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 *spart, const char *row, float cs,
-                                            int32_t tk, float tp, bool use_k, bool use_p)
+__device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 *spart, const char *row, float cs,
+                                            int32_t tk, float tp, bool use_k)
 {
+    const bool use_p = tp > 0.f && tp < 1.f;
     constexpr int kB = kFKeys;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = (int)(blockDim.x >> 5);
@@ -2356,61 +2381,106 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
         const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
         return kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
     };
-    // fn(bits) for every element of chunk c, 16-byte loads (the row is 16-byte aligned here)
-    auto chunk_for_each = [&](int c, auto fn) {
-        const int e0 = c * P.chunk, e1 = min(P.V, e0 + P.chunk);
-        const int v1 = e1 / 8;
-        for (int v = e0 / 8 + lane; v < v1; v += 4 * 32) {
-            uint4 w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (v + 32 * u < v1)
-                    w[u] = ld_stream(row + (size_t)(v + 32 * u) * 16);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (v + 32 * u < v1) {
-                    fn(w[u].x & 0xffffu);
-                    fn(w[u].x >> 16);
-                    fn(w[u].y & 0xffffu);
-                    fn(w[u].y >> 16);
-                    fn(w[u].z & 0xffffu);
-                    fn(w[u].z >> 16);
-                    fn(w[u].w & 0xffffu);
-                    fn(w[u].w >> 16);
+    // A pass over this warp's chunks c = warp, warp + nw, ...: each chunk in two copies of at
+    // most 4 KB (TMA, into the two halves of the warp's ring slot, both in flight), then
+    // start(c), fv(w) for each 16-byte vector w of its elements from shared memory and fe(bits)
+    // for the last elements of the row past a multiple of 8 (global memory), then done(c).  Chunks with want(c) false are not
+    // read (empty copies keep the barriers' phases in step).  A copy that does not land in time
+    // sets C.abort; the pass still returns through every barrier of the block.
+    auto pass = [&](auto want, auto start, auto fv, auto fe, auto done) {
+        constexpr int kHalf = kCutHalfBytes / 2;  // bf16 elements per copy
+        const int nmine = warp < P.nchunks ? (P.nchunks - 1 - warp) / nw + 1 : 0;
+        const int n = 2 * nmine;
+        uint32_t ph = C.ph[warp];
+        auto range = [&](int u, int &c, int &lo, int &hi) {
+            c = warp + nw * (u >> 1);
+            const int c0 = c * P.chunk, c1 = min(P.V, c0 + P.chunk);
+            lo = min(c1, c0 + (u & 1) * kHalf);
+            hi = min(c1, lo + kHalf);
+        };
+        auto issue = [&](int u) {  // lane 0
+            int c, lo, hi;
+            range(u, c, lo, hi);
+            const uint32_t bytes = want(c) ? ((uint32_t)(hi - lo) * 2u) & ~15u : 0u;
+            uint64_t *bar = &C.bar[warp][u & 1];
+            mbar_arrive_expect_tx(bar, bytes);
+            if (bytes)
+                bulk_g2s(P.slot + (u & 1) * kCutHalfBytes, row + (size_t)lo * 2, bytes, bar);
+        };
+        if (lane == 0)
+            for (int u = 0; u < 2 && u < n; ++u)
+                issue(u);
+        for (int u = 0; u < n; ++u) {
+            const int sl = u & 1;
+            if (!__all_sync(kFull, mbar_wait(&C.bar[warp][sl], (ph >> sl) & 1u, P.err))) {
+                if (lane == 0) {  // let the copies still in flight land before the slot is reused
+                    for (int u2 = u; u2 < u + 2 && u2 < n; ++u2)
+                        mbar_wait(&C.bar[warp][u2 & 1], (ph >> (u2 & 1)) & 1u, P.err);
+                    C.abort = 1;
                 }
+                break;
+            }
+            ph ^= 1u << sl;
+            int c, lo, hi;
+            range(u, c, lo, hi);
+            if (want(c)) {
+                if (sl == 0)
+                    start(c);
+                const uint4 *st = reinterpret_cast<const uint4 *>(P.slot + sl * kCutHalfBytes);
+                const int nv = (hi - lo) >> 3;
+                for (int v = lane; v < nv; v += 32)
+                    fv(st[v]);
+                for (int i = lo + nv * 8 + lane; i < hi; i += 32)
+                    fe((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i));
+                if (sl == 1)
+                    done(c);
+            }
+            __syncwarp();  // the half is consumed: refill it
+            if (lane == 0 && u + 2 < n)
+                issue(u + 2);
         }
-        for (int i = v1 * 8 + lane; i < e1; i += 32)
-            fn((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i));
+        if (lane == 0)
+            C.ph[warp] = ph;
+    };
+    auto all = [](int) { return true; };
+    auto nop = [](int) {};
+    auto each8 = [](const uint4 &w, auto fe) {
+        fe(w.x & 0xffffu);
+        fe(w.x >> 16);
+        fe(w.y & 0xffffu);
+        fe(w.y >> 16);
+        fe(w.z & 0xffffu);
+        fe(w.z >> 16);
+        fe(w.w & 0xffffu);
+        fe(w.w >> 16);
     };
 
-    // ---- 1. counts by key offset
-    {
-        unsigned *h = C.hw[warp];
-        const uint32_t sink = (uint32_t)kB + (uint32_t)lane;
-        for (int c = warp; c < P.nchunks; c += nw)
-            chunk_for_each(c, [&](uint32_t b16) { atomicAdd(&h[min(offset(b16), sink)], 1u); });
-    }
-    __syncthreads();
-    for (int o = threadIdx.x; o < kB; o += blockDim.x) {
-        unsigned tot = 0;
-        for (int w = 0; w < nw; ++w)
-            tot += C.hw[w][o];
-        C.bh[o] = tot;
-        C.km[o] = (uint32_t)o < kmax ? fx(x_of<1>(kmax - (uint32_t)o)) : 0ull;
-    }
-    __syncthreads();
-
-    // ---- 2. selection by warp 0 (lanes own 16 consecutive offsets), K1F's one-pass rules
+    // block totals, one token's mass and the block masses for the offsets below n (all threads)
+    auto totals = [&](int n, auto count) {
+        for (int o = threadIdx.x; o < n; o += blockDim.x) {
+            const unsigned tot = count(o);
+            const unsigned long long km = (uint32_t)o < kmax ? fx(x_of<1>(kmax - (uint32_t)o)) : 0ull;
+            C.bh[o] = tot;
+            C.km[o] = km;
+            C.bm[o] = (unsigned long long)tot * km;
+        }
+        __syncthreads();
+    };
+    auto select_window = [&](int win) {
+    // ---- 2. selection by warp 0 over a window of n keys (lanes own n / 32 consecutive offsets),
+    // K1F's one-pass rules; C.pos = the cut offset, or -1 when the cut lies below the window
     if (warp == 0) {
-        constexpr int PER = kB / 32;
+        const int n = win;
+        const int PER = n / 32;  // a power of two
         // first offset o <= olim at which w(0) + ... + w(o) >= target (-1 if never)
         auto crossing = [&](unsigned long long target, int olim, bool by_mass) -> int {
             const int b0 = lane * PER;
+            auto w = [&](int o) -> unsigned long long {
+                return o > olim ? 0ull : by_mass ? C.bm[o] : (unsigned long long)C.bh[o];
+            };
             unsigned long long mine = 0;
-#pragma unroll 4
-            for (int k = 0; k < PER; ++k)
-                if (b0 + k <= olim)
-                    mine += by_mass ? (unsigned long long)C.bh[b0 + k] * C.km[b0 + k] : (unsigned long long)C.bh[b0 + k];
+            for (int k = 0; k < PER; ++k)  // in a lane-rotated order: no shared-memory bank conflicts
+                mine += w(b0 + ((k + lane) & (PER - 1)));
             unsigned long long inc = mine;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -2422,7 +2492,7 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
             int pos = -1;
             if (c < target && inc >= target)
                 for (int k = 0; k < PER; ++k) {
-                    c += by_mass ? (unsigned long long)C.bh[b0 + k] * C.km[b0 + k] : (unsigned long long)C.bh[b0 + k];
+                    c += w(b0 + k);
                     if (c >= target) {
                         pos = b0 + k;
                         break;
@@ -2432,9 +2502,9 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
             return found ? __shfl_sync(kFull, pos, __ffs(found) - 1) : -1;
         };
         bool ok = true;
-        int pcut = kB - 1;
+        int pcut = n - 1;
         if (use_k) {
-            pcut = crossing((unsigned long long)tk, kB - 1, false);
+            pcut = crossing((unsigned long long)tk, n - 1, false);
             ok = pcut >= 0;  // fewer than k tokens in the window
         }
         if (ok && use_p) {
@@ -2442,7 +2512,7 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
             if (use_k) {
                 unsigned long long sk = 0;
                 for (int o = lane; o <= pcut; o += 32)
-                    sk += (unsigned long long)C.bh[o] * C.km[o];
+                    sk += C.bm[o];
                 target = (unsigned long long)ceil((double)tp * (double)warp_sum_u64(sk));
             } else {
                 target = (unsigned long long)ceil((double)tp * C.z);
@@ -2453,30 +2523,124 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
             else
                 ok = use_k;  // top-p alone: the cut lies below the window
         }
+        if (ok && n == kB)  // one token's mass by key offset, zero past the cut (no branch in the pass)
+            for (int o = lane; o <= kB; o += 32)
+                C.kmc[o] = o <= pcut ? C.km[o] : 0ull;
         if (lane == 0)
             C.pos = ok ? pcut : -1;
     }
+    };
+
+    // counts by key offset over the w largest keys, one histogram per warp with a sink per lane
+    // for the rest (no branch); with `flush`, the counts of each chunk move to C.hcc[c] after
+    // the chunk (at most 4096 tokens: 16 bits)
+    // A narrow window (w <= kCutNarrow) of a row whose maximum is at least 512 keys above +0
+    // counts only the tokens inside it: an integer test on both halves of each word (bits &
+    // 0x7fff plus 0x8000 - lowest carries into bit 15 exactly when the bits are at least the
+    // window's lowest, and bit 15 of the bits is clear for positive logits) marks them, and a
+    // lane counts its marked tokens one by one (usually none): one atomic instruction per vector
+    // where every token would take eight.
+    auto count_pass = [&](int w, bool flush) {
+        unsigned *h = C.hw[warp];
+        const uint32_t sink = (uint32_t)w + (uint32_t)lane;
+        auto fe = [&](uint32_t b16) { atomicAdd(&h[min(offset(b16), sink)], 1u); };
+        const bool marks = plain && w <= kCutNarrow;
+        const uint32_t add = 0x8000u - (kmax - 0x8000u - (uint32_t)(w - 1));  // plain: kmax - 0x8000 >= kB
+        const uint32_t add2 = add | (add << 16);
+        auto hit = [&](uint32_t x) { return ((x & 0x7fff7fffu) + add2) & ~x & 0x80008000u; };
+        auto vec = [&](const uint4 &v) {
+            if (!marks) {
+                each8(v, fe);
+                return;
+            }
+            const uint32_t h0 = hit(v.x), h1 = hit(v.y), h2 = hit(v.z), h3 = hit(v.w);
+            uint32_t m = ((h0 >> 15) & 1u) | ((h0 >> 30) & 2u) | ((h1 >> 13) & 4u) | ((h1 >> 28) & 8u) |
+                         ((h2 >> 11) & 16u) | ((h2 >> 26) & 32u) | ((h3 >> 9) & 64u) | ((h3 >> 24) & 128u);
+            while (m) {
+                const int j = __ffs(m) - 1;
+                m &= m - 1;
+                const uint32_t word = j < 4 ? (j < 2 ? v.x : v.y) : (j < 6 ? v.z : v.w);
+                fe((j & 1) ? word >> 16 : word & 0xffffu);
+            }
+        };
+        pass(all, nop, vec, fe, [&](int c) {
+            if (flush) {
+                __syncwarp();  // every lane's counts of the chunk are in
+                for (int o = lane; o < w; o += 32) {
+                    C.hcc[c][o] = (unsigned short)h[o];
+                    h[o] = 0u;
+                }
+                __syncwarp();
+            }
+        });
+        __syncthreads();
+    };
+
+    // ---- 1a. with at most kCutNarrowChunks chunks, first the kCutNarrow largest keys counted per
+    // chunk: a cut inside them gets its partials from the counts, with no second pass (and
+    // nearly every token lands in its lane's sink, which costs the least)
+    if (P.nchunks <= kCutNarrowChunks) {
+        count_pass(kCutNarrow, true);
+        totals(kCutNarrow, [&](int o) {
+            unsigned t = 0;
+            for (int c = 0; c < P.nchunks; ++c)
+                t += C.hcc[c][o];
+            return t;
+        });
+        select_window(kCutNarrow);
+        __syncthreads();
+        const int pn = C.pos;
+        if (pn >= 0) {  // K1F's one-pass partials
+            const uint32_t thr = kmax - (uint32_t)pn;
+            for (int c = warp; c < P.nchunks; c += nw) {
+                const float mk = C.cmx[c];
+                float mc = -INFINITY, sc = 0.f;
+                if (mk > -INFINITY && key_of<1>(mk) >= thr) {
+                    mc = mk;
+                    unsigned long long sum = 0;
+                    for (int o = lane; o <= pn; o += 32)
+                        sum += (unsigned long long)C.hcc[c][o] * C.km[o];
+                    sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
+                }
+                if (lane == 0)
+                    spart[c] = make_float2(mc, sc);
+            }
+            __syncthreads();
+            return thr;
+        }
+        for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
+            (&C.hw[0][0])[i] = 0u;  // sinks of the narrow window sit inside the wide one
+        __syncthreads();
+    }
+
+    // ---- 1. counts over the kFKeys largest keys
+    count_pass(kB, false);
+    totals(kB, [&](int o) {
+        unsigned t = 0;
+        for (int w = 0; w < nw; ++w)
+            t += C.hw[w][o];
+        return t;
+    });
+    select_window(kB);
     __syncthreads();
     const int pcut = C.pos;
     if (pcut >= 0) {
         // ---- 3. chunk partials over the survivors: masses relative to the row maximum, rescaled
         const uint32_t thr = kmax - (uint32_t)pcut;
-        for (int c = warp; c < P.nchunks; c += nw) {
-            const float mk = C.cmx[c];
-            float mc = -INFINITY, sc = 0.f;
-            if (mk > -INFINITY && key_of<1>(mk) >= thr) {
-                mc = mk;
-                unsigned long long sum = 0;
-                chunk_for_each(c, [&](uint32_t b16) {
-                    const uint32_t o = offset(b16);
-                    if (o <= (uint32_t)pcut)
-                        sum += C.km[o];
-                });
-                sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
-            }
-            if (lane == 0)
-                spart[c] = make_float2(mc, sc);
-        }
+        auto live = [&](int c) { return C.cmx[c] > -INFINITY && key_of<1>(C.cmx[c]) >= thr; };
+        for (int c = warp; c < P.nchunks; c += nw)
+            if (lane == 0 && !live(c))
+                spart[c] = make_float2(-INFINITY, 0.f);
+        unsigned long long sum = 0;
+        auto fe = [&](uint32_t b16) { sum += C.kmc[min(offset(b16), (uint32_t)kB)]; };
+        pass(live, nop, [&](const uint4 &w) { each8(w, fe); }, fe,
+             [&](int c) {
+                 const float mc = C.cmx[c];
+                 const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
+                 if (lane == 0)
+                     spart[c] = make_float2(mc, sc);
+                 sum = 0;
+             });
         __syncthreads();
         return thr;
     }
@@ -2499,20 +2663,20 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
             __syncthreads();
             unsigned *hc = C.hw[warp];
             unsigned long long *hm = reinterpret_cast<unsigned long long *>(C.hw[warp]);
-            for (int c = warp; c < P.nchunks; c += nw)
-                chunk_for_each(c, [&](uint32_t b16) {
-                    const uint32_t key = key16(b16);
-                    if (key >= lo && (level == 0 || (key >> 8) == (prefix >> 8))) {
-                        const uint32_t d = (key >> shift) & 255u;
-                        if (by_mass) {
-                            const unsigned long long w = fx(__uint_as_float(b16 << 16));
-                            if (w)
-                                atomicAdd(&hm[d], w);
-                        } else {
-                            atomicAdd(&hc[d], 1u);
-                        }
+            auto fe = [&](uint32_t b16) {
+                const uint32_t key = key16(b16);
+                if (key >= lo && (level == 0 || (key >> 8) == (prefix >> 8))) {
+                    const uint32_t d = (key >> shift) & 255u;
+                    if (by_mass) {
+                        const unsigned long long w = fx(__uint_as_float(b16 << 16));
+                        if (w)
+                            atomicAdd(&hm[d], w);
+                    } else {
+                        atomicAdd(&hc[d], 1u);
                     }
-                });
+                }
+            };
+            pass(all, nop, [&](const uint4 &w) { each8(w, fe); }, fe, nop);
             __syncthreads();
             for (int d = threadIdx.x; d < 256; d += blockDim.x) {
                 unsigned long long t = 0;
@@ -2550,25 +2714,41 @@ __device__ __noinline__ uint32_t kl_cut_row(const Params &P, CutSmem &C, float2 
     const uint32_t thr = max(max(tau, lam), 1u);
 
     // ---- chunk partials over the survivors, relative to each chunk's maximum (K1F's general path)
-    for (int c = warp; c < P.nchunks; c += nw) {
-        const float mk = C.cmx[c];
-        float mc = -INFINITY, sc = 0.f;
-        if (mk > -INFINITY && key_of<1>(mk) >= thr) {
-            mc = mk;
-            const float Mc = mc * cs;
-            unsigned long long sum = 0;
-            chunk_for_each(c, [&](uint32_t b16) {
-                if (key16(b16) >= thr)
-                    sum += __float2ull_rn(ex2(fmaf(__uint_as_float(b16 << 16), cs, -Mc)) * kTwo32);
-            });
-            sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f;
-        }
-        if (lane == 0)
-            spart[c] = make_float2(mc, sc);
-    }
+    auto live = [&](int c) { return C.cmx[c] > -INFINITY && key_of<1>(C.cmx[c]) >= thr; };
+    for (int c = warp; c < P.nchunks; c += nw)
+        if (lane == 0 && !live(c))
+            spart[c] = make_float2(-INFINITY, 0.f);
+    unsigned long long sum = 0;
+    float Mc = 0.f;  // the chunk's maximum, scaled
+    auto fe = [&](uint32_t b16) {
+        if (key16(b16) >= thr)
+            sum += __float2ull_rn(ex2(fmaf(__uint_as_float(b16 << 16), cs, -Mc)) * kTwo32);
+    };
+    pass(live, [&](int c) { Mc = C.cmx[c] * cs; }, [&](const uint4 &w) { each8(w, fe); }, fe,
+         [&](int c) {
+             const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f;
+             if (lane == 0)
+                 spart[c] = make_float2(C.cmx[c], sc);
+             sum = 0;
+         });
     __syncthreads();
     return thr;
 }
+
+template <int DT> __device__ __noinline__ void kl_cut_row(const CutDims P, CutSmem &C, float2 *spart, const char *row, float cs)
+{
+    const int32_t tk = C.tk;
+    const float tp = C.tp;
+    const bool use_k = tk > 0 && tk < P.V;
+    const bool use_p = tp > 0.f && tp < 1.f;
+    if (!(use_k || use_p))
+        return;  // C.thr stays 0
+    const uint32_t thr = kl_cut_key<DT>(P, C, spart, row, cs, tk, tp, use_k);
+    if (threadIdx.x == 0)
+        C.thr = thr;
+    __syncthreads();
+}
+
 
 // Layout check and request-queue reset before KL (one block).
 __global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
@@ -2607,6 +2787,14 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     }
     if (threadIdx.x < kLWarps * kLStages)
         mbar_init(&full[threadIdx.x], 1);
+    if constexpr (CUT) {
+        if (threadIdx.x < 2 * kLWarps)
+            mbar_init(&C.bar[0][0] + threadIdx.x, 1);
+        if (threadIdx.x < kLWarps)
+            C.ph[threadIdx.x] = 0;
+        if (threadIdx.x == 0)
+            C.abort = 0;
+    }
     mbar_fence_init();
     if (threadIdx.x == 0)
         s_abort = 0;
@@ -2659,16 +2847,12 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         const float temp = P.temp[r];
         const bool greedy = !(temp > 0.f);
         const float cs = greedy ? 0.f : kLog2e / temp;
-        int32_t tk = 0;
-        float tp = 1.f;
-        if constexpr (CUT) {
-            tk = P.top_k ? P.top_k[r] : 0;
-            tp = P.top_p ? P.top_p[r] : 1.f;
-        }
-        const bool use_k = tk > 0 && tk < P.V;
-        const bool use_p = tp > 0.f && tp < 1.f;
-        const bool cut = CUT && !greedy && (use_k || use_p);  // as K1F: a request's rows all or none
-        uint32_t thr = 0;  // cut key of the latest row (0 = none)
+        if constexpr (CUT)
+            if (threadIdx.x == 0) {  // read by the cut after the first row's barrier
+                C.tk = P.top_k ? P.top_k[r] : 0;
+                C.tp = P.top_p ? P.top_p[r] : 1.f;
+                C.thr = 0;
+            }
         // inputs of the acceptance test of draft position `lane` (warp 0), issued first
         float ls = 0.f, qs = 1.f, ua = 0.f, usl = 0.f;
         if (warp == 0 && !greedy) {
@@ -2751,8 +2935,11 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             if (s_abort)
                 break;
             if constexpr (CUT)
-                if (cut)  // uniform: the row's cut key, and its partials over the survivors
-                    thr = kl_cut_row<DT>(P, C, spart, row, cs, tk, tp, use_k, use_p);
+                if (!greedy) {  // uniform: the row's cut key, and its partials over the survivors
+                    kl_cut_row<DT>(CutDims{P.V, P.chunk, P.nchunks, P.err, slots}, C, spart, row, cs);
+                    if (C.abort)
+                        break;  // uniform (read after the cut's last barrier)
+                }
             // ---- the row's statistics (K2's per-row combine) and, on a draft row, the test
             if (warp == 0) {
                 float m = -INFINITY, sv = 0.f, best = -INFINITY;
@@ -2788,7 +2975,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     bool accept = true;
                     if (lane == i && i < k) {
                         const float e = fmaf(ls, cs, -Mi);
-                        const float wstar = kept<DT, CUT>(ls, thr) ? ex2(e) : 0.f;
+                        const float wstar = kept<DT, CUT>(ls, CUT ? C.thr : 0u) ? ex2(e) : 0.f;
                         const double lhs = (double)ua * (double)qs;  // exact
                         const float ps = wstar / Si;
                         if (ps > 1e-30f || wstar == 0.f)
@@ -2810,7 +2997,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 break;
             }
         }
-        if (s_abort)
+        if (s_abort || (CUT && C.abort))
             break;
 
         // ---- the output token at row t_j (K2 / K3 arithmetic)
@@ -2818,6 +3005,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         const char *rowj = row_ptr<DT>(P, tj);
         int token = -1;
         const bool residual = !greedy && j < k && P.q;
+        const uint32_t thr = CUT ? C.thr : 0u;  // cut key of row t_j
         if (residual) {  // explicit q: residual chunk masses of row t_j by every warp (K3)
             const float Mj = s_M, Sj = s_S;
             const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
