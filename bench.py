@@ -462,7 +462,9 @@ def main():
         dom_bytes = rows_read * w["V"] * es + rejecting * w["V"] * 4 + small
         dom_name = ("KL: lazy_kernel (request queue, rows streamed through warp-private TMA rings up to "
                     "the first rejection, draw in the same block)")
-        traffic = traffic_lazy_for(args.workload)
+        if filtered:
+            dom_name += "; each reached row cut in the block (key-offset counts, per-chunk partials)"
+        traffic = traffic_lazy_for(args.workload + (f"+k{args.top_k}+p{args.top_p}" if filtered else ""))
         call_bytes = dom_bytes
     dom_s = statistics.mean(row[dom].elapsed_time(row[dom + 1]) for row in ev) / 1e3
     achieved = dom_bytes / dom_s / 1e9
