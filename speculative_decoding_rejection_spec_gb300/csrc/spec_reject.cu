@@ -123,6 +123,10 @@ struct Params {
     const float *top_p;    // [B]
     unsigned long long *counters;  // [SPEC_METRIC_COUNT] acceptance counters to add to, or null
     uint32_t *thr;         // [T] order key below which a token is cut (0 = none)
+    // rows read from host memory by KL: device copies of the target rows it streams ([T, lstride],
+    // written only where read) and of the draft rows its residual passes read ([T - B, V])
+    char *lstage;
+    float *qstage;
     // diagnostics (all may be null)
     float *dbg_pdraft;
     float *dbg_z;
@@ -2095,8 +2099,9 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 
 // Residual mass sum max(0, p(v) - q(v)) over the chunk [lo, hi) by one warp: lane-strided
 // 16-byte groups of target logits and draft probabilities, four groups in flight per lane.
-template <int DT, bool F, int U = 4>
-__device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &f, int64_t lo, int64_t hi, int lane)
+template <int DT, bool F, int U = 4, bool STAGE = false>
+__device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &f, int64_t lo, int64_t hi, int lane,
+                                                     float *qdst = nullptr)
 {
     constexpr int VEC = Elem<DT>::kVec;
     constexpr int ES = Elem<DT>::kSize;
@@ -2112,6 +2117,8 @@ __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &
 #pragma unroll
             for (int h = 0; h < VEC / 4; ++h) {
                 const uint4 qw = ld_stream(f.qrow + v + 4 * h);
+                if (STAGE)  // the device copy of the draft row, for the draw that follows
+                    *reinterpret_cast<uint4 *>(qdst + v + 4 * h) = qw;
                 acc[0] += fmaxf(0.f, f.pm(x[4 * h + 0]) - __uint_as_float(qw.x));
                 acc[1] += fmaxf(0.f, f.pm(x[4 * h + 1]) - __uint_as_float(qw.y));
                 acc[2] += fmaxf(0.f, f.pm(x[4 * h + 2]) - __uint_as_float(qw.z));
@@ -2120,8 +2127,11 @@ __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &
         }
         tail = lo + ng * VEC;
     }
-    for (int64_t v = tail + lane; v < hi; v += 32)
+    for (int64_t v = tail + lane; v < hi; v += 32) {
         acc[0] += f.one(v);
+        if (STAGE)
+            qdst[v] = __ldg(f.qrow + v);
+    }
     return warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
 }
 
@@ -2893,6 +2903,18 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                         const int vi = kk * 32 + lane;
                         v[kk] = (vi < R.nvec) ? ld_stream(u0 + (size_t)vi * 16) : neg_inf_vec<DT>();
                     }
+                    if (P.lstage) {  // the device copy of the row, for the residual pass and the draw
+                        char *d0 = P.lstage + (size_t)(tb + i) * P.lstride * ES + R.lo * ES;
+#pragma unroll
+                        for (int kk = 0; kk < kVecPerLane; ++kk) {
+                            const int vi = kk * 32 + lane;
+                            if (vi < R.nvec)
+                                *reinterpret_cast<uint4 *>(d0 + (size_t)vi * 16) = v[kk];
+                        }
+                        for (int64_t e = R.vhi + lane; e < R.hi; e += 32)
+                            for (int b = 0; b < ES; ++b)
+                                d0[(e - R.lo) * ES + b] = row[e * ES + b];
+                    }
                     if (greedy)
                         argmax_regs<DT>(&spart[c], lane, v, R, row);
                     else
@@ -3002,7 +3024,9 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
 
         // ---- the output token at row t_j (K2 / K3 arithmetic)
         const int64_t tj = tb + j;
-        const char *rowj = row_ptr<DT>(P, tj);
+        // rows in host memory: the output row and the draft row come from their device copies
+        const char *rowj = (HOST && P.lstage) ? P.lstage + (size_t)tj * P.lstride * ES : row_ptr<DT>(P, tj);
+        float *qstage_j = (HOST && P.qstage) ? P.qstage + (db + j) * (int64_t)P.V : nullptr;
         int token = -1;
         const bool residual = !greedy && j < k && P.q;
         const uint32_t thr = CUT ? C.thr : 0u;  // cut key of row t_j
@@ -3010,8 +3034,10 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             const float Mj = s_M, Sj = s_S;
             const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
             for (int c = warp; c < P.nchunks; c += kLWarps) {
-                const float z = warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(
-                    f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), lane);
+                const int64_t lo = (int64_t)c * P.chunk, hi = min((int64_t)P.V, (int64_t)(c + 1) * P.chunk);
+                const float z = (HOST && qstage_j)
+                                    ? warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL, true>(f, lo, hi, lane, qstage_j)
+                                    : warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(f, lo, hi, lane);
                 if (lane == 0)
                     srm[c] = z;
             }
@@ -3058,7 +3084,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 if (Z > 0.f) {
                     float th;
                     const int cc = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
-                    const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
+                    const ResidualMass<DT, CUT> f{rowj, qstage_j ? qstage_j : P.q + (db + j) * P.qstride, cs, Mj,
+                                                  1.f / Sj, thr};
                     token = (int)warp_find(f, (int64_t)cc * P.chunk,
                                            min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
                 } else {  // empty residual: draw from p itself
@@ -3513,7 +3540,8 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 const float *temp, int32_t *out_tokens, int32_t *out_acc, void *ws, size_t ws_bytes,
                 cudaStream_t stream, float *dbg_m, float *dbg_s, int32_t *dbg_am, float *dbg_pd, float *dbg_z,
                 cudaEvent_t *ev = nullptr, int nev = 0, const int32_t *top_k = nullptr, const float *top_p = nullptr,
-                int64_t *counters = nullptr, float *q_stage = nullptr, bool rows_in_host = false)
+                int64_t *counters = nullptr, float *q_stage = nullptr, bool rows_in_host = false,
+                char *row_stage = nullptr)
 {
     spec_status st = check_args(logits, dt, T, V, lstride, q, qstride, ids, cu, B, uni, temp, out_tokens, out_acc, ws);
     if (st != SPEC_OK)
@@ -3585,7 +3613,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     // only up to each request's first rejection
     const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
     const bool cut_ok = !filtered || (DT == 1 && !rows_in_host && di->blocks_lazy_cut > 0);
-    if (cut_ok && !debug && !q_stage && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
+    if (cut_ok && !debug && (!q_stage || rows_in_host) && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
         di->blocks_lazy[DT] > 0) {
         mark();
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
@@ -3598,6 +3626,10 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         }
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
         if (rows_in_host) {
+            // the rows it reads over the host link are copied to device memory for the
+            // residual pass and the draw (q_stage: rows of V floats, row_stage: rows of lstride)
+            P.lstage = row_stage;
+            P.qstage = q ? q_stage : nullptr;
             if (DT)
                 lazy_kernel<1, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
             else
@@ -3860,7 +3892,7 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
         all_in_place
             ? run(logits_in_place, logits_dtype, T, V, V, q_in_place, V, d_ids, d_cu, B, d_uni, d_temp, d_tok, d_acc,
                   d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr,
-                  nullptr, nullptr, true)
+                  nullptr, has_q ? d_q : nullptr, true, d_logits)
             : run(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr, V, d_ids, d_cu,
                   B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr,
                   nullptr, 0, nullptr, nullptr, nullptr, q_in_place ? d_q : nullptr);

@@ -320,8 +320,9 @@ def test_host_entry_matches_device_entry():
 def test_host_entry_reads_pinned_inputs_in_place(name):
     """Pinned inputs are read in place by the kernels: below 64 requests the draft probabilities
     (the rows the residual pass needs are staged into the arena), from 64 requests the target
-    logits too (the first-rejection pass reads rows over the host link; nothing large is
-    copied).  The result is the device entry's, bit for bit."""
+    logits too (the first-rejection pass reads rows over the host link and keeps a device copy
+    of exactly those rows, and of the draft row of each explicit-q rejection, for its residual
+    pass and draw).  The result is the device entry's, bit for bit."""
     import torch
     w = W.generate(name)
     dev = PT.run_gpu(w)
@@ -344,19 +345,40 @@ def test_host_entry_reads_pinned_inputs_in_place(name):
     # the arena holds the logits copy first, then the q copy (256-byte aligned regions)
     es = 2 if w["dtype"] == "bf16" else 4
     base = (-arena.data_ptr()) % 256
-    lbytes = es * w["T"] * w["V"]
+    T, B, V = w["T"], w["B"], w["V"]
+    lbytes = es * T * V
     q0 = base + ((lbytes + 255) // 256) * 256
-    if w["B"] >= 64:  # nothing large was copied
-        assert bool((arena[base:base + lbytes] == 0xA5).all())
+    nd = T - B
+    cu = w["cu_num_draft"]
+    ks = np.diff(cu)
+
+    def rows_written(region, n, width):
+        r = region.view(n, width)
+        return r, set(torch.nonzero((r != 0xA5).any(dim=1)).flatten().cpu().numpy().tolist())
+
+    def same_bytes(r, rows, src):
+        idx = sorted(rows)
+        want = torch.from_numpy(np.ascontiguousarray(src.view(np.uint8).reshape(len(src), -1)[idx])).cuda()
+        return torch.equal(r[torch.tensor(idx, device="cuda")], want)
+
+    # rejecting requests with explicit q (temperature > 0): their draft row at the output position
+    rej = [int(cu[r]) + int(acc[r]) for r in range(B)
+           if has_q and w["temperature"][r] > 0 and 0 <= acc[r] < ks[r]]
+    if B >= 64:
+        # exactly the target rows up to each request's output row were read (and copied)
+        want = {int(cu[r]) + r + i for r in range(B) for i in range(int(acc[r]) + 1)}
+        lr, got = rows_written(arena[base:base + lbytes], T, es * V)
+        assert got == want, (len(got), len(want))
+        assert same_bytes(lr, got, w["logits"])
         if has_q:
-            assert bool((arena[q0:q0 + 4 * (w["T"] - w["B"]) * w["V"]] == 0xA5).all())
-    elif has_q:  # only the rows for the residual pass were staged, each equal to its row of q
-        nd, V = w["T"] - w["B"], w["V"]
-        qregion = arena[q0:q0 + 4 * nd * V].view(nd, 4 * V)
-        written = torch.nonzero((qregion != 0xA5).any(dim=1)).flatten().cpu().numpy()
-        assert 0 < len(written) <= w["B"]
-        qbytes = torch.from_numpy(w["draft_probs"].view(np.uint8).reshape(nd, 4 * V)[written]).cuda()
-        assert torch.equal(qregion[torch.from_numpy(written).cuda()], qbytes)
+            qr, gq = rows_written(arena[q0:q0 + 4 * nd * V], nd, 4 * V)
+            assert gq == set(rej) and same_bytes(qr, gq, w["draft_probs"])
+    else:
+        assert bool((arena[base:base + lbytes] != 0xA5).any())  # copied whole
+        if has_q:  # only the rows for the residual pass were staged, each equal to its row of q
+            qr, gq = rows_written(arena[q0:q0 + 4 * nd * V], nd, 4 * V)
+            assert 0 < len(gq) <= B and gq == set(rej)
+            assert same_bytes(qr, gq, w["draft_probs"])
 
 
 # ---------------------------------------------------------------------------- rows read up to the first rejection
