@@ -2234,6 +2234,9 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #ifndef SPEC_KL_RESIDUAL_UNROLL
 #define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass
 #endif
+#ifndef SPEC_KL_HOST_RESIDUAL_UNROLL
+#define SPEC_KL_HOST_RESIDUAL_UNROLL 8  // the same, draft rows read over the host link
+#endif
 #ifndef SPEC_KL_MIN_BLOCKS
 #define SPEC_KL_MIN_BLOCKS 2  // blocks per SM
 #endif
@@ -3036,7 +3039,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             for (int c = warp; c < P.nchunks; c += kLWarps) {
                 const int64_t lo = (int64_t)c * P.chunk, hi = min((int64_t)P.V, (int64_t)(c + 1) * P.chunk);
                 const float z = (HOST && qstage_j)
-                                    ? warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL, true>(f, lo, hi, lane, qstage_j)
+                                    ? warp_residual_chunk<DT, CUT, SPEC_KL_HOST_RESIDUAL_UNROLL, true>(f, lo, hi, lane,
+                                                                                                       qstage_j)
                                     : warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(f, lo, hi, lane);
                 if (lane == 0)
                     srm[c] = z;
