@@ -2287,6 +2287,7 @@ struct CutSmem {
     float tp;
     uint32_t thr;                       // cut key of the latest row (0 = none)
     int abort;                          // a copy of a pass did not land in time
+    int narrow_miss;                    // the block's latest cut lay below the narrow window
     uint64_t bar[kLWarps][2];           // per warp: one mbarrier per half of its ring slot
     uint32_t ph[kLWarps];               // per warp: the parity each of the two is waiting for
 };
@@ -2592,7 +2593,9 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     // ---- 1a. with at most kCutNarrowChunks chunks, first the kCutNarrow largest keys counted per
     // chunk: a cut inside them gets its partials from the counts, with no second pass (and
     // nearly every token lands in its lane's sink, which costs the least)
-    if (P.nchunks <= kCutNarrowChunks) {
+    // (Skipped while the block's latest cut lay deeper: rows of a batch tend to cut alike, and
+    // either path gives the same key and partials.)
+    if (P.nchunks <= kCutNarrowChunks && !C.narrow_miss) {
         count_pass(kCutNarrow, true);
         totals(kCutNarrow, [&](int o) {
             unsigned t = 0;
@@ -2623,6 +2626,8 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         }
         for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
             (&C.hw[0][0])[i] = 0u;  // sinks of the narrow window sit inside the wide one
+        if (threadIdx.x == 0)
+            C.narrow_miss = 1;
         __syncthreads();
     }
 
@@ -2637,6 +2642,8 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     select_window(kB);
     __syncthreads();
     const int pcut = C.pos;
+    if (threadIdx.x == 0 && pcut >= 0 && pcut < kCutNarrow)
+        C.narrow_miss = 0;  // this cut would have fit the narrow window: try it again next time
     if (pcut >= 0) {
         // ---- 3. chunk partials over the survivors: masses relative to the row maximum, rescaled
         const uint32_t thr = kmax - (uint32_t)pcut;
@@ -2805,8 +2812,10 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             mbar_init(&C.bar[0][0] + threadIdx.x, 1);
         if (threadIdx.x < kLWarps)
             C.ph[threadIdx.x] = 0;
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0) {
             C.abort = 0;
+            C.narrow_miss = 0;
+        }
     }
     mbar_fence_init();
     if (threadIdx.x == 0)
