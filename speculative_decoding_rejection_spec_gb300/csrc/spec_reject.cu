@@ -544,6 +544,11 @@ struct RowInfo {
     float cs = 0.f;
 };
 
+// force_argmax: 0 = by temperature, 1 = argmax on every row, kArgmaxKeepErrors = argmax on
+// every row of a call whose error word already holds its results (no layout check, which would
+// reset the word).
+constexpr int kArgmaxKeepErrors = 2;
+
 __device__ __forceinline__ void row_info(const Params &P, int64_t t, int force_argmax, RowInfo &ri)
 {
     ri.t = t;
@@ -555,7 +560,7 @@ __device__ __forceinline__ void row_info(const Params &P, int64_t t, int force_a
 template <int DT>
 __global__ void __launch_bounds__(kThreads, SPEC_LDG_MIN_BLOCKS) rowstats_kernel(Params P, int force_argmax)
 {
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 && force_argmax != kArgmaxKeepErrors)
         validate_layout(P);
     if (P.B == 0)
         return;
@@ -693,7 +698,33 @@ __device__ __forceinline__ void argmax_regs(float2 *out, int lane, const uint4 (
         m = fmaxf(m, vec_max<DT>(v[k]));  // vectors past the unit hold -inf
     const float mw = warp_max(m);
     int idx = INT_MAX;
-    if (mw > -INFINITY) {
+    if (DT == 1 && mw > -INFINITY && mw != 0.f) {
+        // bf16: a token equals the maximum iff its bits do (not for +-0, handled below).  Per
+        // word, the halves where bits ^ max is zero: (d - 0x00010001) & ~d & 0x80008000 marks the
+        // lower zero half exactly and can only mark the upper one falsely when the lower is zero,
+        // so the first marked half of the first marked word is the vector's first maximum.
+        const uint32_t mb = __float_as_uint(mw) >> 16;
+        const uint32_t m2 = mb | (mb << 16);
+        auto zero_halves = [&](uint32_t x) {
+            const uint32_t d = x ^ m2;
+            return (d - 0x00010001u) & ~d & 0x80008000u;
+        };
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k) {
+            const uint32_t h[4] = {zero_halves(v[k].x), zero_halves(v[k].y), zero_halves(v[k].z), zero_halves(v[k].w)};
+            if (h[0] | h[1] | h[2] | h[3]) {
+                const int v0 = (int)(R.vlo + ((int64_t)k * 32 + lane) * VEC);
+                int e = 0;
+#pragma unroll
+                for (int q = 3; q >= 0; --q)
+                    if (h[q])
+                        e = 2 * q + ((h[q] & 0x8000u) ? 0 : 1);
+                idx = min(idx, v0 + e);
+            }
+        }
+        if (xt == mw)
+            idx = min(idx, (int)(R.vhi + lane));
+    } else if (mw > -INFINITY) {
 #pragma unroll
         for (int k = 0; k < kVecPerLane; ++k) {
             float x[VEC];
@@ -745,7 +776,7 @@ __global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_ke
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kWrWarps * kWrStages];
 
-    if (blockIdx.x == 0)
+    if (blockIdx.x == 0 && force_argmax != kArgmaxKeepErrors)
         validate_layout(P);
     if (P.B == 0)
         return;
@@ -3701,7 +3732,7 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     }
     if (debug && T > 0 && B > 0 && (dbg_am || dbg_m || dbg_s || dbg_pd)) {
         // argmax of every row (the sampling path does not need it), then per-row combine
-        launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 1);
+        launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, kArgmaxKeepErrors);
         const int g = (int)((T + kWarps - 1) / kWarps);
         debug_argmax_kernel<<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s, dbg_am);
     }

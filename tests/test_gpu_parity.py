@@ -283,6 +283,9 @@ def test_first_rejection_pass_device_errors_per_request(draft):
         assert (tok[cu[r] + r:cu[r + 1] + r + 1] == -1).all()
     full = PT.run_gpu(w, debug=True)
     assert np.array_equal(tok, full["tokens"]) and np.array_equal(acc, full["acc"])
+    # the diagnostic entry's error word holds the same per-request errors (its extra argmax
+    # pass over every row does not reset it)
+    assert full["status"] == 5 and full["bits"] == bits and full["first"] == 5
     ref = oracle.reject_sample_workload(w)
     assert (ref.num_accepted[[5, 40]] == -1).all()
 

@@ -176,3 +176,23 @@ def test_first_rejection_pass_with_filters_on_negative_rows():
         assert lazy["status"] == 0
         assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
         PT.assert_parity(w, lazy)
+
+
+def test_first_rejection_pass_with_filters_device_errors_per_request():
+    """k > 32 and an out-of-range draft id on a batch that takes the cut mode invalidate only their
+    request (the same error word as the full pass); the rest match the full pass bit for bit."""
+    B = 72
+    ks = [3] * B
+    ks[7] = 33
+    w = W.generate(dict(B=B, K=ks, V=4096, dtype="bf16", sigma=2.0, temperature=0.9, draft="noisy_q", q_sigma=0.5,
+                        top_k=20, top_p=0.8, seed=131), name="bad-cut")
+    cu = w["cu_num_draft"]
+    w["draft_ids"][cu[50] + 1] = w["V"] + 2
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    for g in (lazy, full):
+        assert g["status"] == 5 and g["bits"] == (binding.DEVERR_SPEC_LEN | binding.DEVERR_DRAFT_ID)
+        assert g["first"] == 7 and g["acc"][7] == -1 and g["acc"][50] == -1
+    for r in (7, 50):
+        assert (lazy["tokens"][cu[r] + r:cu[r + 1] + r + 1] == -1).all()
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
