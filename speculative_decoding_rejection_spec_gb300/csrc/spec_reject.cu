@@ -1708,6 +1708,11 @@ __device__ __forceinline__ int warp_combine_argmax(const float2 *pp, int nchunks
 // ---------------------------------------------------------------------------------------
 
 // Mass of the target distribution in units of 2^M: w(v) = 2^(l_v c - M), x* optionally left out.
+#ifndef SPEC_RANGE_UNROLL
+#define SPEC_RANGE_UNROLL 8  // 16-byte groups in flight per lane in a segment sum of the draw's search
+#endif
+constexpr int kRangeUnroll = SPEC_RANGE_UNROLL;
+
 template <int DT, bool F> struct TargetMass {
     const char *row;
     float cs, M;
@@ -1726,7 +1731,7 @@ template <int DT, bool F> struct TargetMass {
         int64_t v = v0;
         const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0);
         if (aligned) {
-#pragma unroll 8
+#pragma unroll(kRangeUnroll)
             for (; v + VEC <= v1; v += VEC) {
                 float x[VEC];
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
@@ -1764,7 +1769,7 @@ template <int DT, bool F> struct ResidualMass {
         const bool aligned = ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize) & 15) == 0) &&
                              ((reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0);
         if (aligned) {
-#pragma unroll 8
+#pragma unroll(kRangeUnroll)
             for (; v + VEC <= v1; v += VEC) {
                 float x[VEC];
                 unpack<DT>(__ldg(reinterpret_cast<const uint4 *>(row + v * Elem<DT>::kSize)), x);
