@@ -64,8 +64,8 @@ def source_sha(full=False):
 
 
 def traffic_for(workload):
-    """DRAM bytes per launch of the row-statistics kernel from the committed ncu summary,
-    only if it was taken on the current kernel source."""
+    """DRAM bytes per launch of the row-statistics kernel on this workload from the committed
+    ncu summary, only if it was taken on the current kernel source."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
@@ -73,8 +73,7 @@ def traffic_for(workload):
     e = d.get("rowstats", {})
     if e.get("source_sha") != source_sha():
         return None
-    per_unit = e.get("dram_bytes_per_row")
-    return None if per_unit is None else per_unit
+    return e.get("dram_bytes_per_launch", {}).get(workload)
 
 
 def traffic_lazy_for(workload):
@@ -450,8 +449,7 @@ def main():
         dom = 0
         dom_bytes = w["T"] * w["V"] * es + 4 * (w["T"] - w["B"])
         dom_name = "row statistics (K1: rowstats_wr_kernel, warp-private TMA pipelines)"
-        tr = traffic_for(args.workload)
-        traffic = None if tr is None else int(tr * w["T"])
+        traffic = traffic_for(args.workload + (f"+k{args.top_k}+p{args.top_p}" if filtered else ""))
         call_bytes = all_rows_bytes
     else:
         # KL reads each request's target rows up to its output row (the first rejection, or the
