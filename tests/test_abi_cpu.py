@@ -83,3 +83,32 @@ def test_host_entry_checks(lib):
                                      None)
     assert st == 1
     assert lib.spec_reject_last_device_error(None, None, None, None) == 1
+
+
+def test_kernel_counts_per_call_kind(lib):
+    """Which pass a call takes, from the host logic alone: 64 or more requests take the
+    first-rejection pass (2 launches), with top-k / top-p only on bf16 rows; otherwise the full
+    pass (K1, K2, plus the cut with filters, plus the residual pass with draft probabilities)."""
+    for dt in (binding.F32, binding.BF16):
+        for q in (False, True):
+            assert binding.num_kernels(64, q, False, dt) == 2
+            assert binding.num_kernels(63, q, False, dt) == 2 + q
+            assert binding.num_kernels(0, q, True, dt) == 3 + q
+        assert binding.reads_to_first_rejection(1024, False, dt)
+        assert not binding.reads_to_first_rejection(63, False, dt)
+    assert binding.num_kernels(64, True, True, binding.BF16) == 2
+    assert binding.num_kernels(64, True, True, binding.F32) == 4
+    assert binding.reads_to_first_rejection(64, True, binding.BF16)
+    assert not binding.reads_to_first_rejection(64, True, binding.F32)
+
+
+def test_host_arena_size(lib):
+    """The host-buffer entry's arena holds a logits region, a q region, the small arrays and the
+    sampler's workspace; it grows with each of them and rejects bad sizes."""
+    a = binding.host_arena_size(1024, 9216, 128256, binding.BF16, True)
+    b = binding.host_arena_size(1024, 9216, 128256, binding.BF16, False)
+    c = binding.host_arena_size(1024, 9216, 128256, binding.F32, True)
+    assert a > 2 * 9216 * 128256 + 4 * 8192 * 128256
+    assert b < a < c
+    assert b >= 2 * 9216 * 128256 + binding.workspace_size(1024, 9216, 128256, binding.BF16, False)
+    assert lib.spec_reject_host_arena_size(-1, 4, 10, 0, 0) == 0
