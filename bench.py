@@ -483,7 +483,7 @@ def main():
         line["rows_read_per_step"] = rows_read
         line["rows_total"] = int(w["T"])
 
-    if not args.no_e2e and not filtered:  # the host-buffer entry point takes no filters
+    if not args.no_e2e:
         line["e2e"] = e2e(w, dev, args)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w)
@@ -510,6 +510,10 @@ def e2e(w, dev, args):
             "temperature": pinned(w["temperature"])}
     if has_q:
         host["draft_probs"] = pinned(w["draft_probs"])
+    filtered = w.get("top_k") is not None or w.get("top_p") is not None
+    for k in ("top_k", "top_p"):  # cuts go through spec_reject_sample_host_ex
+        if w.get(k) is not None:
+            host[k] = pinned(w[k])
     host["out_tokens"] = torch.empty(w["T"], dtype=torch.int32).pin_memory()
     host["out_num_accepted"] = torch.empty(w["B"], dtype=torch.int32).pin_memory()
     ptrs = {k: v.data_ptr() for k, v in host.items()}
@@ -533,7 +537,7 @@ def e2e(w, dev, args):
     from speculative_decoding_rejection_spec_gb300 import binding as _b
     acc = host["out_num_accepted"].numpy()
     ks = np.diff(w["cu_num_draft"])
-    logits_in_place = _b.reads_to_first_rejection(w["B"])
+    logits_in_place = _b.reads_to_first_rejection(w["B"], filtered, dt)
     h2d = sum(v.numel() * v.element_size() for k, v in host.items()
               if not k.startswith("out_") and k != "draft_probs" and not (k == "logits" and logits_in_place))
     es = 2 if w["dtype"] == "bf16" else 4

@@ -159,7 +159,9 @@ spec_status spec_reject_last_device_error(const void *workspace, void *stream, i
  * rejection); pageable draft_probs is copied whole.  When the target logits are pinned
  * too (and draft_probs, if given), the batch has at least 64 requests and rows are
  * 16-byte aligned, nothing large is copied: the target rows are read in place as well,
- * only those up to each request's output row.  Rows are passed with the same strides as the
+ * only those up to each request's output row (the pass keeps device copies of those rows, and
+ * of the draft row of each explicit-q rejection, in the arena's logits and draft-probability
+ * regions for its residual pass and draw).  Rows are passed with the same strides as the
  * device form (0 = aliasing is not allowed here: strides must be >= V).
  * `device_arena` must hold spec_reject_host_arena_size() bytes.
  */
@@ -169,6 +171,23 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
                                     int32_t B, const float *uniforms, const float *temperature, int32_t *out_tokens,
                                     int32_t *out_num_accepted, void *device_arena, size_t arena_bytes,
                                     void *stream);
+
+/*
+ * spec_reject_sample_host() with top-k / top-p on the target distribution (as
+ * spec_reject_sample_filtered(): "第12章 投机解码：以小博大" §12.2.3 and §12.9) and the acceptance
+ * counters (as spec_reject_sample_ex(), §12.7.5):
+ *   top_k, top_p  host int32 [B] / float [B], or NULL (copied into the arena)
+ *   counters      host int64 [SPEC_METRIC_COUNT], or NULL: this call's counters are added to
+ *                 it (copied to the arena, updated there, copied back)
+ * Pinned bf16 logits of 64 or more requests with cuts are still read in place (each reached row
+ * is cut from its device copy); fp32 logits with cuts are copied whole.  Same arena size.
+ */
+spec_status spec_reject_sample_host_ex(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       const float *draft_probs, const int32_t *draft_ids,
+                                       const int32_t *cu_num_draft, int32_t B, const float *uniforms,
+                                       const float *temperature, int32_t *out_tokens, int32_t *out_num_accepted,
+                                       void *device_arena, size_t arena_bytes, void *stream, const int32_t *top_k,
+                                       const float *top_p, int64_t *counters);
 
 /*
  * Diagnostic form: runs spec_reject_sample() and also writes, per target row,

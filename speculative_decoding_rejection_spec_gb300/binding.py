@@ -26,6 +26,7 @@ EXPORTED = [
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
     "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
     "spec_tree_workspace_size", "spec_tree_verify_greedy", "spec_reject_sample_filtered", "spec_reject_sample_ex",
+    "spec_reject_sample_host_ex",
 ]
 
 
@@ -69,6 +70,8 @@ def load():
     lib.spec_reject_host_arena_size.argtypes = [i32, i64, i32, ctypes.c_int, ctypes.c_int]
     lib.spec_reject_sample_host.restype = ctypes.c_int
     lib.spec_reject_sample_host.argtypes = [P, ctypes.c_int, i64, i32, P, P, P, i32, P, P, P, P, P, sz, P]
+    lib.spec_reject_sample_host_ex.restype = ctypes.c_int
+    lib.spec_reject_sample_host_ex.argtypes = [P, ctypes.c_int, i64, i32, P, P, P, i32, P, P, P, P, P, sz, P, P, P, P]
     lib.spec_reject_status_string.restype = ctypes.c_char_p
     lib.spec_reject_status_string.argtypes = [ctypes.c_int]
     lib.spec_reject_version.restype = ctypes.c_int
@@ -417,13 +420,21 @@ def sample_host(logits: np.ndarray, draft_ids: np.ndarray, cu_num_draft: np.ndar
 
 
 def sample_host_ptrs(ptrs: dict, T: int, V: int, B: int, dtype_code: int, arena, stream=None):
-    """Same as ``sample_host`` but with raw host addresses (e.g. of pinned torch tensors)."""
-    st = load().spec_reject_sample_host(ptrs["logits"], dtype_code, T, V, ptrs.get("draft_probs"), ptrs["draft_ids"],
-                                        ptrs["cu_num_draft"], B, ptrs["uniforms"], ptrs["temperature"],
-                                        ptrs["out_tokens"], ptrs["out_num_accepted"], _ptr(arena),
-                                        int(arena.numel()), _stream(stream))
+    """Same as ``sample_host`` but with raw host addresses (e.g. of pinned torch tensors).
+
+    Optional ``ptrs`` keys ``top_k`` (int32 [B]), ``top_p`` (float32 [B]) and ``counters``
+    (int64 [METRIC_COUNT], added to) take ``spec_reject_sample_host_ex``."""
+    base = (ptrs["logits"], dtype_code, T, V, ptrs.get("draft_probs"), ptrs["draft_ids"], ptrs["cu_num_draft"], B,
+            ptrs["uniforms"], ptrs["temperature"], ptrs["out_tokens"], ptrs["out_num_accepted"], _ptr(arena),
+            int(arena.numel()), _stream(stream))
+    if any(ptrs.get(k) is not None for k in ("top_k", "top_p", "counters")):
+        st = load().spec_reject_sample_host_ex(*base, ptrs.get("top_k"), ptrs.get("top_p"), ptrs.get("counters"))
+        what = "spec_reject_sample_host_ex"
+    else:
+        st = load().spec_reject_sample_host(*base)
+        what = "spec_reject_sample_host"
     if st != 0:
-        raise SpecRejectError(st, "spec_reject_sample_host")
+        raise SpecRejectError(st, what)
 
 
 def to_device(w: dict, device="cuda"):

@@ -596,6 +596,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 
 __device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
+// Orders this thread's earlier generic-proxy writes to global memory before later bulk copies
+// (async proxy) that read them, once a barrier has passed.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
@@ -2820,12 +2824,13 @@ struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
 };
 
 // HOST: the target rows live in pinned host memory (read over the host link with 16-byte loads,
-// sixteen in flight per lane) instead of device memory (TMA bulk copies).  CUT (bf16 rows in
-// device memory): the call has top-k / top-p cuts, applied to each row as it is reached.
+// sixteen in flight per lane) instead of device memory (TMA bulk copies).  CUT (bf16 rows): the
+// call has top-k / top-p cuts, applied to each row as it is reached (rows in host memory are cut
+// from their device copies).
 template <int DT, bool HOST, bool CUT>
 __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Params P)
 {
-    static_assert(!CUT || (DT == 1 && !HOST), "cuts in KL: bf16 rows in device memory");
+    static_assert(!CUT || DT == 1, "cuts in KL: bf16 rows (from host memory: through their device copies)");
     constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char ring[];
     CutSmem &C = *reinterpret_cast<CutSmem *>(ring + kLSmem);  // CUT only: after the rings
@@ -2968,6 +2973,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     else
                         softmax_regs<DT>(&spart[c], cs, lane, v, R, row);
                 }
+                if (CUT && P.lstage)  // the cut reads the device copy through the bulk-copy engine
+                    fence_proxy_async_global();
             } else
             for (int c = warp; c < P.nchunks; c += kLWarps) {
                 const int s = (int)(qc % kLStages);
@@ -3006,7 +3013,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 break;
             if constexpr (CUT)
                 if (!greedy) {  // uniform: the row's cut key, and its partials over the survivors
-                    kl_cut_row<DT>(CutDims{P.V, P.chunk, P.nchunks, P.err, slots}, C, spart, row, cs);
+                    kl_cut_row<DT>(CutDims{P.V, P.chunk, P.nchunks, P.err, slots}, C, spart,
+                                   HOST ? P.lstage + (size_t)(tb + i) * P.lstride * ES : row, cs);
                     if (C.abort)
                         break;  // uniform (read after the cut's last barrier)
                 }
@@ -3443,7 +3451,8 @@ struct DeviceInfo {
     int blocks_residual[2] = {0, 0};
     int blocks_wr[2] = {0, 0};
     int blocks_lazy[2] = {0, 0};
-    int blocks_lazy_cut = 0;  // KL with cuts (bf16)
+    int blocks_lazy_cut = 0;       // KL with cuts (bf16)
+    int blocks_lazy_cut_host = 0;  // the same, rows in host memory
 };
 
 constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
@@ -3479,6 +3488,12 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
                                       (int)kLCutSmem)))
             return e;
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy_cut, lazy_kernel<1, false, true>,
+                                                               kLThreads, kLCutSmem)))
+            return e;
+        if ((e = cudaFuncSetAttribute(lazy_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kLCutSmem)))
+            return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy_cut_host, lazy_kernel<1, true, true>,
                                                                kLThreads, kLCutSmem)))
             return e;
     }
@@ -3658,27 +3673,34 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             cudaEventRecord(ev[evi], stream);
         ++evi;
     };
-    // calls without diagnostics (and with cuts only on bf16 rows in device memory): KL reads rows
-    // only up to each request's first rejection
+    // calls without diagnostics (and with cuts only on bf16 rows, which in host memory need a
+    // device copy to cut from): KL reads rows only up to each request's first rejection
     const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
-    const bool cut_ok = !filtered || (DT == 1 && !rows_in_host && di->blocks_lazy_cut > 0);
+    const bool cut_ok = !filtered || (DT == 1 && (rows_in_host ? row_stage && di->blocks_lazy_cut_host > 0
+                                                               : di->blocks_lazy_cut > 0));
     if (cut_ok && !debug && (!q_stage || rows_in_host) && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
         di->blocks_lazy[DT] > 0) {
         mark();
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
         mark();
+        if (rows_in_host) {
+            // the rows it reads over the host link are copied to device memory for the cut, the
+            // residual pass and the draw (q_stage: rows of V floats, row_stage: rows of lstride)
+            P.lstage = row_stage;
+            P.qstage = q ? q_stage : nullptr;
+        }
         if (filtered) {
-            const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy_cut, B);
-            lazy_kernel<1, false, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
+            const int gridL =
+                (int)clamp_grid((int64_t)di->sms * (rows_in_host ? di->blocks_lazy_cut_host : di->blocks_lazy_cut), B);
+            if (rows_in_host)
+                lazy_kernel<1, true, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
+            else
+                lazy_kernel<1, false, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
             mark();
             return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
         }
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
         if (rows_in_host) {
-            // the rows it reads over the host link are copied to device memory for the
-            // residual pass and the draw (q_stage: rows of V floats, row_stage: rows of lstride)
-            P.lstage = row_stage;
-            P.qstage = q ? q_stage : nullptr;
             if (DT)
                 lazy_kernel<1, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
             else
@@ -3863,6 +3885,7 @@ size_t spec_reject_host_arena_size(int32_t B, int64_t T, int32_t V, spec_dtype l
     o = align256(o + 4 * (size_t)B);                                                    // temperature
     o = align256(o + 4 * (size_t)T);                                                    // out tokens
     o = align256(o + 4 * (size_t)B);                                                    // out accepted
+    o = align256(o + 8 * (size_t)B + 8 * (size_t)SPEC_METRIC_COUNT);                    // top-k, top-p, counters
     return o + pl.total + 256;
 }
 
@@ -3870,6 +3893,18 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
                                     const float *draft_probs, const int32_t *draft_ids, const int32_t *cu_num_draft,
                                     int32_t B, const float *uniforms, const float *temperature, int32_t *out_tokens,
                                     int32_t *out_num_accepted, void *device_arena, size_t arena_bytes, void *stream)
+{
+    return spec_reject_sample_host_ex(target_logits, logits_dtype, T, V, draft_probs, draft_ids, cu_num_draft, B,
+                                      uniforms, temperature, out_tokens, out_num_accepted, device_arena, arena_bytes,
+                                      stream, nullptr, nullptr, nullptr);
+}
+
+spec_status spec_reject_sample_host_ex(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
+                                       const float *draft_probs, const int32_t *draft_ids,
+                                       const int32_t *cu_num_draft, int32_t B, const float *uniforms,
+                                       const float *temperature, int32_t *out_tokens, int32_t *out_num_accepted,
+                                       void *device_arena, size_t arena_bytes, void *stream, const int32_t *top_k,
+                                       const float *top_p, int64_t *counters)
 {
     if (!device_arena || !cu_num_draft || B < 0 || T < B || V < 1 || (T > 0 && (!target_logits || !uniforms ||
         !out_tokens)) || (B > 0 && (!temperature || !out_num_accepted)) || (T > B && !draft_ids))
@@ -3899,6 +3934,10 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     o = align256(o + 4 * (size_t)T);
     int32_t *d_acc = reinterpret_cast<int32_t *>(a + o);
     o = align256(o + 4 * (size_t)B);
+    int32_t *d_topk = reinterpret_cast<int32_t *>(a + o);
+    float *d_topp = reinterpret_cast<float *>(a + o + 4 * (size_t)B);
+    int64_t *d_ctr = reinterpret_cast<int64_t *>(a + o + 8 * (size_t)B);  // 8-byte aligned
+    o = align256(o + 8 * (size_t)B + 8 * (size_t)SPEC_METRIC_COUNT);
     char *d_ws = a + o;
     const size_t ws_bytes = arena_bytes - (size_t)(d_ws - reinterpret_cast<char *>(device_arena));
 
@@ -3917,8 +3956,10 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     // Pinned logits too, and a batch that takes the first-rejection pass: that pass reads the
     // target rows in place as well, only the rows up to each request's output row.
     const void *logits_in_place = (T > 0) ? mapped(target_logits) : nullptr;
+    const bool filtered = top_k || top_p;
     const bool all_in_place = logits_in_place && (!has_q || q_in_place) && B >= SPEC_KL_MIN_REQUESTS &&
-                              aligned(logits_in_place, 16) && ((size_t)V * es) % 16 == 0;
+                              aligned(logits_in_place, 16) && ((size_t)V * es) % 16 == 0 &&
+                              (!filtered || logits_dtype == SPEC_BF16);
     // one cudaMemcpyAsync per buffer
     const struct {
         void *dst;
@@ -3931,6 +3972,9 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
         {d_cu, cu_num_draft, 4 * (size_t)(B + 1)},
         {d_uni, uniforms, 8 * (size_t)T},
         {d_temp, temperature, 4 * (size_t)B},
+        {d_topk, top_k, top_k ? 4 * (size_t)B : 0},
+        {d_topp, top_p, top_p ? 4 * (size_t)B : 0},
+        {d_ctr, counters, counters ? 8 * (size_t)SPEC_METRIC_COUNT : 0},
     };
     for (const auto &c : in)
         if (c.bytes && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -3940,15 +3984,18 @@ spec_status spec_reject_sample_host(const void *target_logits, spec_dtype logits
     spec_status st =
         all_in_place
             ? run(logits_in_place, logits_dtype, T, V, V, q_in_place, V, d_ids, d_cu, B, d_uni, d_temp, d_tok, d_acc,
-                  d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr,
-                  nullptr, has_q ? d_q : nullptr, true, d_logits)
+                  d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, top_k ? d_topk : nullptr,
+                  top_p ? d_topp : nullptr, counters ? d_ctr : nullptr, has_q ? d_q : nullptr, true, d_logits)
             : run(d_logits, logits_dtype, T, V, V, has_q ? (q_in_place ? q_in_place : d_q) : nullptr, V, d_ids, d_cu,
                   B, d_uni, d_temp, d_tok, d_acc, d_ws, ws_bytes, s, nullptr, nullptr, nullptr, nullptr, nullptr,
-                  nullptr, 0, nullptr, nullptr, nullptr, q_in_place ? d_q : nullptr);
+                  nullptr, 0, top_k ? d_topk : nullptr, top_p ? d_topp : nullptr, counters ? d_ctr : nullptr,
+                  q_in_place ? d_q : nullptr);
     if (st != SPEC_OK)
         return st;
     if ((T && cudaMemcpyAsync(out_tokens, d_tok, 4 * (size_t)T, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
         (B && cudaMemcpyAsync(out_num_accepted, d_acc, 4 * (size_t)B, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
+        (counters && cudaMemcpyAsync(counters, d_ctr, 8 * (size_t)SPEC_METRIC_COUNT, cudaMemcpyDeviceToHost, s) !=
+                         cudaSuccess) ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return SPEC_OK;

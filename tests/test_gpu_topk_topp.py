@@ -196,3 +196,48 @@ def test_first_rejection_pass_with_filters_device_errors_per_request():
     for r in (7, 50):
         assert (lazy["tokens"][cu[r] + r:cu[r + 1] + r + 1] == -1).all()
     assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+
+
+# ---------------------------------------------------------------------------- host-buffer entry with cuts
+
+@pytest.mark.parametrize("name,tk,tp,pinned", [
+    ("large-128", 50, 0.9, True),         # bf16, 128 requests: rows read in place, each reached row cut
+    ("large-128", 0, 0.95, False),        # pageable: copied, then the cut mode on the device copy
+    ("deterministic", 100, 0.99, True),   # one-hot drafts
+    ("probabilistic", 1000, 0.8, True),   # fp32 with cuts: logits copied, full pass with the cut kernel
+])
+def test_host_entry_with_filters_and_counters(name, tk, tp, pinned):
+    """spec_reject_sample_host_ex: the device filtered entry's tokens and counts bit for bit, the
+    acceptance counters added onto the caller's host array, and (pinned bf16, >= 64 requests)
+    only the rows up to each output row copied to the arena."""
+    import torch
+    from oracle import closed_forms as cf
+    w = W.generate(name, top_k=tk, top_p=tp)
+    dev = PT.run_gpu(w)
+    has_q = w["draft_probs"] is not None
+
+    def host(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory() if pinned else t.clone()
+
+    keys = ["logits", "draft_ids", "cu_num_draft", "uniforms", "temperature", "top_k", "top_p"]
+    keys += ["draft_probs"] if has_q else []
+    h = {k: host(w[k]) for k in keys}
+    h["out_tokens"] = torch.full((w["T"],), -7, dtype=torch.int32)
+    h["out_num_accepted"] = torch.full((w["B"],), -7, dtype=torch.int32)
+    h["counters"] = torch.full((binding.METRIC_COUNT,), 3, dtype=torch.int64)
+    ptrs = {k: v.data_ptr() for k, v in h.items()}
+    dt = PT.dtype_code(w)
+    arena = torch.full((binding.host_arena_size(w["B"], w["T"], w["V"], dt, has_q),), 0xA5, dtype=torch.uint8,
+                       device="cuda")
+    binding.sample_host_ptrs(ptrs, w["T"], w["V"], w["B"], dt, arena)
+    tok, acc = h["out_tokens"].numpy(), h["out_num_accepted"].numpy()
+    assert np.array_equal(tok, dev["tokens"]) and np.array_equal(acc, dev["acc"])
+    assert h["counters"].tolist() == [x + 3 for x in cf.acceptance_counters(w["cu_num_draft"], acc)]
+    if pinned and w["dtype"] == "bf16" and w["B"] >= 64:
+        es, T, B, V = 2, w["T"], w["B"], w["V"]
+        base = (-arena.data_ptr()) % 256
+        rows = arena[base:base + es * T * V].view(T, es * V)
+        got = set(torch.nonzero((rows != 0xA5).any(dim=1)).flatten().cpu().numpy().tolist())
+        cu = w["cu_num_draft"]
+        assert got == {int(cu[r]) + r + i for r in range(B) for i in range(int(acc[r]) + 1)}
