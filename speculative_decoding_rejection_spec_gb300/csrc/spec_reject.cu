@@ -2288,17 +2288,18 @@ constexpr size_t kLSmem = (size_t)kLWarps * kLStages * kUnitBytes;
 // ---- KL with top-k / top-p (bf16 rows): the cut of one row, by the whole block
 //
 // The same cut as K1F, from the row KL has just streamed (its unfiltered chunk partials are in
-// shared memory; the row is read again, mostly from L2):
-//   1. counts by order-key offset below the maximum's key, over the kFKeys largest keys (one
-//      histogram per warp, a sink per lane for the rest), and one token's fixed-point mass per
-//      offset;
-//   2. warp 0 finds the k-th largest key, S_k and the top-p key from the totals (integer
-//      sums), as K1F's one-pass path;
-//   3. one more pass gives each chunk's partial over the survivors: per element the mass of its
-//      key offset, summed as integers, which is K1F's count x mass sum.
-// A cut outside the window is found by a radix select on the 16-bit order key (two passes of
-// digit histograms per selection) with the partials of K1F's general path.  Either way the cut
-// key and the partials are K1F's, bit for bit.
+// shared memory; the row is read again through the warp's ring slot, mostly from L2):
+//   1. with at most kCutNarrowChunks chunks, the tokens of the kCutNarrow largest keys counted by
+//      order-key offset below the maximum's key, per chunk (only vectors holding such a token
+//      are unpacked); warp 0 finds the k-th largest key, S_k and the top-p key from the totals
+//      (integer sums of count x fixed-point mass, K1F's one-pass rules), and a cut inside this
+//      window takes K1F's one-pass partials from the per-chunk counts;
+//   2. otherwise the same over the kFKeys largest keys (one histogram per warp, a sink per lane
+//      for the rest), and one more pass gives each chunk's partial over the survivors: per
+//      element the mass of its key offset, summed as integers, which is K1F's count x mass sum;
+//   3. a cut below that window is found by a radix select on the 16-bit order key (two passes
+//      of digit histograms per selection), with the partials of K1F's general path.
+// Whichever step finds it, the cut key and the partials are K1F's, bit for bit.
 
 constexpr int kCutHalfBytes = kUnitBytes / 2;  // a pass moves each chunk in two copies of this size
 static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot as two halves");
