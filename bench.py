@@ -53,14 +53,20 @@ def peaks():
 
 
 def source_sha(full=False):
-    """Hash of the kernel source: by default up to the end of the row-statistics kernel (K1 and
+    """Hash of the kernel code: by default up to the end of the row-statistics kernel (K1 and
     everything it can use are defined before that point; later code cannot change it), with
-    full=True the whole file."""
+    full=True the whole file.  Comments and blank space are left out (they compile to nothing),
+    so a recorded traffic figure stays valid until the code itself changes."""
+    import re
     with open(KERNEL_SOURCE, "rb") as f:
         src = f.read()
     marker = b"// K1F: top-k / top-p cut"
     cut = -1 if full else src.find(marker)
-    return hashlib.sha256(src if cut < 0 else src[:cut]).hexdigest()[:16]
+    code = (src if cut < 0 else src[:cut]).decode()
+    code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+    code = re.sub(r"//[^\n]*", " ", code)
+    code = " ".join(code.split())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def traffic_for(workload):
