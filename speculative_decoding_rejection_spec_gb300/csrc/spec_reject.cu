@@ -2305,11 +2305,13 @@ constexpr int kCutHalfBytes = kUnitBytes / 2;  // a pass moves each chunk in two
 static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot as two halves");
 
 constexpr int kCutNarrow = 128;       // largest keys counted per chunk first (one binade of bf16)
-constexpr int kCutNarrowChunks = 32;  // chunks (4096 tokens) a row may have for the per-chunk counts
+constexpr int kCutNarrowChunks = 64;  // chunks (4096 tokens) a row may have for the per-chunk counts
 
 struct CutSmem {
     unsigned hw[kLWarps][kFKeys + 32];                // per warp: tokens per key offset, then a sink per lane
-    unsigned short hcc[kCutNarrowChunks][kCutNarrow]; // per chunk: tokens of the kCutNarrow largest keys
+    unsigned char hcc[kCutNarrowChunks][kCutNarrow];  // per chunk: tokens of the kCutNarrow largest keys
+                                                      // (8 bits; hcc_over when a count did not fit)
+    int hcc_over;
     unsigned bh[kFKeys];                // block totals per key offset
     unsigned long long km[kFKeys];      // fixed-point mass of one token per key offset
     unsigned long long bm[kFKeys];      // block masses per key offset (tokens x km)
@@ -2422,6 +2424,8 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         C.cmx[c] = spart[c].x;
     for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
         (&C.hw[0][0])[i] = 0u;
+    if (threadIdx.x == 0)
+        C.hcc_over = 0;
     __syncthreads();
     const float m = C.m;
     if (!(m > -INFINITY))
@@ -2588,7 +2592,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
 
     // counts by key offset over the w largest keys, one histogram per warp with a sink per lane
     // for the rest (no branch); with `flush`, the counts of each chunk move to C.hcc[c] after
-    // the chunk (at most 4096 tokens: 16 bits)
+    // the chunk (8 bits each; a larger count sets C.hcc_over)
     // A narrow window (w <= kCutNarrow) of a row whose maximum is at least 512 keys above +0
     // counts only the tokens inside it: an integer test on both halves of each word (bits &
     // 0x7fff plus 0x8000 - lowest carries into bit 15 exactly when the bits are at least the
@@ -2622,7 +2626,10 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             if (flush) {
                 __syncwarp();  // every lane's counts of the chunk are in
                 for (int o = lane; o < w; o += 32) {
-                    C.hcc[c][o] = (unsigned short)h[o];
+                    const unsigned n = h[o];
+                    C.hcc[c][o] = (unsigned char)min(n, 255u);
+                    if (n > 255u)
+                        C.hcc_over = 1;
                     h[o] = 0u;
                 }
                 __syncwarp();
@@ -2632,21 +2639,24 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     };
 
     // ---- 1a. with at most kCutNarrowChunks chunks, first the kCutNarrow largest keys counted per
-    // chunk: a cut inside them gets its partials from the counts, with no second pass (and
-    // nearly every token lands in its lane's sink, which costs the least)
-    // (Skipped while the block's latest cut lay deeper: rows of a batch tend to cut alike, and
-    // either path gives the same key and partials.)
+    // chunk: a cut inside them gets its partials from the counts, with no second pass.  (Skipped
+    // while the block's latest cut lay deeper: rows of a batch tend to cut alike, and either
+    // path gives the same key and partials.  A chunk with more than 255 tokens on one key of
+    // the window takes the wide path too.)
     if (P.nchunks <= kCutNarrowChunks && !C.narrow_miss) {
         count_pass(kCutNarrow, true);
-        totals(kCutNarrow, [&](int o) {
-            unsigned t = 0;
-            for (int c = 0; c < P.nchunks; ++c)
-                t += C.hcc[c][o];
-            return t;
-        });
-        select_window(kCutNarrow);
-        __syncthreads();
-        const int pn = C.pos;
+        int pn = -1;
+        if (!C.hcc_over) {  // uniform: read after the pass's last barrier
+            totals(kCutNarrow, [&](int o) {
+                unsigned t = 0;
+                for (int c = 0; c < P.nchunks; ++c)
+                    t += C.hcc[c][o];
+                return t;
+            });
+            select_window(kCutNarrow);
+            __syncthreads();
+            pn = C.pos;
+        }
         if (pn >= 0) {  // K1F's one-pass partials
             const uint32_t thr = kmax - (uint32_t)pn;
             for (int c = warp; c < P.nchunks; c += nw) {

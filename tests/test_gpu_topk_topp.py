@@ -241,3 +241,20 @@ def test_host_entry_with_filters_and_counters(name, tk, tp, pinned):
         got = set(torch.nonzero((rows != 0xA5).any(dim=1)).flatten().cpu().numpy().tolist())
         cu = w["cu_num_draft"]
         assert got == {int(cu[r]) + r + i for r in range(B) for i in range(int(acc[r]) + 1)}
+
+
+def test_first_rejection_pass_with_filters_many_tied_maxima():
+    """300 tokens of the first chunk tied with each row's maximum: more than an 8-bit per-chunk
+    count holds, so the cut takes the 512-key path; top-k keeps every tied token (ties kept), and
+    the result is the full pass's and the oracle's."""
+    w = W.generate(dict(B=64, K=3, V=8192, dtype="bf16", sigma=2.0, boost=4.0, temperature=0.8, draft="noisy_q",
+                        q_sigma=0.5, top_k=50, top_p=0.9, seed=141), name="tied-maxima")
+    bits = w["logits"]
+    for t in range(w["T"]):
+        bits[t, :300] = bits[t].view(np.int16).max()  # positive maxima: the largest bits
+    assert (W.logits_as_f32(w)[:, :300] == W.logits_as_f32(w).max(axis=1, keepdims=True)).all()
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    assert lazy["status"] == 0
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
