@@ -46,6 +46,16 @@ def test_full_size_parity(name):
     PT.assert_parity(w, gpu, oracle.reject_sample_workload(w, debug=True))
 
 
+def test_full_size_parity_with_filters():
+    """The filtered benchmark's workload at full size (large-1024, top-k 50, top-p 0.9), in the
+    launch configuration it times: the cut mode of the first-rejection pass."""
+    w = W.generate("large-1024", top_k=50, top_p=0.9)
+    assert binding.reads_to_first_rejection(w["B"], True, binding.BF16)
+    gpu = PT.run_gpu(w)
+    assert gpu["status"] == 0
+    PT.assert_parity(w, gpu, oracle.reject_sample_workload(w, debug=True))
+
+
 @pytest.mark.parametrize("name", ["greedy", "probabilistic", "deterministic", "large-128"])
 def test_config_parity_unaligned_rows(name):
     """The same workloads with the logits one element off a 16-byte boundary, which sends the
