@@ -3248,27 +3248,46 @@ __global__ void __launch_bounds__(kThreads) stage_rows_kernel(Params P, float *s
 __global__ void __launch_bounds__(kThreads) metrics_kernel(const int32_t *cu, const int32_t *acc, int32_t B,
                                                            unsigned long long *counters)
 {
-    __shared__ unsigned long long s_cnt[SPEC_METRIC_COUNT];
+    // Lanes take one request each; every count is summed over the warp first (a ballot's
+    // population per accepted position, a warp reduction for the rest), then once per warp into
+    // 32-bit block totals, then once per block into the 64-bit counters: integer sums, so the
+    // order does not matter.
+    __shared__ unsigned s_cnt[SPEC_METRIC_COUNT];
+    const int lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < SPEC_METRIC_COUNT; i += blockDim.x)
-        s_cnt[i] = 0;
+        s_cnt[i] = 0u;
     __syncthreads();
-    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < B; r += gridDim.x * blockDim.x) {
-        const int a = acc[r];
-        if (a < 0)
-            continue;
-        const int k = cu[r + 1] - cu[r];
-        if (k > 0)
-            atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFTS], 1ull);
-        atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFT_TOKENS], (unsigned long long)k);
-        atomicAdd(&s_cnt[SPEC_METRIC_NUM_ACCEPTED_TOKENS], (unsigned long long)a);
-        atomicAdd(&s_cnt[SPEC_METRIC_NUM_VERIFIES], 1ull);
-        for (int i = 0; i < a && i < SPEC_REJECT_MAX_SPEC_LEN; ++i)
-            atomicAdd(&s_cnt[SPEC_METRIC_ACCEPTED_PER_POS + i], 1ull);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); r0 < B; r0 += stride) {
+        const int64_t r = r0 + lane;  // warp-uniform loop: every lane takes part in the reductions
+        const int a = r < B ? acc[r] : -1;
+        const bool valid = a >= 0;
+        const int k = valid ? cu[r + 1] - cu[r] : 0;
+        const unsigned drafts = __popc(__ballot_sync(kFull, valid && k > 0));
+        const unsigned verifies = __popc(__ballot_sync(kFull, valid));
+        const unsigned tokens = __reduce_add_sync(kFull, (unsigned)(valid ? k : 0));
+        const unsigned accepted = __reduce_add_sync(kFull, (unsigned)(valid ? a : 0));
+        const int amax = __reduce_max_sync(kFull, (unsigned)(valid ? a : 0));
+        if (lane == 0) {
+            if (drafts)
+                atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFTS], drafts);
+            if (verifies)
+                atomicAdd(&s_cnt[SPEC_METRIC_NUM_VERIFIES], verifies);
+            if (tokens)
+                atomicAdd(&s_cnt[SPEC_METRIC_NUM_DRAFT_TOKENS], tokens);
+            if (accepted)
+                atomicAdd(&s_cnt[SPEC_METRIC_NUM_ACCEPTED_TOKENS], accepted);
+        }
+        for (int i = 0; i < amax && i < SPEC_REJECT_MAX_SPEC_LEN; ++i) {
+            const unsigned n = __popc(__ballot_sync(kFull, valid && a > i));
+            if (lane == 0 && n)
+                atomicAdd(&s_cnt[SPEC_METRIC_ACCEPTED_PER_POS + i], n);
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < SPEC_METRIC_COUNT; i += blockDim.x)
         if (s_cnt[i])
-            atomicAdd(counters + i, s_cnt[i]);
+            atomicAdd(counters + i, (unsigned long long)s_cnt[i]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -3340,16 +3359,22 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(Params P, const int
 // n-gram draft proposer ("第12章 投机解码：以小博大" §12.4.4)
 // ---------------------------------------------------------------------------------------
 
-// One block per request.  For n = max_n .. min_n, the block's threads test candidate
-// starts s in ascending blocks of blockDim.x positions (every s in [0, L - 2n], so the
-// occurrence lies wholly before the final n tokens); the first block of candidates with a
-// hit gives the leftmost occurrence.  The proposal is the (at most k) tokens after it.
+// One block per request, one pass over its context for every n at once: each thread takes
+// candidate starts s (sixteen at a time, their first tokens loaded together), and at each s
+// finds the largest n in [min_n, max_n] whose last n context tokens occur at s wholly before
+// the final n tokens (s <= L - 2n); a first-token test against the n suffixes, held in shared
+// memory, settles almost every s.  The block keeps the best (n, then the smallest s) as one
+// 64-bit key (n above, 2^40 - 1 - s below) reduced by a maximum; the proposal is the (at most
+// k) tokens after that occurrence.
+constexpr int kNgramPer = 16;  // candidate starts per thread per sweep
 __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int64_t *cu, int32_t B,
                                                          int min_n, int max_n, int k, int64_t max_model_len,
                                                          int32_t *out, int32_t *out_num)
 {
-    __shared__ int32_t pat[SPEC_NGRAM_MAX_N];
-    __shared__ int s_first;
+    constexpr unsigned long long kSMask = (1ull << 40) - 1;
+    __shared__ int32_t suf[SPEC_NGRAM_MAX_N];  // the last nmax tokens of the context
+    __shared__ unsigned long long s_best[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int r = blockIdx.x; r < B; r += gridDim.x) {
         const int64_t c0 = cu[r];
         const int64_t L = cu[r + 1] - c0;
@@ -3357,40 +3382,59 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, 
         int64_t kk = k;
         if (max_model_len > 0)
             kk = min(kk, max_model_len - L);
-        int64_t found = -1;
-        int found_n = 0;
-        for (int n = max_n; kk > 0 && n >= min_n && found < 0; --n) {
-            if (n <= 0 || 2 * (int64_t)n > L)
-                continue;
-            __syncthreads();  // pat of the previous n is no longer read
-            if (threadIdx.x < n)
-                pat[threadIdx.x] = ctx[L - n + threadIdx.x];
-            __syncthreads();
-            const int64_t last = L - 2 * (int64_t)n;
-            for (int64_t s0 = 0; s0 <= last; s0 += blockDim.x) {
-                const int64_t st = s0 + threadIdx.x;
-                bool hit = st <= last;
-                for (int i = 0; hit && i < n; ++i)
-                    hit = ctx[st + i] == pat[i];
-                if (__syncthreads_or(hit)) {  // uniform: every thread takes this branch
-                    if (threadIdx.x == 0)
-                        s_first = INT_MAX;
-                    __syncthreads();
-                    if (hit)
-                        atomicMin(&s_first, (int)threadIdx.x);
-                    __syncthreads();
-                    found = s0 + s_first;
-                    found_n = n;
-                    break;
+        const int nmax = (int)min((int64_t)max_n, L / 2);  // 2n <= L
+        const bool search = kk > 0 && nmax >= min_n;
+        __syncthreads();  // suf and s_best of the previous request are no longer read
+        if (search && (int)threadIdx.x < nmax)
+            suf[threadIdx.x] = ctx[L - nmax + threadIdx.x];
+        __syncthreads();
+        unsigned long long best = 0;
+        if (search) {
+            const int64_t last = L - 2 * (int64_t)min_n;  // the largest start for the shortest n
+            const int64_t step = (int64_t)blockDim.x * kNgramPer;
+            for (int64_t s0 = 0; s0 <= last; s0 += step) {
+                int32_t t0[kNgramPer];
+#pragma unroll
+                for (int u = 0; u < kNgramPer; ++u) {
+                    const int64_t st = s0 + (int64_t)u * blockDim.x + threadIdx.x;
+                    t0[u] = st <= last ? ctx[st] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kNgramPer; ++u) {
+                    const int64_t st = s0 + (int64_t)u * blockDim.x + threadIdx.x;
+                    if (st > last)
+                        continue;
+                    for (int n = (int)min((int64_t)nmax, (L - st) / 2); n >= min_n; --n) {
+                        const int32_t *pat = suf + (nmax - n);  // the last n tokens
+                        if (t0[u] != pat[0])
+                            continue;
+                        bool ok = true;
+                        for (int i = 1; ok && i < n; ++i)
+                            ok = ctx[st + i] == pat[i];
+                        if (ok) {
+                            best = max(best, ((unsigned long long)n << 40) | (kSMask - (unsigned long long)st));
+                            break;  // the largest n at this start
+                        }
+                    }
                 }
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            best = max(best, __shfl_xor_sync(kFull, best, o));
+        if (lane == 0)
+            s_best[warp] = best;
+        __syncthreads();
+        best = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+            best = max(best, s_best[w]);
+        const int found_n = (int)(best >> 40);
+        const int64_t found = best ? (int64_t)(kSMask - (best & kSMask)) : -1;
         const int cnt = found < 0 ? 0 : (int)min(kk, L - (found + found_n));
         for (int i = threadIdx.x; i < k; i += blockDim.x)
             out[(int64_t)r * k + i] = i < cnt ? ctx[found + found_n + i] : -1;
         if (threadIdx.x == 0)
             out_num[r] = cnt;
-        __syncthreads();  // s_first / pat are reused by this block's next request
     }
 }
 
