@@ -3360,14 +3360,20 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(Params P, const int
 // ---------------------------------------------------------------------------------------
 
 // One block per request, one pass over its context for every n at once: each thread takes
-// candidate starts s (sixteen at a time, their first tokens loaded together), and at each s
+// candidate starts s (SPEC_NGRAM_PER at a time, their first tokens loaded together), and at each s
 // finds the largest n in [min_n, max_n] whose last n context tokens occur at s wholly before
 // the final n tokens (s <= L - 2n); a first-token test against the n suffixes, held in shared
 // memory, settles almost every s.  The block keeps the best (n, then the smallest s) as one
 // 64-bit key (n above, 2^40 - 1 - s below) reduced by a maximum; the proposal is the (at most
 // k) tokens after that occurrence.
-constexpr int kNgramPer = 16;  // candidate starts per thread per sweep
-__global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int64_t *cu, int32_t B,
+#ifndef SPEC_NGRAM_PER
+#define SPEC_NGRAM_PER 4  // candidate starts per thread per sweep
+#endif
+#ifndef SPEC_NGRAM_MIN_BLOCKS
+#define SPEC_NGRAM_MIN_BLOCKS 8  // resident blocks per SM the registers must allow (one wave at B = 1024)
+#endif
+constexpr int kNgramPer = SPEC_NGRAM_PER;
+__global__ void __launch_bounds__(kThreads, SPEC_NGRAM_MIN_BLOCKS) ngram_kernel(const int32_t *tokens, const int64_t *cu, int32_t B,
                                                          int min_n, int max_n, int k, int64_t max_model_len,
                                                          int32_t *out, int32_t *out_num)
 {
