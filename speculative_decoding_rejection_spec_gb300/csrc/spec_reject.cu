@@ -2622,7 +2622,18 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                 fe((j & 1) ? word >> 16 : word & 0xffffu);
             }
         };
-        pass(all, nop, vec, fe, [&](int c) {
+        // a chunk whose maximum lies below the window holds no token of it: not read (its
+        // per-chunk counts are zeros)
+        auto reaches = [&](int c) {
+            const float mk = C.cmx[c];
+            return mk > -INFINITY && key_of<1>(mk) + (uint32_t)(w - 1) >= kmax;
+        };
+        if (flush)
+            for (int c = warp; c < P.nchunks; c += nw)
+                if (!reaches(c))
+                    for (int o = lane; o < w; o += 32)
+                        C.hcc[c][o] = 0;
+        pass(reaches, nop, vec, fe, [&](int c) {
             if (flush) {
                 __syncwarp();  // every lane's counts of the chunk are in
                 for (int o = lane; o < w; o += 32) {

@@ -258,3 +258,20 @@ def test_first_rejection_pass_with_filters_many_tied_maxima():
     assert lazy["status"] == 0
     assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
     PT.assert_parity(w, lazy)
+
+
+@pytest.mark.parametrize("tk,tp", [(20, 0.9), (0, 0.95), (3000, 1.0)])
+def test_first_rejection_pass_with_filters_low_chunks(tk, tp):
+    """Rows whose last six chunks lie far below the maximum (logits lowered by 20): the cut's count
+    passes skip chunks whose maximum is below their window; the result is the full pass's and
+    the oracle's."""
+    w = W.generate(dict(B=64, K=4, V=32768, dtype="bf16", sigma=2.0, temperature=0.9, draft="noisy_q",
+                        q_sigma=0.5, top_k=tk, top_p=tp, seed=151), name="low-chunks")
+    x = W.logits_as_f32(w).copy()
+    x[:, 2 * 4096:] -= np.float32(20.0)
+    w["logits"] = W.f32_to_bf16_bits(x)
+    lazy = PT.run_gpu(w)
+    full = PT.run_gpu(w, debug=True)
+    assert lazy["status"] == 0
+    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
