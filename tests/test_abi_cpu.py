@@ -112,3 +112,14 @@ def test_host_arena_size(lib):
     assert b < a < c
     assert b >= 2 * 9216 * 128256 + binding.workspace_size(1024, 9216, 128256, binding.BF16, False)
     assert lib.spec_reject_host_arena_size(-1, 4, 10, 0, 0) == 0
+
+
+def test_host_entry_with_options_checks(lib):
+    """spec_reject_sample_host_ex rejects what spec_reject_sample_host rejects, before any copy."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    args = [fake, 0, 8, 100, None, fake, fake, 2, fake, fake, fake, fake, fake]
+    assert lib.spec_reject_sample_host_ex(*args, 16, None, fake, fake, fake) == 3  # arena too small
+    bad = list(args)
+    bad[6] = None  # cu_num_draft
+    assert lib.spec_reject_sample_host_ex(*bad, 1 << 30, None, None, None, None) == 1
