@@ -123,9 +123,12 @@ spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtyp
  * and renormalised; that p' is used for the acceptance test, the recovered token and the
  * bonus token.  top_k[r] <= 0 or >= V, and top_p[r] >= 1 or <= 0, switch a filter off;
  * greedy requests ignore both.  top_k (int32 [B]) and top_p (fp32 [B]) are device arrays,
- * either may be NULL.  Filtered rows are cut by one thread-block cluster per row, at most
- * 8 blocks of at most 20 chunks of 8 KB, which limits V (V <= 655360 bf16 or 327680 fp32;
- * SPEC_ERR_UNSUPPORTED beyond).  row_sum and p_draft are
+ * either may be NULL.  bf16 calls of 64 or more requests on 16-byte-aligned rows (without
+ * diagnostics) cut each row the first-rejection pass reaches, in the block that reads it;
+ * otherwise every row is cut by one thread-block cluster, at most 8 blocks of at most 20
+ * chunks of 8 KB.  Both give the same cut and the same outputs.  The cluster limits V
+ * (V <= 655360 bf16 or 327680 fp32; SPEC_ERR_UNSUPPORTED beyond, for every call with
+ * filters).  row_sum and p_draft are
  * optional diagnostic outputs (device fp32 [T] and [T - B]): the restricted normaliser
  * sum over kept tokens of exp((l - m) / T_r) and p'(x*).  Same workspace as
  * spec_reject_sample().
