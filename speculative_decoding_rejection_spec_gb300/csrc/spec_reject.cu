@@ -2633,7 +2633,11 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                 if (!reaches(c))
                     for (int o = lane; o < w; o += 32)
                         C.hcc[c][o] = 0;
-        pass(reaches, nop, vec, fe, [&](int c) {
+        bool low = false;  // some chunk is skipped (else the pass takes every chunk without a test)
+        for (int c = threadIdx.x; c < P.nchunks; c += blockDim.x)
+            low = low || !reaches(c);
+        low = __syncthreads_or(low);
+        auto flush_chunk = [&](int c) {
             if (flush) {
                 __syncwarp();  // every lane's counts of the chunk are in
                 for (int o = lane; o < w; o += 32) {
@@ -2645,7 +2649,11 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                 }
                 __syncwarp();
             }
-        });
+        };
+        if (low)
+            pass(reaches, nop, vec, fe, flush_chunk);
+        else
+            pass(all, nop, vec, fe, flush_chunk);
         __syncthreads();
     };
 
