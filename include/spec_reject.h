@@ -26,8 +26,16 @@
  *
  * Conventions of every entry point:
  *   - Device pointers are device memory owned by the caller; host pointers are
- *     host memory owned by the caller.  The library allocates nothing and keeps
- *     no state between calls.
+ *     host memory owned by the caller.  The library allocates nothing.  The only
+ *     state it keeps between calls is, per device, a cache of launch shapes (SM
+ *     count and kernel occupancy, filled by the first call made with that device
+ *     current, safely when several host threads make it at once) and the address
+ *     of the fixed scratch array of spec_reject_sample_noalloc(); no result
+ *     depends on either.
+ *   - A CUDA error that earlier work left pending on the calling thread
+ *     (cudaPeekAtLastError() != cudaSuccess) is reported as SPEC_ERR_CUDA before
+ *     anything is launched and is left pending; SPEC_ERR_CUDA after a launch
+ *     therefore means the call's own launch or copy failed.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
  *     asynchronous on that stream unless stated otherwise.
  *   - Errors the host can see (null pointers, bad sizes or strides, dtype,
