@@ -28,32 +28,12 @@ constexpr int kUnitBytes = SPEC_UNIT_BYTES;  // bytes of logits per (row, chunk)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Work-queue first-rejection pass (KW): units of work and queue sizing.  A row item is up to
-// kQRowGroup chunks of one target row; a residual item is up to kQResGroup residual units of
-// kQResTokens tokens (target logits and draft probabilities of one output row).  The queue
-// holds every item a call can publish while it runs, plus one claim per warp beyond them.
-#ifndef SPEC_WQ_ROW_GROUP
-#define SPEC_WQ_ROW_GROUP 2
-#endif
-#ifndef SPEC_WQ_RES_GROUP
-#define SPEC_WQ_RES_GROUP 4
-#endif
-constexpr int kQRowGroup = SPEC_WQ_ROW_GROUP;
-constexpr int kQResGroup = SPEC_WQ_RES_GROUP;
-constexpr int kQResTokens = 1024;
-constexpr int kQMaxWarps = 4096;  // the pass's grid is clamped to this many warps
-constexpr int kQCtlWords = 16;
-
 // Layout of the workspace (all offsets 256-byte aligned).  The error word comes first so
 // that spec_reject_last_device_error() finds it without knowing the call's sizes.
 struct Plan {
     int chunk;    // logits per chunk
     int nchunks;  // chunks per row
-    int nres;     // residual units per row (kQResTokens tokens each)
-    int row_items, res_items;  // queue items per target row / per residual pass
-    size_t dq_cap;             // queue entries
-    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, off_rcnt, off_thr, off_ctl, off_fresh, off_dq,
-        off_cnt, total;
+    size_t off_err, off_part, off_rstate, off_rstat, off_rpart, off_rcnt, off_thr, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -65,11 +45,6 @@ inline bool make_plan(int32_t B, int64_t T, int32_t V, spec_dtype dt, int has_q,
     const int es = dt == SPEC_BF16 ? 2 : 4;
     pl->chunk = kUnitBytes / es;
     pl->nchunks = (V + pl->chunk - 1) / pl->chunk;
-    pl->nres = (V + kQResTokens - 1) / kQResTokens;
-    pl->row_items = (pl->nchunks + kQRowGroup - 1) / kQRowGroup;
-    pl->res_items = (pl->nres + kQResGroup - 1) / kQResGroup;
-    pl->dq_cap = (size_t)(T - B) * pl->row_items + (has_q ? (size_t)B * pl->res_items : 0) + kQMaxWarps;
-    const size_t rmass = (size_t)(pl->nres > pl->nchunks ? pl->nres : pl->nchunks);
     size_t o = 0;
     pl->off_err = o;
     o = align256(o + 4 * sizeof(int32_t));
@@ -80,19 +55,11 @@ inline bool make_plan(int32_t B, int64_t T, int32_t V, spec_dtype dt, int has_q,
     pl->off_rstat = o;
     o = align256(o + sizeof(float2) * (size_t)(B + 1));
     pl->off_rpart = o;
-    o = align256(o + (has_q ? sizeof(float) * (size_t)B * rmass : 0));
+    o = align256(o + (has_q ? sizeof(float) * (size_t)B * (size_t)pl->nchunks : 0));
     pl->off_rcnt = o;
     o = align256(o + (has_q ? sizeof(int32_t) * (size_t)B : 0));
     pl->off_thr = o;
     o = align256(o + sizeof(uint32_t) * (size_t)T);
-    pl->off_ctl = o;
-    o = align256(o + sizeof(uint32_t) * kQCtlWords);
-    pl->off_fresh = o;
-    o = align256(o + 16 * (size_t)T);
-    pl->off_dq = o;
-    o = align256(o + 16 * pl->dq_cap);
-    pl->off_cnt = o;
-    o = align256(o + sizeof(int32_t) * (size_t)T);
     pl->total = o + 256;  // slack for aligning the caller's pointer
     return true;
 }
@@ -114,8 +81,7 @@ struct Params {
     // workspace
     float2 *part;     // [T * nchunks] chunk partials
     int32_t *err;     // [0] SPEC_DEVERR_* bits, [1] first bad request (INT_MAX = none)
-    int32_t *rstate;  // [B] K2 / K3: output position j of a pending explicit-q recovery, else -1;
-                      //     KW: last position whose row has been published
+    int32_t *rstate;  // [B] output position j of a pending explicit-q recovery, else -1
     float2 *rstat;    // [B] (M, S) of that output row
     float *rpart;     // [B * nchunks] residual chunk masses
     int32_t *rcnt;    // [B] residual chunks done (zeroed by K2, counted up by K3)
@@ -132,27 +98,7 @@ struct Params {
     // diagnostics (all may be null)
     float *dbg_pdraft;
     float *dbg_z;
-    // work-queue pass (KW)
-    uint32_t *wq_ctl;          // [kQCtlWords] claim counters, published count, finished requests
-    ulonglong2 *wq_fresh;      // [T] rows streamed from the start (the first wq_depth of each request)
-    ulonglong2 *wq_dq;         // [dq_cap] items published while the pass runs
-    int32_t *wq_cnt;           // [T] per target row: chunks reduced (+1 once the rows before it accepted)
-    int wq_depth;              // rows of a request streamed ahead of its latest decision
-    int wq_tail_depth;         // the same once the fresh rows are used up and the queue runs low
-    int wq_spare_items;        // queued items below which the queue counts as running low
-    int wq_nres, wq_row_items, wq_res_items;
-    uint32_t wq_cap;
 };
-
-// Launch of the work-queue first-rejection pass (defined in queue.cu): the set-up kernel, then
-// the pass, on `stream`.  Returns the first launch error.
-// With `between` set, that event is recorded between the two launches and the pass waits for
-// the set-up kernel in plain stream order instead.
-cudaError_t launch_queue_pass(const Params &P, int DT, int sms, int blocks_per_sm, cudaStream_t stream,
-                              cudaEvent_t between);
-// Blocks per SM of the pass for the given logits dtype (0 if it cannot run), and the kernel
-// attribute set-up its launch needs; called once per device.
-cudaError_t queue_pass_occupancy(int DT, int *blocks_per_sm);
 
 
 namespace {

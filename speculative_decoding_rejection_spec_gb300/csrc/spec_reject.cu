@@ -2612,7 +2612,6 @@ struct DeviceInfo {
     int blocks_lazy[2] = {0, 0};
     int blocks_lazy_cut = 0;       // KL with cuts (bf16)
     int blocks_lazy_cut_host = 0;  // the same, rows in host memory
-    int blocks_queue[2] = {0, 0};  // KW, the work-queue first-rejection pass
 };
 
 constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
@@ -2662,8 +2661,6 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
                                                                kLThreads, kLCutSmem)))
             return e;
     }
-    if ((e = queue_pass_occupancy(DT, &di.blocks_queue[DT])))
-        return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
 
@@ -2698,27 +2695,6 @@ cudaError_t device_info(DeviceInfo **out)
 bool cuda_error_pending() { return cudaPeekAtLastError() != cudaSuccess; }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Rows KW streams ahead of each request's latest decision.  Depth 1 reads only rows the method
-// needs; a deeper window also reads rows past some first rejections but shortens the chain of
-// row-after-row waits, which pays when a batch is too small to keep HBM busy otherwise.
-#ifndef SPEC_WQ_FULL_DEPTH_BYTES
-#define SPEC_WQ_FULL_DEPTH_BYTES (64ll << 20)  // batches with at most this many logit bytes stream every row
-#endif
-#ifndef SPEC_WQ_DEPTH
-#define SPEC_WQ_DEPTH 1
-#endif
-#ifndef SPEC_WQ_TAIL_DEPTH
-#define SPEC_WQ_TAIL_DEPTH 3  // rows streamed ahead once the fresh rows are used up and work runs low
-#endif
-#ifndef SPEC_WQ_SPARE_PER_BLOCK
-#define SPEC_WQ_SPARE_PER_BLOCK 2  // queued items per block below which work counts as running low
-#endif
-int queue_depth(int64_t T, int32_t V, int DT)
-{
-    const int64_t bytes = T * (int64_t)V * (DT ? 2 : 4);
-    return bytes <= SPEC_WQ_FULL_DEPTH_BYTES ? SPEC_REJECT_MAX_SPEC_LEN + 1 : SPEC_WQ_DEPTH;
-}
 
 // Blocks for a persistent launch: enough to fill every SM at full occupancy, no more
 // than there is work for, at least one.
@@ -2870,41 +2846,9 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             cudaEventRecord(ev[evi], stream);
         ++evi;
     };
-    const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
-    // calls on device rows without cuts or diagnostics: KW streams the target rows up to each
-    // request's output row from a queue shared by every warp of the GPU
-    const bool q_rows_aligned = !q || (aligned(q, 16) && ((size_t)qstride * 4) % 16 == 0);
-#ifndef SPEC_USE_WQ
-#define SPEC_USE_WQ 0
-#endif
-    if (SPEC_USE_WQ && !filtered && !debug && !q_stage && !rows_in_host && B > 0 && T <= INT32_MAX && rows_aligned &&
-        q_rows_aligned && di->blocks_queue[DT] > 0) {
-        P.wq_ctl = reinterpret_cast<uint32_t *>(base + pl.off_ctl);
-        P.wq_fresh = reinterpret_cast<ulonglong2 *>(base + pl.off_fresh);
-        P.wq_dq = reinterpret_cast<ulonglong2 *>(base + pl.off_dq);
-        P.wq_cnt = reinterpret_cast<int32_t *>(base + pl.off_cnt);
-        P.wq_cap = (uint32_t)pl.dq_cap;
-        P.wq_nres = pl.nres;
-        P.wq_row_items = pl.row_items;
-        P.wq_res_items = pl.res_items;
-        P.wq_depth = queue_depth(T, V, DT);
-        P.wq_tail_depth = SPEC_WQ_TAIL_DEPTH;
-        P.wq_spare_items = (int)((int64_t)di->sms * di->blocks_queue[DT] * SPEC_WQ_SPARE_PER_BLOCK);
-        P.rstate = reinterpret_cast<int32_t *>(base + pl.off_rstate);
-        if (q)
-            P.rcnt = reinterpret_cast<int32_t *>(base + pl.off_rcnt);
-        mark();
-        // with stage events the set-up kernel and the pass are timed apart (an event between
-        // them replaces the programmatic dependency by plain stream order)
-        cudaEvent_t mid = (evi < nev && ev[evi]) ? ev[evi] : nullptr;
-        ++evi;
-        if (launch_queue_pass(P, DT, di->sms, di->blocks_queue[DT], stream, mid) != cudaSuccess)
-            return SPEC_ERR_CUDA;
-        mark();
-        return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
-    }
     // calls without diagnostics (and with cuts only on bf16 rows, which in host memory need a
     // device copy to cut from): KL reads rows only up to each request's first rejection
+    const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
     const bool cut_ok = !filtered || (DT == 1 && (rows_in_host ? row_stage && di->blocks_lazy_cut_host > 0
                                                                : di->blocks_lazy_cut > 0));
     if (cut_ok && !debug && (!q_stage || rows_in_host) && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
@@ -3424,10 +3368,8 @@ int spec_reject_version(void) { return 100; }
 
 int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters)
 {
-    if (!has_filters && B > 0)
-        return 2;  // set-up, then the work-queue pass up to each first rejection
-    if (B >= SPEC_KL_MIN_REQUESTS && logits_dtype == SPEC_BF16)
-        return 2;  // layout check, then the pass up to each first rejection with cuts
+    if (B >= SPEC_KL_MIN_REQUESTS && (!has_filters || logits_dtype == SPEC_BF16))
+        return 2;  // layout check, then the pass up to each first rejection
     return (has_filters ? 3 : 2) + (has_draft_probs ? 1 : 0);
 }
 

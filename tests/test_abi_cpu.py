@@ -86,21 +86,16 @@ def test_host_entry_checks(lib):
 
 
 def test_kernel_counts_per_call_kind(lib):
-    """Which pass a call takes, from the host logic alone: a call without top-k / top-p takes the
-    work-queue first-rejection pass (set-up, then the pass: 2 launches) for any B >= 1; with
-    filters, 64 or more requests on bf16 rows take the first-rejection pass with cuts (2
-    launches); otherwise the full pass (K1, K2, plus the cut with filters, plus the residual pass
-    with draft probabilities)."""
+    """Which pass a call takes, from the host logic alone: 64 or more requests take the
+    first-rejection pass (2 launches), with top-k / top-p only on bf16 rows; otherwise the full
+    pass (K1, K2, plus the cut with filters, plus the residual pass with draft probabilities)."""
     for dt in (binding.F32, binding.BF16):
         for q in (False, True):
             assert binding.num_kernels(64, q, False, dt) == 2
-            assert binding.num_kernels(1, q, False, dt) == 2
-            assert binding.num_kernels(0, q, False, dt) == 2 + q
+            assert binding.num_kernels(63, q, False, dt) == 2 + q
             assert binding.num_kernels(0, q, True, dt) == 3 + q
-            assert binding.num_kernels(63, q, True, dt) == 3 + q
         assert binding.reads_to_first_rejection(1024, False, dt)
-        assert binding.reads_to_first_rejection(1, False, dt)
-        assert not binding.reads_to_first_rejection(63, True, dt)
+        assert not binding.reads_to_first_rejection(63, False, dt)
     assert binding.num_kernels(64, True, True, binding.BF16) == 2
     assert binding.num_kernels(64, True, True, binding.F32) == 4
     assert binding.reads_to_first_rejection(64, True, binding.BF16)
