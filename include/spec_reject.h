@@ -282,10 +282,13 @@ spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype lo
  * every GPU loading this library holds until the process exits.  A batch whose
  * spec_reject_workspace_size() exceeds that returns SPEC_ERR_WORKSPACE and launches
  * nothing (for V = 128256 bf16 logits with draft probabilities and K = 8 that is
- * 3432 requests, 30888 target rows).  The call allocates nothing.
+ * 3376 requests, 30384 target rows).  Argument errors are reported first, with the status
+ * spec_reject_sample() returns for them.  The call allocates nothing.
  *
- * The first call on a device (the current device) looks up the array's device address;
- * make that first call before any stream capture.  Every call shares the one array and
+ * The first call on a device (the current device) looks up the array's device address
+ * (once, safely when several host threads make it at once); make that first call before
+ * any stream capture.  cudaDeviceReset() on a device invalidates that address: do not call
+ * this entry on that device again in the same process.  Every call shares the one array and
  * leaves its contents behind: calls that can overlap on the GPU (different streams, or
  * different host threads on one device) race and must be serialised by the caller.
  *
@@ -380,6 +383,13 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
  * (2), plus the top-k / top-p cut with filters, plus the residual pass with draft
  * probabilities. */
 int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters);
+
+/* Blocks (one thread-block cluster) that work on each request in a call of B requests with
+ * V-token rows on the current device that reads rows up to each first rejection without top-k /
+ * top-p: 1 when the batch fills the GPU one block per request, else 2, 4 or 8 (rows split over
+ * more warps); 0 for invalid sizes or when no device is usable.  The pages have no counterpart:
+ * this reports the launch shape, for tests and measurements. */
+int spec_reject_blocks_per_request(spec_dtype logits_dtype, int32_t B, int32_t V);
 
 /* Static description of a status code. */
 const char *spec_reject_status_string(spec_status status);

@@ -26,7 +26,7 @@ EXPORTED = [
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
     "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
     "spec_tree_workspace_size", "spec_tree_verify_greedy", "spec_reject_sample_filtered", "spec_reject_sample_ex",
-    "spec_reject_sample_host_ex",
+    "spec_reject_sample_host_ex", "spec_reject_blocks_per_request",
 ]
 
 
@@ -92,6 +92,8 @@ def load():
                                                 P, sz, P, P, P]
     lib.spec_reject_sample_ex.restype = ctypes.c_int
     lib.spec_reject_sample_ex.argtypes = sample_args + [P]
+    lib.spec_reject_blocks_per_request.restype = ctypes.c_int
+    lib.spec_reject_blocks_per_request.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int, ctypes.c_int]
     _lib = lib
@@ -317,6 +319,11 @@ def num_kernels(B: int, has_draft_probs: bool, has_filters: bool = False, dtype:
     """Kernels one call of B requests launches (16-byte-aligned rows in device memory)."""
     return int(load().spec_reject_num_kernels(int(dtype), int(B), int(bool(has_draft_probs)),
                                               int(bool(has_filters))))
+
+
+def blocks_per_request(B: int, V: int, dtype: int = BF16) -> int:
+    """Blocks (a thread-block cluster) per request of an unfiltered call on the current device."""
+    return int(load().spec_reject_blocks_per_request(int(dtype), int(B), int(V)))
 
 
 def reads_to_first_rejection(B: int, has_filters: bool = False, dtype: int = BF16) -> bool:

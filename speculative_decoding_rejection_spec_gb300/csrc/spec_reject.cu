@@ -1348,7 +1348,7 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #define SPEC_KL_STAGES 1      // ring slots per warp (8 warps x 2 blocks: 16 units in flight per SM)
 #endif
 #ifndef SPEC_KL_MIN_REQUESTS
-#define SPEC_KL_MIN_REQUESTS 64  // smaller batches: each request's chain of rows would set the time
+#define SPEC_KL_MIN_REQUESTS 64  // smaller batches with cuts or host rows: the full pass is faster
 #endif
 #ifndef SPEC_KL_RESIDUAL_UNROLL
 #define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass
@@ -1359,6 +1359,10 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #ifndef SPEC_KL_MIN_BLOCKS
 #define SPEC_KL_MIN_BLOCKS 2  // blocks per SM
 #endif
+#ifndef SPEC_KL_CLUSTER_LOG2
+#define SPEC_KL_CLUSTER_LOG2 -1  // -1: cluster size by the rule below; 0..3: always 1, 2, 4 or 8 blocks
+#endif
+
 constexpr int kLWarps = SPEC_KL_WARPS;
 constexpr int kLStages = SPEC_KL_STAGES;
 constexpr int kLThreads = kLWarps * 32;
@@ -1932,14 +1936,51 @@ struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
     __device__ __forceinline__ float operator()(int c) const { return z[c]; }
 };
 
+// Cluster helpers of the clustered first-rejection pass (CS blocks per request).  With CS = 1
+// they reduce to the block's own shared memory and __syncthreads().
+template <int CS> __device__ __forceinline__ void cluster_barrier()
+{
+    if constexpr (CS > 1)
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    else
+        __syncthreads();
+}
+
+template <int CS> __device__ __forceinline__ unsigned cluster_rank()
+{
+    if constexpr (CS > 1) {
+        unsigned r;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+        return r;
+    } else {
+        return 0;
+    }
+}
+
+// The same shared variable in block `rank` of the cluster (generic address).
+template <int CS, class T> __device__ __forceinline__ T *in_block(T *p, unsigned rank)
+{
+    if constexpr (CS > 1)
+        return cg::this_cluster().map_shared_rank(p, rank);
+    else
+        return p;
+}
+
 // HOST: the target rows live in pinned host memory (read over the host link with 16-byte loads,
 // sixteen in flight per lane) instead of device memory (TMA bulk copies).  CUT (bf16 rows): the
 // call has top-k / top-p cuts, applied to each row as it is reached (rows in host memory are cut
 // from their device copies).
-template <int DT, bool HOST, bool CUT>
+// CS > 1: a thread-block cluster of CS blocks works on each request.  Its CS * kLWarps warps
+// split every row and every residual pass (chunk c goes to cluster warp c mod (CS * kLWarps)),
+// write their chunk partials and residual masses into the leader block's (rank 0) shared
+// memory, and the leader's warp 0 decides and draws; the leader claims the requests and
+// sends the request index and each decision to every block of the cluster.  Every block
+// takes the same cluster barriers in the same order.
+template <int DT, bool HOST, bool CUT, int CS = 1>
 __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Params P)
 {
     static_assert(!CUT || DT == 1, "cuts in KL: bf16 rows (from host memory: through their device copies)");
+    static_assert(CS == 1 || (!HOST && !CUT), "clusters: rows in device memory, no cuts");
     constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char ring[];
     CutSmem &C = *reinterpret_cast<CutSmem *>(ring + kLSmem);  // CUT only: after the rings
@@ -1949,6 +1990,12 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     __shared__ int s_r, s_go, s_abort;
     __shared__ float s_M, s_S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned rank = cluster_rank<CS>();
+    const bool leader = rank == 0;
+    const int cw = (int)rank * kLWarps + warp;  // this warp's index in the cluster
+    constexpr int kCW = CS * kLWarps;           // warps per cluster
+    float2 *const lpart = in_block<CS>(spart, 0u);  // the leader's chunk partials
+    float *const lrm = in_block<CS>(srm, 0u);       // and residual masses
 
     if (P.err[0] & SPEC_DEVERR_LAYOUT) {  // the whole batch is invalid (as K2 reports it)
         for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < P.B; r += gridDim.x * blockDim.x)
@@ -1970,7 +2017,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     mbar_fence_init();
     if (threadIdx.x == 0)
         s_abort = 0;
-    __syncthreads();
+    cluster_barrier<CS>();  // every block's shared state is set up before any block writes into it
     unsigned char *slots = ring + (size_t)warp * kLStages * kUnitBytes;
     uint64_t *bars = full + warp * kLStages;
     int64_t qi = 0, qc = 0;  // this warp's units issued (lane 0) and consumed; slot = count % stages
@@ -1987,12 +2034,15 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     };
 
     for (;;) {
-        if (threadIdx.x == 0)
-            s_r = atomicAdd(P.err + 2, 1);
-        __syncthreads();
+        if (leader && threadIdx.x == 0) {
+            const int nr = s_abort ? P.B : atomicAdd(P.err + 2, 1);
+            for (unsigned q = 0; q < (unsigned)CS; ++q)
+                *in_block<CS>(&s_r, q) = nr;
+        }
+        cluster_barrier<CS>();
         const int r = s_r;
-        if (r >= P.B || s_abort)
-            break;  // uniform
+        if (r >= P.B || (CS == 1 && s_abort))
+            break;  // uniform across the cluster
         const int cu0 = P.cu[r];
         const int k = P.cu[r + 1] - cu0;
         const int64_t tb = (int64_t)cu0 + r;
@@ -2004,7 +2054,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             xs = P.ids[db + lane];
         const unsigned badid = __ballot_sync(kFull, !too_long && lane < k && (xs < 0 || xs >= P.V));
         if (too_long || badid) {
-            if (warp == 0) {
+            if (leader && warp == 0) {
                 for (int64_t i = lane; i <= k; i += 32)
                     P.out_tokens[tb + i] = -1;
                 if (lane == 0) {
@@ -2013,7 +2063,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     atomicMin(P.err + 1, r);
                 }
             }
-            __syncthreads();  // s_r is rewritten for the next request
+            cluster_barrier<CS>();  // s_r is rewritten for the next request
             continue;
         }
         const float temp = P.temp[r];
@@ -2027,7 +2077,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             }
         // inputs of the acceptance test of draft position `lane` (warp 0), issued first
         float ls = 0.f, qs = 1.f, ua = 0.f, usl = 0.f;
-        if (warp == 0 && !greedy) {
+        if (leader && warp == 0 && !greedy) {
             if (lane < k) {
                 ls = load1<DT>(row_ptr<DT>(P, tb + lane), xs);
                 if (P.q)
@@ -2037,17 +2087,17 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             if (lane <= k)
                 usl = P.uni[2 * (tb + lane) + 1];  // the sampling draw, wherever the output lands
         }
-        const float us32 = (warp == 0 && !greedy && k == 32) ? P.uni[2 * (tb + 32) + 1] : 0.f;
+        const float us32 = (leader && warp == 0 && !greedy && k == 32) ? P.uni[2 * (tb + 32) + 1] : 0.f;
 
         int j = k;       // output position: the first rejection, else the bonus row
         int am = 0;      // argmax of the latest row (greedy)
         float Mi = 0.f, Si = 0.f;
         for (int i = 0; i <= k; ++i) {
             const char *row = row_ptr<DT>(P, tb + i);
-            // ---- stream row t_i: this warp's units c = warp, warp + kLWarps, ...
-            int ci = warp;
+            // ---- stream row t_i: this warp's units c = cw, cw + kCW, ...
+            int ci = cw;
             if (!HOST && lane == 0)
-                for (int s = 0; s < kLStages && ci < P.nchunks; ++s, ci += kLWarps)
+                for (int s = 0; s < kLStages && ci < P.nchunks; ++s, ci += kCW)
                     issue(row, ci);
             bool ok = true;
             if constexpr (HOST) {
@@ -2085,7 +2135,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 if (CUT && P.lstage)  // the cut reads the device copy through the bulk-copy engine
                     fence_proxy_async_global();
             } else
-            for (int c = warp; c < P.nchunks; c += kLWarps) {
+            for (int c = cw; c < P.nchunks; c += kCW) {
                 const int s = (int)(qc % kLStages);
                 if (!__all_sync(kFull, mbar_wait(&bars[s], (uint32_t)(qc / kLStages) & 1, P.err))) {
                     ok = false;
@@ -2108,17 +2158,17 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 ++qc;
                 if (lane == 0 && ci < P.nchunks) {  // the slot is in registers: refill it
                     issue(row, ci);
-                    ci += kLWarps;
+                    ci += kCW;
                 }
                 if (greedy)
-                    argmax_regs<DT>(&spart[c], lane, v, R, row);
+                    argmax_regs<DT>(&lpart[c], lane, v, R, row);
                 else
-                    softmax_regs<DT>(&spart[c], cs, lane, v, R, row);
+                    softmax_regs<DT>(&lpart[c], cs, lane, v, R, row);
             }
             if (!ok && lane == 0)
-                s_abort = 1;
-            __syncthreads();  // the row's chunk partials are in spart
-            if (s_abort)
+                *in_block<CS>(&s_abort, 0u) = 1;
+            cluster_barrier<CS>();  // the row's chunk partials are in the leader's spart
+            if (CS == 1 && s_abort)
                 break;
             if constexpr (CUT)
                 if (!greedy) {  // uniform: the row's cut key, and its partials over the survivors
@@ -2128,7 +2178,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                         break;  // uniform (read after the cut's last barrier)
                 }
             // ---- the row's statistics (K2's per-row combine) and, on a draft row, the test
-            if (warp == 0) {
+            if (leader && warp == 0) {
                 float m = -INFINITY, sv = 0.f, best = -INFINITY;
                 int idx = INT_MAX;
                 for (int c = lane; c < P.nchunks; c += 32) {
@@ -2173,18 +2223,21 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     go = i < k && __shfl_sync(kFull, accept, i & 31);
                 }
                 if (lane == 0) {
-                    s_go = go;
-                    s_M = Mi;
-                    s_S = Si;
+                    const int g = (CS > 1 && s_abort) ? 2 : (int)go;  // 2: a block gave up on a wait
+                    for (unsigned q = 0; q < (unsigned)CS; ++q) {
+                        *in_block<CS>(&s_go, q) = g;
+                        *in_block<CS>(&s_M, q) = Mi;
+                        *in_block<CS>(&s_S, q) = Si;
+                    }
                 }
             }
-            __syncthreads();
-            if (!s_go) {
+            cluster_barrier<CS>();
+            if (s_go != 1) {
                 j = i;
                 break;
             }
         }
-        if (s_abort || (CUT && C.abort))
+        if ((CS == 1 && s_abort) || (CS > 1 && s_go == 2) || (CUT && C.abort))
             break;
 
         // ---- the output token at row t_j (K2 / K3 arithmetic)
@@ -2198,18 +2251,18 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         if (residual) {  // explicit q: residual chunk masses of row t_j by every warp (K3)
             const float Mj = s_M, Sj = s_S;
             const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
-            for (int c = warp; c < P.nchunks; c += kLWarps) {
+            for (int c = cw; c < P.nchunks; c += kCW) {
                 const int64_t lo = (int64_t)c * P.chunk, hi = min((int64_t)P.V, (int64_t)(c + 1) * P.chunk);
                 const float z = (HOST && qstage_j)
                                     ? warp_residual_chunk<DT, CUT, SPEC_KL_HOST_RESIDUAL_UNROLL, true>(f, lo, hi, lane,
                                                                                                        qstage_j)
                                     : warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(f, lo, hi, lane);
                 if (lane == 0)
-                    srm[c] = z;
+                    lrm[c] = z;
             }
-            __syncthreads();
+            cluster_barrier<CS>();
         }
-        if (warp == 0) {
+        if (leader && warp == 0) {
             const float us = greedy ? 0.f : (j < 32 ? __shfl_sync(kFull, usl, j & 31) : us32);
             if (greedy) {
                 token = am;  // the argmax of row t_j: the first mismatch, or the bonus row
@@ -2282,7 +2335,10 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     atomicAdd(C + SPEC_METRIC_ACCEPTED_PER_POS + lane, 1ull);
             }
         }
-        __syncthreads();  // spart, srm and the shared scalars are reused by the next request
+        if constexpr (CS == 1)
+            __syncthreads();  // spart, srm and the shared scalars are reused by the next request
+        // (clusters: the barrier after the next claim orders this request's last reads of
+        // them before any write of the next one)
     }
     // gave up on a wait: let this warp's copies still in flight land before exiting
     if (lane == 0)
@@ -2612,6 +2668,7 @@ struct DeviceInfo {
     int blocks_lazy[2] = {0, 0};
     int blocks_lazy_cut = 0;       // KL with cuts (bf16)
     int blocks_lazy_cut_host = 0;  // the same, rows in host memory
+    int clusters_lazy[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // KL with clusters of 1, 2, 4, 8 blocks
 };
 
 constexpr size_t kWrSmem = (size_t)kWrWarps * kWrStages * kUnitBytes;
@@ -2623,6 +2680,51 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 cudaError_t g_dev_err[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
+
+// Launch of KL with clusters of CS blocks (CS > 1): one cluster per request at a time.
+template <int DT, int CS> cudaError_t launch_lazy_cluster(const Params &P, int clusters, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(clusters * CS), 1, 1);
+    cfg.blockDim = dim3(kLThreads, 1, 1);
+    cfg.dynamicSmemBytes = kLSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lazy_kernel<DT, false, false, CS>, P);
+}
+
+// Clusters of CS blocks of KL that fit on the device at once (whole GPU).
+template <int DT, int CS> cudaError_t lazy_cluster_occupancy(int &clusters)
+{
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(lazy_kernel<DT, false, false, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kLSmem)))
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(CS * 64), 1, 1);
+    cfg.blockDim = dim3(kLThreads, 1, 1);
+    cfg.dynamicSmemBytes = kLSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&clusters, lazy_kernel<DT, false, false, CS>, &cfg);
+    if (e) {  // clusters of this size cannot run here: the call keeps to smaller ones
+        (void)cudaGetLastError();
+        clusters = 0;
+        return cudaSuccess;
+    }
+    return cudaSuccess;
+}
 
 template <int DT> cudaError_t fill_info(DeviceInfo &di)
 {
@@ -2647,6 +2749,10 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy[DT], lazy_kernel<DT, false, false>,
                                                            kLThreads, kLSmem)))
         return e;
+    if ((e = lazy_cluster_occupancy<DT, 2>(di.clusters_lazy[DT][1])) || (e = lazy_cluster_occupancy<DT, 4>(di.clusters_lazy[DT][2])) ||
+        (e = lazy_cluster_occupancy<DT, 8>(di.clusters_lazy[DT][3])))
+        return e;
+    di.clusters_lazy[DT][0] = di.blocks_lazy[DT];  // per SM; multiplied by the SM count at launch
     if constexpr (DT == 1) {
         if ((e = cudaFuncSetAttribute(lazy_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kLCutSmem)))
@@ -2695,6 +2801,21 @@ cudaError_t device_info(DeviceInfo **out)
 bool cuda_error_pending() { return cudaPeekAtLastError() != cudaSuccess; }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// log2 of the blocks per request of KL on device rows without cuts: clusters serve batches too
+// small to fill the GPU one block per request.  The largest cluster (at most 8 blocks) such
+// that the GPU holds a cluster for every request at once and every warp of a cluster has at
+// least one chunk of each row (a cluster serialises its requests' draws, and its barriers cost
+// more than a small row saves).
+int lazy_cluster_log2(const DeviceInfo &di, int DT, int32_t B, int nchunks)
+{
+    if (SPEC_KL_CLUSTER_LOG2 >= 0)
+        return di.clusters_lazy[DT][SPEC_KL_CLUSTER_LOG2] > 0 ? SPEC_KL_CLUSTER_LOG2 : 0;
+    for (int c = 3; c >= 1; --c)
+        if (di.clusters_lazy[DT][c] >= B && (kLWarps << c) <= nchunks)
+            return c;
+    return 0;
+}
 
 // Blocks for a persistent launch: enough to fill every SM at full occupancy, no more
 // than there is work for, at least one.
@@ -2851,7 +2972,10 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     const bool rows_aligned = aligned(logits, 16) && ((size_t)lstride * (DT ? 2 : 4)) % 16 == 0;
     const bool cut_ok = !filtered || (DT == 1 && (rows_in_host ? row_stage && di->blocks_lazy_cut_host > 0
                                                                : di->blocks_lazy_cut > 0));
-    if (cut_ok && !debug && (!q_stage || rows_in_host) && B >= SPEC_KL_MIN_REQUESTS && T > 0 && rows_aligned &&
+    // any B >= 1 on device rows without cuts (small batches in clusters of blocks); with cuts,
+    // or rows in host memory, batches of at least SPEC_KL_MIN_REQUESTS
+    const bool kl_batch = B >= ((filtered || rows_in_host) ? SPEC_KL_MIN_REQUESTS : 1);
+    if (cut_ok && !debug && (!q_stage || rows_in_host) && kl_batch && T > 0 && rows_aligned &&
         di->blocks_lazy[DT] > 0) {
         mark();
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
@@ -2873,6 +2997,25 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
         }
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
+        if (!rows_in_host) {
+            // clusters of CS blocks per request, for batches too small to fill the GPU one block per
+            // request: the largest CS (at most 8) such that the GPU holds a cluster for every request
+            // at once and every warp of a cluster has at least one chunk of each row (a cluster
+            // serialises its requests' draws, and its barriers cost more than a small row saves)
+            const int ci = lazy_cluster_log2(*di, DT, B, pl.nchunks);
+            if (ci > 0) {
+                const int ncl = (int)clamp_grid(di->clusters_lazy[DT][ci], B);
+                cudaError_t e;
+                if (DT)
+                    e = ci == 1 ? launch_lazy_cluster<1, 2>(P, ncl, stream)
+                                : ci == 2 ? launch_lazy_cluster<1, 4>(P, ncl, stream) : launch_lazy_cluster<1, 8>(P, ncl, stream);
+                else
+                    e = ci == 1 ? launch_lazy_cluster<0, 2>(P, ncl, stream)
+                                : ci == 2 ? launch_lazy_cluster<0, 4>(P, ncl, stream) : launch_lazy_cluster<0, 8>(P, ncl, stream);
+                mark();
+                return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+            }
+        }
         if (rows_in_host) {
             if (DT)
                 lazy_kernel<1, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
@@ -3366,9 +3509,18 @@ const char *spec_reject_status_string(spec_status status)
 
 int spec_reject_version(void) { return 100; }
 
+int spec_reject_blocks_per_request(spec_dtype logits_dtype, int32_t B, int32_t V)
+{
+    Plan pl;
+    DeviceInfo *di;
+    if (B < 1 || !make_plan(B, B, V, logits_dtype, 0, &pl) || device_info(&di) != cudaSuccess)
+        return 0;
+    return 1 << lazy_cluster_log2(*di, logits_dtype == SPEC_BF16 ? 1 : 0, B, pl.nchunks);
+}
+
 int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters)
 {
-    if (B >= SPEC_KL_MIN_REQUESTS && (!has_filters || logits_dtype == SPEC_BF16))
+    if (B >= (has_filters ? SPEC_KL_MIN_REQUESTS : 1) && (!has_filters || logits_dtype == SPEC_BF16))
         return 2;  // layout check, then the pass up to each first rejection
     return (has_filters ? 3 : 2) + (has_draft_probs ? 1 : 0);
 }

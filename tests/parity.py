@@ -133,3 +133,22 @@ def assert_rowstats(w, gpu, ref):
     tol = 1e-5 * zr + (2e-6 if explicit else 0.0)
     bad = np.abs(zg - zr) > tol
     assert not bad.any(), f"Z: gpu {zg[bad][:4]} oracle {zr[bad][:4]}"
+
+
+def assert_both_paths(w, ref=None, max_mismatch_frac=0.01, rowstats=True):
+    """The production call (the pass that reads rows up to each first rejection, in clusters of
+    blocks for small batches) and the diagnostic call (the full pass over every row, with the
+    per-row probabilities) both against the oracle, and against each other: they take every
+    decision with the same arithmetic, so their outputs must be identical."""
+    ref = ref if ref is not None else oracle.reject_sample_workload(w, debug=True)
+    full = run_gpu(w, debug=True)
+    assert full["status"] == 0 or full["status"] == 5, full["status"]
+    c, _, _ = assert_parity(w, full, ref, max_mismatch_frac=max_mismatch_frac)
+    if rowstats:
+        assert_rowstats(w, full, ref)
+    prod = run_gpu(w)
+    assert prod["status"] == full["status"] and prod["bits"] == full["bits"]
+    assert_parity(w, prod, ref, max_mismatch_frac=max_mismatch_frac)
+    assert np.array_equal(prod["tokens"], full["tokens"]) and np.array_equal(prod["acc"], full["acc"]), \
+        f"{w['name']}: the two passes differ"
+    return c, prod, full, ref

@@ -86,16 +86,20 @@ def test_host_entry_checks(lib):
 
 
 def test_kernel_counts_per_call_kind(lib):
-    """Which pass a call takes, from the host logic alone: 64 or more requests take the
-    first-rejection pass (2 launches), with top-k / top-p only on bf16 rows; otherwise the full
-    pass (K1, K2, plus the cut with filters, plus the residual pass with draft probabilities)."""
+    """Which pass a call takes, from the host logic alone: without top-k / top-p every batch of
+    at least one request takes the first-rejection pass (2 launches); with them, 64 or more
+    requests on bf16 rows; otherwise the full pass (K1, K2, plus the cut with filters, plus the
+    residual pass with draft probabilities)."""
     for dt in (binding.F32, binding.BF16):
         for q in (False, True):
             assert binding.num_kernels(64, q, False, dt) == 2
-            assert binding.num_kernels(63, q, False, dt) == 2 + q
+            assert binding.num_kernels(1, q, False, dt) == 2
+            assert binding.num_kernels(0, q, False, dt) == 2 + q
             assert binding.num_kernels(0, q, True, dt) == 3 + q
+            assert binding.num_kernels(63, q, True, dt) == 3 + q
         assert binding.reads_to_first_rejection(1024, False, dt)
-        assert not binding.reads_to_first_rejection(63, False, dt)
+        assert binding.reads_to_first_rejection(1, False, dt)
+        assert not binding.reads_to_first_rejection(63, True, dt)
     assert binding.num_kernels(64, True, True, binding.BF16) == 2
     assert binding.num_kernels(64, True, True, binding.F32) == 4
     assert binding.reads_to_first_rejection(64, True, binding.BF16)
@@ -123,3 +127,26 @@ def test_host_entry_with_options_checks(lib):
     bad = list(args)
     bad[6] = None  # cu_num_draft
     assert lib.spec_reject_sample_host_ex(*bad, 1 << 30, None, None, None, None) == 1
+
+
+def test_noalloc_capacity_and_oversized_batches(lib):
+    """The fixed scratch of spec_reject_sample_noalloc holds the workspace of 3376 requests of
+    K = 8 drafts over V = 128256 bf16 logits with draft probabilities (30384 target rows), and
+    not of one request more; a larger batch is refused with SPEC_ERR_WORKSPACE after the
+    argument checks and before any CUDA call (no device needed)."""
+    cap = 8 << 20
+    size = lambda B: lib.spec_reject_workspace_size(B, 9 * B, 128256, binding.BF16, 1)
+    assert size(3376) <= cap < size(3377)
+    fake = ctypes.c_void_p(4096)
+    for B in (3377, 40000):
+        st = lib.spec_reject_sample_noalloc(fake, binding.BF16, 9 * B, 128256, 128256, fake, 128256, fake, fake, B,
+                                            fake, fake, fake, fake, None, None)
+        assert st == 3 and binding.status_string(st) == "workspace too small"
+    # argument errors come first, as in spec_reject_sample
+    st = lib.spec_reject_sample_noalloc(None, binding.BF16, 9 * 40000, 128256, 128256, None, 0, None, None, 40000,
+                                        None, None, None, None, None, None)
+    assert st == lib.spec_reject_sample(None, binding.BF16, 9 * 40000, 128256, 128256, None, 0, None, None, 40000,
+                                        None, None, None, None, None, 0, None) == 1
+    st = lib.spec_reject_sample_noalloc(fake, binding.BF16, 8, 2000000, 2000000, None, 0, fake, fake, 2,
+                                        fake, fake, fake, fake, None, None)
+    assert st == 2  # V above SPEC_REJECT_MAX_VOCAB: unsupported, as spec_reject_sample reports it

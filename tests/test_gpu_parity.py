@@ -28,11 +28,8 @@ SMALL = ["tiny", "greedy", "probabilistic", "deterministic", "large-128"]
 @pytest.mark.parametrize("name", SMALL)
 def test_config_parity_and_rowstats(name):
     w = W.generate(name)
-    ref = oracle.reject_sample_workload(w, debug=True)
-    gpu = PT.run_gpu(w, debug=True)
-    assert gpu["status"] == 0, gpu
-    c, _, _ = PT.assert_parity(w, gpu, ref)
-    PT.assert_rowstats(w, gpu, ref)
+    c, prod, full, ref = PT.assert_both_paths(w)
+    assert full["status"] == 0, full
     if name == "greedy":
         assert c.flagged == 0  # every greedy decision is an exact comparison
 
@@ -104,10 +101,7 @@ def test_ragged_k_zero_and_max_odd_vocab(dtype, draft):
     """k in 0..32 (k = 0 and k = 32 present), V = 5003 (odd: misaligned rows, vector tails)."""
     w = W.generate(dict(B=24, K=_mixed_k(24, 5), V=5003, dtype=dtype, sigma=1.0, temperature=1.0, draft=draft,
                         q_sigma=0.3, p_match=0.9, seed=21), name=f"ragged-{dtype}-{draft}")
-    ref = oracle.reject_sample_workload(w, debug=True)
-    gpu = PT.run_gpu(w, debug=True)
-    PT.assert_parity(w, gpu, ref, max_mismatch_frac=0.05)
-    PT.assert_rowstats(w, gpu, ref)
+    PT.assert_both_paths(w, max_mismatch_frac=0.05)
 
 
 @pytest.mark.parametrize("V", [1, 7, 1001, 4096, 4097, 12289])
@@ -117,10 +111,7 @@ def test_vocab_edges(V):
         for draft in ("noisy_q", "uniform"):
             w = W.generate(dict(B=6, K=3, V=V, dtype=dtype, sigma=1.5, temperature=0.9, draft=draft, seed=V),
                            name=f"V{V}-{dtype}-{draft}")
-            ref = oracle.reject_sample_workload(w, debug=True)
-            gpu = PT.run_gpu(w, debug=True)
-            PT.assert_parity(w, gpu, ref, max_mismatch_frac=0.2)
-            PT.assert_rowstats(w, gpu, ref)
+            PT.assert_both_paths(w, max_mismatch_frac=0.2)
 
 
 def test_q_equals_p_accepts_everything():
@@ -164,10 +155,7 @@ def test_one_hot_target_and_masked_logits(dtype):
     sel = isd & hot_rows & (rng.random(w["T"]) < 0.5)
     w["draft_ids"][drow[sel]] = hot[sel]
     w["logits"][:] = W.f32_to_bf16_bits(lg) if dtype == "bf16" else lg
-    ref = oracle.reject_sample_workload(w, debug=True)
-    gpu = PT.run_gpu(w, debug=True)
-    PT.assert_parity(w, gpu, ref)
-    PT.assert_rowstats(w, gpu, ref)
+    PT.assert_both_paths(w)
 
 
 def test_mixed_greedy_and_sampled_explicit_q():
@@ -175,10 +163,7 @@ def test_mixed_greedy_and_sampled_explicit_q():
     temps[::5] = 0.0
     w = W.generate(dict(B=40, K="ragged", K_max=8, V=7000, dtype="bf16", sigma=2.5, temperature=temps,
                         draft="noisy_q", q_sigma=0.5, seed=61), name="mixed")
-    ref = oracle.reject_sample_workload(w, debug=True)
-    gpu = PT.run_gpu(w, debug=True)
-    PT.assert_parity(w, gpu, ref)
-    PT.assert_rowstats(w, gpu, ref)
+    PT.assert_both_paths(w)
 
 
 def test_greedy_bf16_ties_lowest_index():
@@ -191,12 +176,9 @@ def test_greedy_bf16_ties_lowest_index():
     req = np.repeat(np.arange(w["B"]), 6)
     isd = (rows - (w["cu_num_draft"][req] + req)) < 5
     w["draft_ids"][:] = am[isd]
-    ref = oracle.reject_sample_workload(w, debug=True)
-    gpu = PT.run_gpu(w, debug=True)
-    c, _, _ = PT.assert_parity(w, gpu, ref)
+    c, prod, full, ref = PT.assert_both_paths(w)
     assert c.flagged == 0
-    assert (gpu["acc"] == 5).all()
-    PT.assert_rowstats(w, gpu, ref)
+    assert (prod["acc"] == 5).all()
 
 
 def test_zero_uniforms():
@@ -407,6 +389,7 @@ def test_first_rejection_pass_equals_full_pass(name, over):
     lazy = PT.run_gpu(w)
     full = PT.run_gpu(w, debug=True)
     assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
 
 
 def test_first_rejection_pass_long_chains_and_counters():
@@ -419,9 +402,45 @@ def test_first_rejection_pass_long_chains_and_counters():
     lazy = PT.run_gpu(w)
     full = PT.run_gpu(w, debug=True)
     assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_parity(w, lazy)
     assert (lazy["acc"] == K).any()  # q = p accepts every draft
     d = binding.to_device(w, "cuda")
     ctr = torch.zeros(binding.METRIC_COUNT, dtype=torch.int64, device="cuda")
     tok, acc = binding.sample_ex(**d, counters=ctr)
     from oracle import closed_forms as cf
     assert ctr.cpu().tolist() == cf.acceptance_counters(w["cu_num_draft"], acc.cpu().numpy())
+
+
+# ---------------------------------------------------------------------------- requests split over clusters
+
+@pytest.mark.parametrize("name,over,blocks", [
+    ("large-128", {}, 2),                                                   # 128 requests, 32 chunks per row
+    ("probabilistic", {}, 4),                                               # 32 fp32 requests, 63 chunks
+    ("wide", dict(B=24, K=4, V=262144, dtype="bf16", sigma=2.0, temperature=0.9, draft="noisy_q", q_sigma=0.7,
+                  q_temperature=1.0, seed=131), 8),                         # 24 requests, 64 chunks
+    ("wide-onehot", dict(B=20, K=6, V=262144, dtype="bf16", sigma=2.0, temperature=1.0, draft="target_mix",
+                         p_match=0.6, seed=132), 8),
+])
+def test_cluster_per_request_parity(name, over, blocks):
+    """Batches too small to fill the GPU one block per request split each request's rows and
+    residual pass over a thread-block cluster; the outputs match the oracle and, bit for bit,
+    the full pass."""
+    import torch
+    w = W.generate(name, **over) if name in W.CONFIGS else W.generate(over, name=name)
+    got = binding.blocks_per_request(w["B"], w["V"], PT.dtype_code(w))
+    if torch.cuda.get_device_properties(0).multi_processor_count >= 148:
+        assert got == blocks, got
+    PT.assert_both_paths(w, rowstats=False)
+
+
+def test_first_rejection_pass_branches_b72():
+    """Every branch of the first-rejection pass in one batch of 72 requests, against the oracle:
+    k in 0..32 (0 and 32 present), greedy and sampled requests mixed, one-hot drafts with bf16
+    rows of V = 12289 (ragged last chunk), and explicit draft probabilities with fp32 rows of
+    V = 4097."""
+    temps = np.where(np.arange(72) % 3 == 0, 0.0, 0.8).astype(np.float32)
+    for dtype, V, draft in (("bf16", 12289, "target_mix"), ("f32", 4097, "noisy_q")):
+        w = W.generate(dict(B=72, K=_mixed_k(72, 141), V=V, dtype=dtype, sigma=1.5, temperature=temps, draft=draft,
+                            p_match=0.8, q_sigma=0.3, seed=142), name=f"branches-{dtype}")
+        c, prod, full, ref = PT.assert_both_paths(w, max_mismatch_frac=0.05, rowstats=False)
+        assert (prod["acc"][temps == 0] >= 0).all()
