@@ -1,12 +1,20 @@
 """Benchmark of the batched rejection sampler on one GB300 (or N replicas).
 
-One step = one spec_reject_sample() call over a whole synthetic batch (every kernel
-of the path: row statistics, per-request finalize, and for explicit draft
-probabilities the residual and recovery passes), inputs resident in HBM.
+One step = one spec_reject_sample() call over a whole synthetic batch (every kernel of
+the path: the layout check, then the pass that reads each request's target rows up to
+its output row, decides, runs the residual pass of explicit-q rejections and draws the
+output token), inputs resident in HBM.
 
 Default workload: the large-batch sweep point B=1024, K=8, V=128256, bf16 target
 logits, explicit fp32 draft probabilities, temperature 0.7 (2.36 GB of logits +
 4.2 GB of draft probabilities per step: larger than L2, so no flush is needed).
+Exactly --steps calls are timed with CUDA events; SM clocks and clock-event reasons are
+read through NVML every 0.5 ms during that region.
+
+The JSON line also carries `per_config`: the other workloads of the target's list
+(tiny, greedy, probabilistic, deterministic, large-128, large-512), each timed for
+about half a second of calls in the same run (L2 flushed before every call when the
+inputs are smaller than twice L2), with its dominant kernel's roofline fraction.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (a bounded
 sample of the same workload on the host cores).
@@ -142,6 +150,72 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, reading only) every
+    half millisecond from a thread during the timed region: timed regions of a few milliseconds
+    are too short for nvidia-smi's 50 ms sampling."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            uuid = getattr(__import__("torch").cuda.get_device_properties(torch_device), "uuid", None)
+            found = False
+            if uuid is not None:
+                sid = str(uuid)
+                sid = sid if sid.startswith("GPU-") else "GPU-" + sid
+                found = lib.nvmlDeviceGetHandleByUUID(sid.encode(), ctypes.byref(h)) == 0
+            if not found and lib.nvmlDeviceGetHandleByIndex_v2(torch_device.index or 0, ctypes.byref(h)) != 0:
+                return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.ok = True
+        except OSError:
+            pass
+
+    def _one(self):
+        clk, rs = self.ct.c_uint(), self.ct.c_ulonglong()
+        a = self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(clk))
+        b = self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, self.ct.byref(rs))
+        return (float(clk.value) if a == 0 else None), (int(rs.value) if b == 0 else 0)
+
+    def start(self):
+        import threading
+        self.samples, self.stop_flag = [], False
+
+        def run():
+            while not self.stop_flag:
+                self.samples.append(self._one())
+                time.sleep(0.0005)
+        if self.ok:
+            self.th = threading.Thread(target=run, daemon=True)
+            self.th.start()
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self.stop_flag = True
+        self.th.join()
+        self.samples.append(self._one())
+        sm = [c for c, _ in self.samples if c is not None]
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "NVML, every 0.5 ms"}
+
+
+def clock_sampler(dev):
+    """NVML sampling where libnvidia-ml can be loaded, else nvidia-smi every 50 ms."""
+    n = NvmlClocks(dev)
+    return n if n.ok else ClockSampler(dev.index or 0)
+
+
 def cpu_baseline(w, target_s=8.0):
     """The oracle as it stands on the host cores, on the first requests of the workload."""
     import oracle
@@ -199,7 +273,7 @@ def time_calls(fn, steps, warmup, dev):
         fn()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    sampler = ClockSampler(dev.index or 0)
+    sampler = clock_sampler(dev)
     sampler.start()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
@@ -235,7 +309,7 @@ def time_graph(fn, steps, warmup, dev, per_graph=20):
         g.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    sampler = ClockSampler(dev.index or 0)
+    sampler = clock_sampler(dev)
     sampler.start()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
@@ -393,6 +467,7 @@ def main():
     ap.add_argument("--workload", default="large-1024")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' figures")
     ap.add_argument("--top-k", type=int, default=None, help="top-k on the target, every request")
     ap.add_argument("--top-p", type=float, default=None, help="top-p on the target, every request")
     ap.add_argument("--path", default="sample", choices=["sample", "tree", "ngram", "counters"],
@@ -433,51 +508,116 @@ def main():
     G.build()
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    peak, peak_kind = peaks()
+
+    m = measure(w, dev, args.steps, args.warmup, tk_tp=(args.top_k, args.top_p), barrier=world > 1)
+    if world > 1:
+        t = torch.tensor([m["total_ms"]], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        m["total_ms"] = float(t.item())
+    ms = m["total_ms"] / args.steps
+    positions = W.total_drafts(w)
+    value = positions * world / (ms / 1e3)
+    workload_key = args.workload + (f"+k{args.top_k}+p{args.top_p}" if filtered else "")
+    roofline = roofline_of(m, peak, peak_kind, workload_key)
+
+    meta["l2"] = m["l2"]
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
+            "hbm_gbs_effective": round(m["alg_bytes"] / (ms / 1e3) / 1e9, 1),
+            "stage_ms": [round(x, 4) for x in m["stage_ms"]], "stages": m["stages"],
+            "roofline": roofline, "gpu_launches": m["kernels"] * args.steps, "clocks": m["clocks"],
+            "rows_read_per_step": m["rows_read"], "rows_total": int(w["T"]),
+            "blocks_per_request": m["blocks_per_request"]}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(w, dev, args)
+    if rank == 0 and world == 1 and not args.no_per_config and not filtered:
+        line["per_config"] = per_config(args, dev, peak, peak_kind)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_seconds=0.0):
+    """One sampler call per step over workload w (inputs resident in HBM).  Times `steps` plain
+    calls with CUDA events on the launching stream (at least `min_seconds` of them when that is
+    set), then the same number of calls through the stage-event entry for each kernel's own
+    time.  Returns the times, the call's algorithmic bytes (rows read up to each output row,
+    the draft rows of explicit-q rejections, the small arrays) and the launch shape."""
+    import torch
+    from speculative_decoding_rejection_spec_gb300 import binding
     d = binding.to_device(w, dev)
     has_q = d["draft_probs"] is not None
     dt = binding.BF16 if w["dtype"] == "bf16" else binding.F32
     buf = binding.make_buffers(w["B"], w["T"], w["V"], dt, has_q, dev)
     tk = None if w.get("top_k") is None else torch.from_numpy(w["top_k"]).to(dev)
     tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).to(dev)
+    filtered = tk is not None or tp is not None
     nk = binding.num_kernels(w["B"], has_q, filtered, dt)
     lazy = binding.reads_to_first_rejection(w["B"], filtered, dt)
     stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    call = lambda: binding.sample_profiled(d, buf, [], stream, tk, tp)
+    for _ in range(warmup):
+        call()
+    st, bits, _ = binding.last_device_error(buf.workspace)
+    if st != 0:
+        raise SystemExit(f"device input error bits {bits}")
+    torch.cuda.synchronize()
+    # inputs smaller than twice the L2 cache: flush it before every timed call (a write of a
+    # buffer larger than L2, outside the events), so that no call reads what the last one left
+    in_bytes = sum(t.numel() * t.element_size() for t in d.values() if t is not None)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev) if in_bytes < 2 * l2 else None
+    if min_seconds > 0:  # enough calls to fill the requested time
+        t0 = time.perf_counter()
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 5
+        steps = max(steps, min(20000, int(min_seconds / max(per, 1e-6))))
+    clocks = clock_sampler(dev)
+    if barrier:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    if flush is None:
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        total_ms = start.elapsed_time(stop)
+    else:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in pairs:
+            flush.zero_()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(a.elapsed_time(b) for a, b in pairs)
+    clk = clocks.stop()
+    if barrier:
+        torch.distributed.barrier()
+    # per-kernel times: the same calls with an event after each kernel
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(min(steps, 200))]
     for row in ev:
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-
-    for _ in range(args.warmup):
-        binding.sample_profiled(d, buf, [], stream, tk, tp)
-    st, bits, _ = binding.last_device_error(buf.workspace)
-    if st != 0:
-        raise SystemExit(f"device input error bits {bits}")
-
-    sampler = ClockSampler(dev.index or 0)
-    if world > 1:
-        torch.distributed.barrier()
+    for row in ev:
+        if flush is not None:
+            flush.zero_()
+        binding.sample_profiled(d, buf, row, stream, tk, tp)
     torch.cuda.synchronize()
-    sampler.start()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        binding.sample_profiled(d, buf, ev[i], stream, tk, tp)
-    stop.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms = total_ms / args.steps
     stage_ms = [statistics.mean(row[i].elapsed_time(row[i + 1]) for row in ev) for i in range(nk)]
-    positions = W.total_drafts(w)
-    value = positions * world / (ms / 1e3)
 
     es = 2 if w["dtype"] == "bf16" else 4
     acc = buf.out_num_accepted.cpu().numpy()
@@ -485,57 +625,67 @@ def main():
     valid = acc >= 0
     rejecting = int((valid & (acc < ks)).sum()) if has_q else 0
     small = 8 * (w["T"] - w["B"]) + 12 * w["T"] + 4 * (2 * w["B"] + 1)
-    all_rows_bytes = w["T"] * w["V"] * es + rejecting * w["V"] * 4 + small  # every target row once
-    peak, peak_kind = peaks()
-    if not lazy:
-        # K1 reads every target row (and with cuts, the cut kernel re-reads the filtered ones)
-        stages = (["rowstats"] + (["topk_topp_cut"] if filtered else []) + ["finalize"]
-                  + (["residual"] if has_q else []))
+    if lazy:
+        rows_read = int((acc[valid] + 1).sum())
+        stages = ["layout_check", "rows_to_first_rejection"]
+        dom = 1
+        dom_bytes = rows_read * w["V"] * es + rejecting * w["V"] * 4 + small
+        bpr = binding.blocks_per_request(w["B"], w["V"], dt) if not filtered else 1
+        dom_name = ("KL: lazy_kernel (request queue; rows streamed through warp-private TMA rings up to the first "
+                    "rejection; residual pass and draw in the same block" +
+                    (f"; each request split over a cluster of {bpr} blocks" if bpr > 1 else "") + ")")
+        if filtered:
+            dom_name += "; each reached row cut in the block (key-offset counts, per-chunk partials)"
+        alg = dom_bytes
+    else:
+        rows_read = int(w["T"])
+        stages = (["rowstats"] + (["topk_topp_cut"] if filtered else []) + ["finalize"] + (["residual"] if has_q else []))
         dom = 0
         dom_bytes = w["T"] * w["V"] * es + 4 * (w["T"] - w["B"])
         dom_name = "row statistics (K1: rowstats_wr_kernel, warp-private TMA pipelines)"
-        traffic = traffic_for(args.workload + (f"+k{args.top_k}+p{args.top_p}" if filtered else ""))
-        call_bytes = all_rows_bytes
-    else:
-        # KL reads each request's target rows up to its output row (the first rejection, or the
-        # bonus row) and, on an explicit-q rejection, that draft row
-        stages = ["layout_check", "rows_to_first_rejection"]
-        dom = 1
-        rows_read = int((acc[valid] + 1).sum())
-        dom_bytes = rows_read * w["V"] * es + rejecting * w["V"] * 4 + small
-        dom_name = ("KL: lazy_kernel (request queue, rows streamed through warp-private TMA rings up to "
-                    "the first rejection, draw in the same block)")
-        if filtered:
-            dom_name += "; each reached row cut in the block (key-offset counts, per-chunk partials)"
-        traffic = traffic_lazy_for(args.workload + (f"+k{args.top_k}+p{args.top_p}" if filtered else ""))
-        call_bytes = dom_bytes
-    dom_s = statistics.mean(row[dom].elapsed_time(row[dom + 1]) for row in ev) / 1e3
-    achieved = dom_bytes / dom_s / 1e9
-    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
-                "algorithmic_bytes_per_launch": dom_bytes, "ms_per_launch": round(1e3 * dom_s, 4),
-                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+        bpr = 0
+        alg = w["T"] * w["V"] * es + rejecting * w["V"] * 4 + small
+    out = {"total_ms": total_ms, "steps": steps, "stage_ms": stage_ms, "stages": stages, "dom": dom,
+           "l2": ("L2 flushed before every call (inputs smaller than twice L2)" if flush is not None
+                  else "inputs larger than twice L2 (no flush)"),
+           "dom_bytes": dom_bytes, "dom_name": dom_name, "alg_bytes": alg, "rows_read": rows_read,
+           "kernels": nk, "clocks": clk, "lazy": lazy, "blocks_per_request": bpr}
+    del d, buf
+    torch.cuda.empty_cache()
+    return out
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
-            "hbm_gbs_effective": round(call_bytes / (ms / 1e3) / 1e9, 1),
-            "all_rows_gbs_equivalent": round(all_rows_bytes / (ms / 1e3) / 1e9, 1),
-            "stage_ms": [round(x, 4) for x in stage_ms], "stages": stages,
-            "rows_per_s": w["T"] * world / (ms / 1e3),
-            "roofline": roofline, "gpu_launches": nk * args.steps, "clocks": clocks}
-    if lazy:
-        line["rows_read_per_step"] = rows_read
-        line["rows_total"] = int(w["T"])
 
-    if not args.no_e2e:
-        line["e2e"] = e2e(w, dev, args)
-    if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(w)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+def roofline_of(m, peak, peak_kind, workload_key):
+    dom_ms = m["stage_ms"][m["dom"]]
+    achieved = m["dom_bytes"] / (dom_ms / 1e3) / 1e9
+    traffic = traffic_lazy_for(workload_key) if m["lazy"] else traffic_for(workload_key)
+    return {"bound": "hbm", "kernel": m["dom_name"], "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
+            "algorithmic_bytes_per_launch": m["dom_bytes"], "ms_per_launch": round(dom_ms, 4),
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+
+
+PER_CONFIG = ["tiny", "greedy", "probabilistic", "deterministic", "large-128", "large-512"]
+
+
+def per_config(args, dev, peak, peak_kind):
+    """The other workloads of the target's config list, measured in the same run (each for
+    about half a second of calls): step time, the dominant kernel and its roofline fraction."""
+    from speculative_decoding_rejection_spec_gb300 import workloads as W
+    out = {}
+    for name in PER_CONFIG:
+        w = W.generate(name)
+        m = measure(w, dev, 20, max(args.warmup, 3), min_seconds=0.5)
+        ms = m["total_ms"] / m["steps"]
+        rf = roofline_of(m, peak, peak_kind, name)
+        out[name] = {"ms_per_step": round(ms, 5), "value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT,
+                     "steps": m["steps"], "kernel": rf["kernel"], "kernel_ms": rf["ms_per_launch"],
+                     "algorithmic_bytes": m["dom_bytes"], "achieved_gbs": rf["achieved"], "frac": rf["frac"],
+                     "frac_of_nominal_8tbs": rf["frac_of_nominal_8tbs"], "traffic": rf["traffic"],
+                     "rows_read": m["rows_read"], "rows_total": int(w["T"]),
+                     "blocks_per_request": m["blocks_per_request"], "stage_ms": [round(x, 4) for x in m["stage_ms"]],
+                     "l2": m["l2"], "clocks": m["clocks"]}
+    return out
 
 
 def e2e(w, dev, args):

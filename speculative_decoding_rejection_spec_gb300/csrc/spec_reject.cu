@@ -1923,9 +1923,15 @@ template <int DT> __device__ __noinline__ void kl_cut_row(const CutDims P, CutSm
 }
 
 
+// Programmatic dependent launch: KL may be scheduled while the layout check still runs; it
+// waits here for that kernel's writes (the error word, the request queue) before reading them.
+__device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Layout check and request-queue reset before KL (one block).
 __global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
 {
+    allow_dependents();
     validate_layout(P);
     if (threadIdx.x == 0)
         P.err[2] = 0;  // next request to hand out
@@ -1997,6 +2003,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     float2 *const lpart = in_block<CS>(spart, 0u);  // the leader's chunk partials
     float *const lrm = in_block<CS>(srm, 0u);       // and residual masses
 
+    wait_for_prerequisite();
     if (P.err[0] & SPEC_DEVERR_LAYOUT) {  // the whole batch is invalid (as K2 reports it)
         for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < P.B; r += gridDim.x * blockDim.x)
             P.out_acc[r] = -1;
@@ -2682,21 +2689,38 @@ cudaError_t g_dev_err[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
 
 // Launch of KL with clusters of CS blocks (CS > 1): one cluster per request at a time.
-template <int DT, int CS> cudaError_t launch_lazy_cluster(const Params &P, int clusters, cudaStream_t stream)
+// Launch of KL (any variant; clusters of CS blocks when CS > 1), after the layout check: with
+// `pdl` as a programmatic dependent launch (the kernel waits for the check's writes itself).
+template <class K>
+cudaError_t launch_lazy(K kernel, int grid, int cs, size_t smem, const Params &P, bool pdl, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(clusters * CS), 1, 1);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kLThreads, 1, 1);
-    cfg.dynamicSmemBytes = kLSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cs > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cs;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lazy_kernel<DT, false, false, CS>, P);
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+template <int DT, int CS> cudaError_t launch_lazy_cluster(const Params &P, int clusters, bool pdl, cudaStream_t stream)
+{
+    return launch_lazy(lazy_kernel<DT, false, false, CS>, clusters * CS, CS, kLSmem, P, pdl, stream);
 }
 
 // Clusters of CS blocks of KL that fit on the device at once (whole GPU).
@@ -2979,6 +3003,8 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         di->blocks_lazy[DT] > 0) {
         mark();
         lazy_init_kernel<<<1, 256, 0, stream>>>(P);
+        // the pass follows as a programmatic dependent launch unless a stage event separates them
+        const bool pdl = !(evi < nev && ev[evi]);
         mark();
         if (rows_in_host) {
             // the rows it reads over the host link are copied to device memory for the cut, the
@@ -2989,12 +3015,11 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         if (filtered) {
             const int gridL =
                 (int)clamp_grid((int64_t)di->sms * (rows_in_host ? di->blocks_lazy_cut_host : di->blocks_lazy_cut), B);
-            if (rows_in_host)
-                lazy_kernel<1, true, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
-            else
-                lazy_kernel<1, false, true><<<gridL, kLThreads, kLCutSmem, stream>>>(P);
+            const cudaError_t e = rows_in_host
+                                      ? launch_lazy(lazy_kernel<1, true, true>, gridL, 1, kLCutSmem, P, pdl, stream)
+                                      : launch_lazy(lazy_kernel<1, false, true>, gridL, 1, kLCutSmem, P, pdl, stream);
             mark();
-            return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+            return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
         }
         const int gridL = (int)clamp_grid((int64_t)di->sms * di->blocks_lazy[DT], B);
         if (!rows_in_host) {
@@ -3007,28 +3032,26 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 const int ncl = (int)clamp_grid(di->clusters_lazy[DT][ci], B);
                 cudaError_t e;
                 if (DT)
-                    e = ci == 1 ? launch_lazy_cluster<1, 2>(P, ncl, stream)
-                                : ci == 2 ? launch_lazy_cluster<1, 4>(P, ncl, stream) : launch_lazy_cluster<1, 8>(P, ncl, stream);
+                    e = ci == 1 ? launch_lazy_cluster<1, 2>(P, ncl, pdl, stream)
+                                : ci == 2 ? launch_lazy_cluster<1, 4>(P, ncl, pdl, stream)
+                                          : launch_lazy_cluster<1, 8>(P, ncl, pdl, stream);
                 else
-                    e = ci == 1 ? launch_lazy_cluster<0, 2>(P, ncl, stream)
-                                : ci == 2 ? launch_lazy_cluster<0, 4>(P, ncl, stream) : launch_lazy_cluster<0, 8>(P, ncl, stream);
+                    e = ci == 1 ? launch_lazy_cluster<0, 2>(P, ncl, pdl, stream)
+                                : ci == 2 ? launch_lazy_cluster<0, 4>(P, ncl, pdl, stream)
+                                          : launch_lazy_cluster<0, 8>(P, ncl, pdl, stream);
                 mark();
                 return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
             }
         }
-        if (rows_in_host) {
-            if (DT)
-                lazy_kernel<1, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
-            else
-                lazy_kernel<0, true, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
-        } else {
-            if (DT)
-                lazy_kernel<1, false, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
-            else
-                lazy_kernel<0, false, false><<<gridL, kLThreads, kLSmem, stream>>>(P);
-        }
+        cudaError_t e;
+        if (rows_in_host)
+            e = DT ? launch_lazy(lazy_kernel<1, true, false>, gridL, 1, kLSmem, P, pdl, stream)
+                   : launch_lazy(lazy_kernel<0, true, false>, gridL, 1, kLSmem, P, pdl, stream);
+        else
+            e = DT ? launch_lazy(lazy_kernel<1, false, false>, gridL, 1, kLSmem, P, pdl, stream)
+                   : launch_lazy(lazy_kernel<0, false, false>, gridL, 1, kLSmem, P, pdl, stream);
         mark();
-        return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+        return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
     }
     if (rows_in_host)
         return SPEC_ERR_INVALID_ARG;  // only the first-rejection pass reads rows in host memory
