@@ -570,10 +570,120 @@ def check_top_k_top_p(impl=None, N=300_000):
     return True, "ok"
 
 
+def _expected_margins(l32, temps, cu, ids, u, q):
+    """Per request, by numpy / scipy routines: the visited positions' smallest relative
+    acceptance margin |u*q* - p*| / max(p*, u*q*), the output row's sampling margin
+    min(theta - C(v-1), C(v) - theta) / Z with C = cumsum(residual), v = searchsorted(C,
+    theta, side='right'), theta = u_s * Z, and whether that row is an explicit-q residual."""
+    B = len(cu) - 1
+    out = []
+    for r in range(B):
+        k = int(cu[r + 1] - cu[r])
+        tb, db = int(cu[r]) + r, int(cu[r])
+        p_rows = special.softmax(l32[tb:tb + k + 1].astype(np.float64) / np.float64(np.float32(temps[r])), axis=1)
+        acc_m, j = np.inf, k
+        for i in range(k):
+            x = int(ids[db + i])
+            qs = np.float64(q[db + i, x]) if q is not None else 1.0
+            lhs, rhs = np.float64(u[tb + i, 0]) * qs, p_rows[i, x]
+            big = max(lhs, rhs)
+            if big > 0:
+                acc_m = min(acc_m, abs(lhs - rhs) / big)
+            if not lhs < rhs:
+                j = i
+                break
+        p = p_rows[j]
+        explicit = q is not None and j < k
+        if j < k:
+            res = np.maximum(p - q[db + j].astype(np.float64), 0.0) if q is not None else p.copy()
+            if q is None:
+                res[int(ids[db + j])] = 0.0
+        else:
+            res = p
+        C = np.cumsum(res)
+        Z = C[-1]
+        theta = np.float64(u[tb + j, 1]) * Z
+        v = int(np.searchsorted(C, theta, side="right"))
+        lo = C[v - 1] if v > 0 else 0.0
+        smp = min(theta - lo, C[v] - theta) / Z
+        out.append((j, acc_m, smp, explicit, smp * Z))
+    return out
+
+
+def check_margins_and_flags(impl=None):
+    """The oracle's near-boundary report, which decides which GPU requests may differ: its
+    margins against an independent numpy recomputation (1e-12), and its flags against the bands
+    applied to those margins, on 8- and 16-token rows with decisions planted near a boundary."""
+    rng = np.random.default_rng(1500)
+    for V, explicit in ((8, True), (16, True), (8, False), (16, False)):
+        B = 48
+        ks = rng.integers(0, 4, size=B)
+        cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+        T = int(cu[-1]) + B
+        l32 = (rng.standard_normal((T, V)) * 1.5).astype(np.float32)
+        temps = rng.choice([0.7, 1.0, 1.3], size=B).astype(np.float32)
+        q = None
+        if explicit:
+            q = rng.random((T - B, V)) ** 2
+            q = (q / q.sum(axis=1, keepdims=True)).astype(np.float32)
+        ids = np.array([rng.choice(V, p=(q[d] / q[d].sum()) if q is not None else None) for d in range(T - B)],
+                       np.int32)
+        u = rng.random((T, 2)).astype(np.float32)
+        # plant near-boundary decisions: for every third request, position 0's coin a relative
+        # 3e-6 from p / q (inside the 1e-5 band); for every fourth, the output row's draw a
+        # relative 2e-6 from a CDF boundary
+        pre = _expected_margins(l32, temps, cu, ids, u, q)
+        for r in range(B):
+            tb, db, k = int(cu[r]) + r, int(cu[r]), int(ks[r])
+            if r % 3 == 0 and k > 0:
+                p0 = special.softmax(l32[tb].astype(np.float64) / np.float64(temps[r]))
+                x = int(ids[db])
+                qs = float(q[db, x]) if q is not None else 1.0
+                target = p0[x] / qs * (1 + (3e-6 if r % 2 else -3e-6))
+                if target < 1:
+                    u[tb, 0] = np.float32(target)
+        mid = _expected_margins(l32, temps, cu, ids, u, q)
+        for r in range(B):
+            if r % 4 == 1:
+                j = mid[r][0]
+                tb, db, k = int(cu[r]) + r, int(cu[r]), int(ks[r])
+                p = special.softmax(l32[tb + j].astype(np.float64) / np.float64(temps[r]))
+                res = p if j == k else (np.maximum(p - q[db + j], 0.0) if q is not None else p.copy())
+                if q is None and j < k:
+                    res[int(ids[db + j])] = 0.0
+                C = np.cumsum(res)
+                b = min(V - 2, int(rng.integers(0, V - 1)))
+                if C[-1] > 0 and 0 < C[b] < C[-1]:
+                    u[tb + j, 1] = np.float32(C[b] / C[-1] * (1 + 2e-6))
+        want = _expected_margins(l32, temps, cu, ids, u, q)
+        res = oracle.reject_sample(l32, ids, cu, u, temps, q, debug=True, impl=impl)
+        near_acc = near_smp = 0
+        for r, (j, am, sm, expl, sabs) in enumerate(want):
+            if res.num_accepted[r] != j:
+                return False, f"V={V} request {r}: accepted {res.num_accepted[r]}, expected {j}"
+            got_a, got_s = float(res.margin[r, 0]), float(res.margin[r, 1])
+            if (np.isinf(am) != np.isinf(got_a)) or (np.isfinite(am) and abs(got_a - am) > 1e-12):
+                return False, f"V={V} request {r}: acceptance margin {got_a} vs {am}"
+            if abs(got_s - sm) > 1e-12:
+                return False, f"V={V} request {r}: sampling margin {got_s} vs {sm}"
+            f = int(res.flags[r])
+            if bool(f & oracle.NEAR_ACCEPT) != (am <= 1e-5):
+                return False, f"V={V} request {r}: acceptance flag {f} for margin {am}"
+            if bool(f & oracle.NEAR_SAMPLE) != (sm <= 1e-5):
+                return False, f"V={V} request {r}: sampling flag {f} for margin {sm}"
+            if bool(f & oracle.NEAR_SAMPLE_ABS) != (expl and sabs <= 2e-6):
+                return False, f"V={V} request {r}: absolute flag {f} for margin {sabs}"
+            near_acc += am <= 1e-5
+            near_smp += sm <= 1e-5
+        if near_acc < 3 or near_smp < 3:
+            return False, f"V={V}: too few planted near-boundary decisions ({near_acc}, {near_smp})"
+    return True, "ok"
+
+
 ALL_CHECKS = [
     check_output_distribution, check_acceptance_rate, check_residual_mass, check_accepted_length,
     check_exact_enumeration, check_q_equals_p, check_disjoint_supports, check_one_hot_draft,
     check_greedy_worked_chain, check_rollback_arithmetic, check_greedy_ties_and_bonus, check_zero_drafts,
     check_extreme_uniforms, check_row_statistics, check_invalid_inputs, check_degenerate_residual,
-    check_top_k_top_p,
+    check_top_k_top_p, check_margins_and_flags,
 ]

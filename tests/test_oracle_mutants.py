@@ -32,6 +32,10 @@ MUTANTS = {
                                  "} else {\n                    for (int32_t v = 0; v < V; ++v)\n                        r[v] = p[v];\n                    r[draft_ids[db + j - 1 > 0 ? db + j - 1 : 0]] = 0.0;\n                }"),
     "greedy_tie_last_index": ("if (l > bv) {", "if (l >= bv) {"),
     "degenerate_residual_ignored": ("if (Z > 0.0) {", "if (1) {"),
+    # the near-boundary report that excuses GPU mismatches
+    "sampling_margin_one_side_only": ("*margin = a < b ? a : b;", "*margin = b;"),
+    "acceptance_margin_unscaled": ("if (big > 0.0 && fabs(lhs - rhs) / big < margin_accept)\n                    margin_accept = fabs(lhs - rhs) / big;",
+                                   "if (big > 0.0 && fabs(lhs - rhs) < margin_accept)\n                    margin_accept = fabs(lhs - rhs);"),
 }
 
 # smaller statistical checks keep the mutant run short
@@ -43,7 +47,7 @@ FAST_CHECKS = [
     P.check_exact_enumeration, P.check_q_equals_p, P.check_disjoint_supports, P.check_one_hot_draft,
     P.check_greedy_worked_chain, P.check_rollback_arithmetic, P.check_greedy_ties_and_bonus, P.check_zero_drafts,
     P.check_extreme_uniforms, P.check_row_statistics, P.check_invalid_inputs, P.check_degenerate_residual,
-    P.check_top_k_top_p,
+    P.check_top_k_top_p, P.check_margins_and_flags,
 ]
 
 
