@@ -752,6 +752,25 @@ template <int DT, bool F> struct TargetMass {
         }
         return ((s[0] + s[1]) + (s[2] + s[3])) + scalar_sum(*this, v, v1);
     }
+    // Masses of the 32 bytes of logits from element v0 (16 bf16 / 8 fp32 tokens) with two
+    // 16-byte loads; vec_ok(v0) says whether those loads are aligned.
+    static constexpr int kSpan = 32 / Elem<DT>::kSize;
+    __device__ __forceinline__ bool vec_ok(int64_t v0) const
+    {
+        return ((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize)) & 15) == 0;
+    }
+    __device__ __forceinline__ void span(int64_t v0, float (&w)[kSpan]) const
+    {
+        constexpr int VEC = Elem<DT>::kVec;
+        const uint4 *p = reinterpret_cast<const uint4 *>(row + v0 * Elem<DT>::kSize);
+        const uint4 a = __ldg(p), b = __ldg(p + 1);
+        float x[2 * VEC];
+        unpack<DT>(a, x);
+        unpack<DT>(b, x + VEC);
+#pragma unroll
+        for (int e = 0; e < kSpan; ++e)
+            w[e] = (v0 + e == excl || !kept<DT, F>(x[e], thr)) ? 0.f : ex2(fmaf(x[e], cs, -M));
+    }
 };
 
 // Explicit-q residual mass r(v) = max(0, 2^(l_v c - M) / S - q(v)) in probability units.
@@ -791,6 +810,34 @@ template <int DT, bool F> struct ResidualMass {
             }
         }
         return ((s[0] + s[1]) + (s[2] + s[3])) + scalar_sum(*this, v, v1);
+    }
+    static constexpr int kSpan = 32 / Elem<DT>::kSize;
+    __device__ __forceinline__ bool vec_ok(int64_t v0) const
+    {
+        return (((reinterpret_cast<uintptr_t>(row + v0 * Elem<DT>::kSize)) | reinterpret_cast<uintptr_t>(qrow + v0)) &
+                15) == 0;
+    }
+    __device__ __forceinline__ void span(int64_t v0, float (&w)[kSpan]) const
+    {
+        constexpr int VEC = Elem<DT>::kVec;
+        const uint4 *p = reinterpret_cast<const uint4 *>(row + v0 * Elem<DT>::kSize);
+        const uint4 a = __ldg(p), b = __ldg(p + 1);
+        float x[2 * VEC];
+        unpack<DT>(a, x);
+        unpack<DT>(b, x + VEC);
+        const float4 *q4 = reinterpret_cast<const float4 *>(qrow + v0);
+        float qv[kSpan];
+#pragma unroll
+        for (int h = 0; h < kSpan / 4; ++h) {
+            const float4 t = __ldg(q4 + h);
+            qv[4 * h + 0] = t.x;
+            qv[4 * h + 1] = t.y;
+            qv[4 * h + 2] = t.z;
+            qv[4 * h + 3] = t.w;
+        }
+#pragma unroll
+        for (int e = 0; e < kSpan; ++e)
+            w[e] = fmaxf(0.f, pm(x[e]) - qv[e]);
     }
 };
 
@@ -837,6 +884,111 @@ __device__ int64_t warp_find(const F &f, int64_t lo, int64_t hi, float theta, in
         return lo + (__ffs(hit) - 1);
     const unsigned pos = __ballot_sync(kFull, w > 0.f);
     return pos ? lo + (31 - __clz(pos)) : hi - 1;
+}
+
+// ---- the same search by a whole block (all threads call it; blockDim.x threads, at most 32
+// warps).  Thread i owns the kSpan tokens [lo + i * kSpan, ...) of the range (a chunk: at
+// most blockDim.x * kSpan tokens), loads them at once (two 16-byte loads of logits), and a
+// block scan over the threads' totals finds the thread whose tokens hold theta; that thread
+// finishes the search in registers.  One round trip to memory instead of one per level.
+struct BlockSearch {
+    float wsum[32];
+    int hit_thread;
+    int pos_thread;
+    int64_t token;
+};
+
+template <class F>
+__device__ __noinline__ int64_t block_find(const F &f, int64_t lo, int64_t hi, float theta, BlockSearch &S)
+{
+    constexpr int N = F::kSpan;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
+    const int64_t s0 = lo + (int64_t)tid * N;
+    float w[N];
+    if (s0 + N <= hi && f.vec_ok(s0)) {
+        f.span(s0, w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            w[e] = (s0 + e < hi) ? f.one(s0 + e) : 0.f;
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        tot += w[e];
+    float incl = warp_incl_scan(tot, lane);
+    if (lane == 31)
+        S.wsum[warp] = incl;
+    if (tid == 0) {
+        S.hit_thread = INT_MAX;
+        S.pos_thread = -1;
+    }
+    __syncthreads();
+    float base = 0.f;
+    for (int k = 0; k < warp; ++k)
+        base += S.wsum[k];
+    incl += base;
+    const unsigned hit = __ballot_sync(kFull, incl > theta);
+    const unsigned pos = __ballot_sync(kFull, tot > 0.f);
+    if (lane == 0) {
+        if (hit)
+            atomicMin(&S.hit_thread, warp * 32 + __ffs(hit) - 1);
+        if (pos)
+            atomicMax(&S.pos_thread, warp * 32 + 31 - __clz(pos));
+    }
+    __syncthreads();
+    const int h = S.hit_thread;
+    if (h != INT_MAX ? tid == h : tid == S.pos_thread) {
+        int64_t tok = -1, last = -1;
+        float c = incl - tot;
+        const float th = h != INT_MAX ? theta : INFINITY;  // rounding left theta beyond the total
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            if (w[e] > 0.f)
+                last = s0 + e;
+            c += w[e];
+            if (tok < 0 && c > th)
+                tok = s0 + e;
+        }
+        S.token = tok >= 0 ? tok : (last >= 0 ? last : hi - 1);
+    }
+    if (h == INT_MAX && S.pos_thread < 0 && tid == 0)
+        S.token = hi - 1;
+    __syncthreads();
+    const int64_t tok = S.token;
+    __syncthreads();  // S is reused by the caller's next search
+    (void)nw;
+    return tok;
+}
+
+// Total mass of [lo, hi) by a whole block (thread i: kSpan tokens from lo + i * kSpan).
+template <class F> __device__ __noinline__ float block_range_mass(const F &f, int64_t lo, int64_t hi, BlockSearch &S)
+{
+    constexpr int N = F::kSpan;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
+    float tot = 0.f;
+    for (int64_t s0 = lo + (int64_t)tid * N; s0 < hi; s0 += (int64_t)blockDim.x * N) {
+        float w[N];
+        if (s0 + N <= hi && f.vec_ok(s0)) {
+            f.span(s0, w);
+        } else {
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+                w[e] = (s0 + e < hi) ? f.one(s0 + e) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            tot += w[e];
+    }
+    tot = warp_sum(tot);
+    if (lane == 0)
+        S.wsum[warp] = tot;
+    __syncthreads();
+    float z = 0.f;
+    for (int k = 0; k < nw; ++k)
+        z += S.wsum[k];
+    __syncthreads();
+    return z;
 }
 
 // Masses of the chunks of row t relative to 2^M (K1 partials), one chunk optionally

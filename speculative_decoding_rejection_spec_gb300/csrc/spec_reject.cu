@@ -1995,6 +1995,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     __shared__ float srm[kLMaxChunks];     // residual chunk masses (explicit q)
     __shared__ int s_r, s_go, s_abort;
     __shared__ float s_M, s_S;
+    __shared__ BlockSearch bsearch;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const unsigned rank = cluster_rank<CS>();
     const bool leader = rank == 0;
@@ -2083,7 +2084,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 C.thr = 0;
             }
         // inputs of the acceptance test of draft position `lane` (warp 0), issued first
-        float ls = 0.f, qs = 1.f, ua = 0.f, usl = 0.f;
+        float ls = 0.f, qs = 1.f, ua = 0.f;
         if (leader && warp == 0 && !greedy) {
             if (lane < k) {
                 ls = load1<DT>(row_ptr<DT>(P, tb + lane), xs);
@@ -2091,10 +2092,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     qs = __ldg(P.q + (db + lane) * P.qstride + xs);
                 ua = P.uni[2 * (tb + lane)];
             }
-            if (lane <= k)
-                usl = P.uni[2 * (tb + lane) + 1];  // the sampling draw, wherever the output lands
         }
-        const float us32 = (leader && warp == 0 && !greedy && k == 32) ? P.uni[2 * (tb + 32) + 1] : 0.f;
 
         int j = k;       // output position: the first rejection, else the bonus row
         int am = 0;      // argmax of the latest row (greedy)
@@ -2269,10 +2267,12 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             }
             cluster_barrier<CS>();
         }
-        if (leader && warp == 0) {
-            const float us = greedy ? 0.f : (j < 32 ? __shfl_sync(kFull, usl, j & 31) : us32);
+        if (leader) {
+            // the draw, by the whole block: chunk masses scanned by every warp alike (smem), the
+            // chunk searched by all threads at once (block_find: one round trip to memory)
+            const float us = greedy ? 0.f : __ldg(P.uni + 2 * tj + 1);
             if (greedy) {
-                token = am;  // the argmax of row t_j: the first mismatch, or the bonus row
+                token = am;  // warp 0: the argmax of row t_j, the first mismatch or the bonus row
             } else if (j == k) {  // bonus: draw from p
                 float M, S;
                 warp_combine_soft(spart, P.nchunks, cs, lane, M, S);
@@ -2281,15 +2281,15 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
                 TargetMass<DT, CUT> f{rowj, cs, M, -1, thr};
-                token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
-                                       lane);
+                token = (int)block_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
+                                        bsearch);
             } else if (!residual) {  // one-hot draft: residual = p without x*
-                const float Mj = Mi;
+                const float Mj = s_M;
                 const int xj = __shfl_sync(kFull, xs, j & 31);
                 const int cx = xj / P.chunk;
                 TargetMass<DT, CUT> fx{rowj, cs, Mj, xj, thr};
-                const float mx = warp_range_mass(fx, (int64_t)cx * P.chunk,
-                                                 min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), lane);
+                const float mx = block_range_mass(fx, (int64_t)cx * P.chunk,
+                                                  min((int64_t)P.V, (int64_t)(cx + 1) * P.chunk), bsearch);
                 ChunkMassFromPartials cm{spart, cs, Mj, cx, mx};
                 float Z = chunk_total(cm, P.nchunks, lane);
                 int64_t excl = xj;
@@ -2301,8 +2301,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 float th;
                 const int c = chunk_locate(cm, P.nchunks, us * Z, lane, th);
                 TargetMass<DT, CUT> f{rowj, cs, Mj, excl, thr};
-                token = (int)warp_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
-                                       lane);
+                token = (int)block_find(f, (int64_t)c * P.chunk, min((int64_t)P.V, (int64_t)(c + 1) * P.chunk), th,
+                                        bsearch);
             } else {  // explicit q: locate in the residual (K3)
                 const float Mj = s_M, Sj = s_S;
                 const ChunkMassFromShared cmz{srm};
@@ -2312,18 +2312,20 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                     const int cc = chunk_locate(cmz, P.nchunks, us * Z, lane, th);
                     const ResidualMass<DT, CUT> f{rowj, qstage_j ? qstage_j : P.q + (db + j) * P.qstride, cs, Mj,
                                                   1.f / Sj, thr};
-                    token = (int)warp_find(f, (int64_t)cc * P.chunk,
-                                           min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
+                    token = (int)block_find(f, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk),
+                                            th, bsearch);
                 } else {  // empty residual: draw from p itself
                     const ChunkMassFromPartials cm{spart, cs, Mj, -1, 0.f};
                     const float Zp = chunk_total(cm, P.nchunks, lane);
                     float th;
                     const int cc = chunk_locate(cm, P.nchunks, us * Zp, lane, th);
                     const TargetMass<DT, CUT> ft{rowj, cs, Mj, -1, thr};
-                    token = (int)warp_find(ft, (int64_t)cc * P.chunk,
-                                           min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk), th, lane);
+                    token = (int)block_find(ft, (int64_t)cc * P.chunk, min((int64_t)P.V, (int64_t)(cc + 1) * P.chunk),
+                                            th, bsearch);
                 }
             }
+        }
+        if (leader && warp == 0) {
             // ---- outputs
             if (lane == 0)
                 P.out_acc[r] = j;

@@ -149,6 +149,24 @@ def assert_both_paths(w, ref=None, max_mismatch_frac=0.01, rowstats=True):
     prod = run_gpu(w)
     assert prod["status"] == full["status"] and prod["bits"] == full["bits"]
     assert_parity(w, prod, ref, max_mismatch_frac=max_mismatch_frac)
-    assert np.array_equal(prod["tokens"], full["tokens"]) and np.array_equal(prod["acc"], full["acc"]), \
-        f"{w['name']}: the two passes differ"
+    assert_same_unflagged(w, prod, full, ref)
     return c, prod, full, ref
+
+
+def assert_same_unflagged(w, a, b, ref=None):
+    """Two GPU runs of the same batch agree on every request the oracle does not flag.  The two
+    passes take every decision with the same arithmetic except the draw's search inside the
+    located chunk (the first-rejection pass sums the chunk in 256 segments by a whole block,
+    the full pass in 32 segments by one warp), so they may differ only on draws the oracle
+    flags as within the near-boundary band."""
+    ref = ref if ref is not None else oracle.reject_sample_workload(w, debug=True)
+    flagged = (ref.flags & (oracle.NEAR_ANY | oracle.NONFINITE)) != 0
+    cu = w["cu_num_draft"]
+    diff = []
+    for r in range(w["B"]):
+        lo, hi = int(cu[r]) + r, int(cu[r + 1]) + r + 1
+        if a["acc"][r] != b["acc"][r] or not np.array_equal(a["tokens"][lo:hi], b["tokens"][lo:hi]):
+            diff.append(r)
+    bad = [r for r in diff if not flagged[r]]
+    assert not bad, f"{w['name']}: the two passes differ on unflagged requests {bad[:5]}"
+    return diff

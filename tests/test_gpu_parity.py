@@ -75,7 +75,7 @@ def test_production_entry_matches_diagnostic_entry():
     w = W.generate("probabilistic", B=8)
     a = PT.run_gpu(w)
     b = PT.run_gpu(w, debug=True)
-    assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["acc"], b["acc"])
+    PT.assert_same_unflagged(w, a, b)
 
 
 def test_deterministic_repeat():
@@ -260,7 +260,7 @@ def test_device_errors_layout(which):
 def test_first_rejection_pass_device_errors_per_request(draft):
     """The same per-request errors on a batch that takes the first-rejection pass (B >= 64):
     k > 32 and an out-of-range draft id invalidate only their request; the rest match the full
-    pass bit for bit."""
+    pass on every request the oracle does not flag."""
     B = 70
     ks = [3] * B
     ks[5] = 33
@@ -274,7 +274,7 @@ def test_first_rejection_pass_device_errors_per_request(draft):
     for r in (5, 40):
         assert (tok[cu[r] + r:cu[r + 1] + r + 1] == -1).all()
     full = PT.run_gpu(w, debug=True)
-    assert np.array_equal(tok, full["tokens"]) and np.array_equal(acc, full["acc"])
+    PT.assert_same_unflagged(w, dict(tokens=tok, acc=acc), full)
     # the diagnostic entry's error word holds the same per-request errors (its extra argmax
     # pass over every row does not reset it)
     assert full["status"] == 5 and full["bits"] == bits and full["first"] == 5
@@ -381,14 +381,16 @@ def test_host_entry_reads_pinned_inputs_in_place(name):
 @pytest.mark.parametrize("name,over", [("tiny", dict(B=96)), ("greedy", {}), ("probabilistic", dict(B=80)),
                                        ("deterministic", {}), ("large-128", {})])
 def test_first_rejection_pass_equals_full_pass(name, over):
-    """Calls without cuts or diagnostics on 64 or more requests read each request's rows only up
+    """Calls without cuts or diagnostics read each request's rows only up
     to its first rejection (KL); the diagnostic entry still runs the full pass over every row
-    (K1, K2, K3).  Both take every decision with the same arithmetic, so the outputs are the same
-    bit for bit (fp32 and bf16 rows, explicit and one-hot drafts, greedy requests)."""
+    (K1, K2, K3).  Both take every decision with the same arithmetic and differ only in how the
+    draw searches inside the located chunk (a block's 256 segments against a warp's 32), so the
+    outputs agree on every request the oracle does not flag (fp32 and bf16 rows, explicit and
+    one-hot drafts, greedy requests), and the first-rejection pass matches the oracle."""
     w = W.generate(name, **over)
     lazy = PT.run_gpu(w)
     full = PT.run_gpu(w, debug=True)
-    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_same_unflagged(w, lazy, full)
     PT.assert_parity(w, lazy)
 
 
@@ -401,7 +403,7 @@ def test_first_rejection_pass_long_chains_and_counters():
                    name="long-chains")
     lazy = PT.run_gpu(w)
     full = PT.run_gpu(w, debug=True)
-    assert np.array_equal(lazy["tokens"], full["tokens"]) and np.array_equal(lazy["acc"], full["acc"])
+    PT.assert_same_unflagged(w, lazy, full)
     PT.assert_parity(w, lazy)
     assert (lazy["acc"] == K).any()  # q = p accepts every draft
     d = binding.to_device(w, "cuda")
@@ -423,8 +425,8 @@ def test_first_rejection_pass_long_chains_and_counters():
 ])
 def test_cluster_per_request_parity(name, over, blocks):
     """Batches too small to fill the GPU one block per request split each request's rows and
-    residual pass over a thread-block cluster; the outputs match the oracle and, bit for bit,
-    the full pass."""
+    residual pass over a thread-block cluster; the outputs match the oracle and, on every request
+    the oracle does not flag, the full pass."""
     import torch
     w = W.generate(name, **over) if name in W.CONFIGS else W.generate(over, name=name)
     got = binding.blocks_per_request(w["B"], w["V"], PT.dtype_code(w))
