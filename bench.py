@@ -44,6 +44,7 @@ UNIT = "draft positions/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_rejection_spec_gb300", "csrc", "spec_reject.cu")
+KERNEL_COMMON = os.path.join(ROOT, "speculative_decoding_rejection_spec_gb300", "csrc", "common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -61,16 +62,19 @@ def peaks():
 
 
 def source_sha(full=False):
-    """Hash of the kernel code: by default up to the end of the row-statistics kernel (K1 and
-    everything it can use are defined before that point; later code cannot change it), with
-    full=True the whole file.  Comments and blank space are left out (they compile to nothing),
-    so a recorded traffic figure stays valid until the code itself changes."""
+    """Hash of the kernel code: by default the shared device code (common.cuh) and the kernel
+    file up to the end of the row-statistics kernel (K1 and everything it can use are defined
+    before that point; later code cannot change it), with full=True both files whole.  Comments
+    and blank space are left out (they compile to nothing), so a recorded traffic figure stays
+    valid until the code itself changes."""
     import re
-    with open(KERNEL_SOURCE, "rb") as f:
-        src = f.read()
-    marker = b"// K1F: top-k / top-p cut"
-    cut = -1 if full else src.find(marker)
-    code = (src if cut < 0 else src[:cut]).decode()
+    parts = []
+    for path, whole in ((KERNEL_COMMON, True), (KERNEL_SOURCE, full)):
+        with open(path, "rb") as f:
+            src = f.read()
+        cut = -1 if whole else src.find(b"// K1F: top-k / top-p cut")
+        parts.append((src if cut < 0 else src[:cut]).decode())
+    code = "\n".join(parts)
     code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
     code = re.sub(r"//[^\n]*", " ", code)
     code = " ".join(code.split())

@@ -254,12 +254,13 @@ spec_status spec_reject_sample_ex(const void *target_logits, spec_dtype logits_d
  * Measurement form of spec_reject_sample() / spec_reject_sample_filtered() (top_k and top_p
  * may be NULL): identical work, plus cudaEventRecord of caller-created events (cudaEvent_t
  * handles) on `stream`: stage_events[0] before the first kernel, then one after each kernel
- * launched, in order.  Calls without cuts of at least 64 requests on 16-byte-aligned rows: the
- * layout check, then the pass that reads rows up to each first rejection and draws the
- * outputs.  Otherwise: row
- * statistics, the top-k / top-p cut (filtered calls only), the per-request finalize, the
- * residual / recovery pass (with draft_probs only).  Entries beyond num_events, or NULL
- * entries, are skipped.
+ * launched, in order.  Calls on 16-byte-aligned rows without cuts (any B >= 1), or with cuts on
+ * bf16 rows and at least 64 requests: the layout check, then the pass that reads rows up to
+ * each first rejection and draws the outputs (2 events after the first; with events the pass
+ * follows the check in plain stream order instead of as a programmatic dependent launch).
+ * Otherwise: row statistics, the top-k / top-p cut (filtered calls only), the per-request
+ * finalize, the residual / recovery pass (with draft_probs only).  Entries beyond num_events,
+ * or NULL entries, are skipped.
  * The pages have no counterpart: this exists to time each kernel on its own stream.
  */
 spec_status spec_reject_sample_profiled(const void *target_logits, spec_dtype logits_dtype, int64_t T, int32_t V,
@@ -378,10 +379,10 @@ spec_status spec_ngram_propose(const int32_t *tokens, const int64_t *cu_tokens, 
                                int32_t *out_num_drafts, void *stream);
 
 /* Kernels one call of B requests on 16-byte-aligned rows in device memory launches: 2 when
- * B >= 64 and the call has no top-k / top-p or its rows are bf16 (the layout check, then the
- * pass that reads rows up to each first rejection); otherwise row statistics and the finalize
- * (2), plus the top-k / top-p cut with filters, plus the residual pass with draft
- * probabilities. */
+ * B >= 1 and the call has no top-k / top-p, or B >= 64 with top-k / top-p on bf16 rows (the
+ * layout check, then the pass that reads rows up to each first rejection); otherwise row
+ * statistics and the finalize (2), plus the top-k / top-p cut with filters, plus the residual
+ * pass with draft probabilities. */
 int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters);
 
 /* Blocks (one thread-block cluster) that work on each request in a call of B requests with

@@ -7,33 +7,43 @@
 // §12.9), or the bonus token from p after the last draft; at temperature 0 compare with
 // the argmax instead.
 //
-// Structure on the GPU (all steps are kernels of this file; nothing runs on the host):
+// Structure on the GPU (every step is a kernel of this library; nothing runs on the host).
+// Rows are split into chunks of 8 KB of logits (4096 bf16 / 2048 fp32); a chunk reduces to a
+// partial: sampling rows (m_c, s_c) with m_c the chunk max and s_c = sum 2^(l c - fl(m_c c)),
+// c = log2(e) / T_r; greedy rows (max, lowest index of the max).
 //
-//   K1 rowstats   one streaming pass over every target row, split into 8 KB chunks
-//                 (4096 bf16 / 2048 fp32 logits).  Each warp owns a contiguous range of
-//                 (row, chunk) units and reduces each chunk to a partial:
-//                   sampling rows: (m_c, s_c) with m_c the chunk max and
-//                                  s_c = sum_v 2^(l_v * c - fl(m_c * c)), c = log2(e) / T_r,
-//                                  the draft token x* of a verify row left out;
-//                   greedy rows:   (max, lowest index of the max).
-//                 128-bit loads that do not allocate in L1, 8 in flight per lane.  Block 0
-//                 also validates the ragged layout and initialises the error word.
-//   K2 finalize   one warp per request.  Lane i combines the chunk partials of verify row i
-//                 (online max / rescaled sum), adds x* back, forms p(x*) and takes the
-//                 acceptance decision u * q(x*) < p(x*) (or x* == argmax); a ballot gives the
-//                 first rejection j.  For the bonus and one-hot recoveries it then locates
-//                 the output token: a warp scan over the chunk masses finds the chunk that
-//                 holds u * Z, a three-level warp descent (32 segments -> 32 sub-segments ->
-//                 one element) finds the token inside it.  Explicit-q recoveries are left to
-//                 K3 / K4.
-//   K3 residual   explicit q only: warps stream (request, chunk) units of target row j and
-//                 draft row j of each rejecting request, reducing sum max(0, p - q) per
-//                 chunk; the warp that completes a request's last chunk (a per-request
-//                 counter) locates the recovered token as K2 does.
+//   KL  lazy_kernel, the first-rejection pass: every call without diagnostics whose rows are
+//       16-byte aligned (top-k / top-p: bf16 rows and at least 64 requests; rows in pinned
+//       host memory: at least 64 requests).  After a one-block layout check (lazy_init_kernel,
+//       chained by programmatic dependent launch), persistent blocks take requests from an
+//       atomic queue.  Per request the block streams rows t_0, t_1, ... through warp-private
+//       TMA rings (cp.async.bulk into shared memory, bounded mbarrier waits), reduces each
+//       chunk to its partial in shared memory, and warp 0 combines the row and decides
+//       position i; the walk stops at the first rejection j.  An explicit-q rejection runs the
+//       residual pass over target row t_j and draft row j (chunk masses of max(0, p - q), all
+//       warps); the whole block then draws the output token (chunk scan, then block_find over
+//       the located chunk) and warp 0 writes the outputs.  Batches too small to fill the GPU
+//       one block per request run with thread-block clusters of 2, 4 or 8 blocks per request
+//       (chunks spread over every warp of the cluster, partials gathered in the leader block
+//       through distributed shared memory).  With cuts, each reached row is cut in the block
+//       (kl_cut_row); with rows in host memory, rows are read over the host link with 16-byte
+//       loads and copied to the device for the residual pass and the draw.
+//   K1  rowstats_wr_kernel / rowstats_kernel, the full pass's row statistics: every chunk of
+//       every row, warp-private TMA rings (register-staged 16-byte loads for misaligned rows);
+//       block 0 checks the layout.
+//   K1F filter_kernel: top-k / top-p cut of each filtered row by one thread-block cluster.
+//   K2  finalize_kernel: one warp per request; combines the chunk partials of each verify row,
+//       takes the acceptance decisions (ballot for the first rejection) and draws the bonus /
+//       one-hot recoveries (chunk scan + three-level warp descent).
+//   K3  residual_kernel: explicit-q recoveries; warps stream (request, chunk) units of target
+//       row j and draft row j; the warp completing a request's last chunk draws.
+//   Also: metrics_kernel (acceptance counters), tree_walk_kernel (greedy tree verification),
+//   ngram_kernel (n-gram proposer), the diagnostic kernels and the host-row staging kernel.
 //
 // Every reduction has a fixed order (warp butterflies, sequential chunk combines), so
-// identical inputs give identical outputs; there are no floating-point atomics.  No kernel
-// waits on another block, so nothing can hang.
+// identical inputs give identical outputs; there are no floating-point atomics.  No block
+// waits for another block except through a thread-block cluster's hardware barrier, which
+// every block of the cluster takes in the same order; every mbarrier wait is bounded.
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
