@@ -1377,6 +1377,8 @@ constexpr int kLWarps = SPEC_KL_WARPS;
 constexpr int kLStages = SPEC_KL_STAGES;
 constexpr int kLThreads = kLWarps * 32;
 constexpr size_t kLSmem = (size_t)kLWarps * kLStages * kUnitBytes;
+// The draw's block_find gives each thread 32 bytes of logits of the located chunk.
+static_assert(kLThreads * 32 >= kUnitBytes, "a block of KL must cover a whole chunk in block_find");
 
 // ---- KL with top-k / top-p (bf16 rows): the cut of one row, by the whole block
 //
