@@ -446,3 +446,35 @@ def test_first_rejection_pass_branches_b72():
                             p_match=0.8, q_sigma=0.3, seed=142), name=f"branches-{dtype}")
         c, prod, full, ref = PT.assert_both_paths(w, max_mismatch_frac=0.05, rowstats=False)
         assert (prod["acc"][temps == 0] >= 0).all()
+
+
+# ---------------------------------------------------------------------------- graph capture
+
+@pytest.mark.parametrize("name,over", [("probabilistic", {}), ("large-128", {}), ("tiny", {}),
+                                       ("greedy", dict(B=16))])
+def test_call_replays_from_a_cuda_graph(name, over):
+    """After one eager call on the device (which fills the launch-shape cache), the call can be
+    captured into a CUDA graph (the layout check, then the first-rejection pass as a
+    programmatic dependent launch, in clusters of blocks for small batches) and replayed; each
+    replay gives the eager call's outputs."""
+    import torch
+    w = W.generate(name, **over)
+    d = binding.to_device(w)
+    buf = binding.make_buffers(w["B"], w["T"], w["V"], PT.dtype_code(w), d["draft_probs"] is not None)
+    tok, acc = binding.sample(**d, buffers=buf)
+    ref_tok, ref_acc = tok.cpu().numpy().copy(), acc.cpu().numpy().copy()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            binding.sample(**d, buffers=buf)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        buf.out_tokens.fill_(-7)
+        buf.out_num_accepted.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(buf.out_tokens.cpu().numpy(), ref_tok)
+        assert np.array_equal(buf.out_num_accepted.cpu().numpy(), ref_acc)
+    assert binding.last_device_error(buf.workspace)[0] == 0
