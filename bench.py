@@ -531,7 +531,7 @@ def main():
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": meta,
             "hbm_gbs_effective": round(m["alg_bytes"] / (ms / 1e3) / 1e9, 1),
             "stage_ms": [round(x, 4) for x in m["stage_ms"]], "stages": m["stages"],
-            "roofline": roofline, "gpu_launches": m["kernels"] * args.steps, "clocks": m["clocks"],
+            "roofline": roofline, "gpu_launches": m["launches"] * args.steps, "clocks": m["clocks"],
             "rows_read_per_step": m["rows_read"], "rows_total": int(w["T"]),
             "blocks_per_request": m["blocks_per_request"]}
 
@@ -563,6 +563,7 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
     tp = None if w.get("top_p") is None else torch.from_numpy(w["top_p"]).to(dev)
     filtered = tk is not None or tp is not None
     nk = binding.num_kernels(w["B"], has_q, filtered, dt)
+    launches = binding.launches_per_call(w["B"], w["V"], has_q, filtered, dt)
     lazy = binding.reads_to_first_rejection(w["B"], filtered, dt)
     stream = torch.cuda.current_stream()
     call = lambda: binding.sample_profiled(d, buf, [], stream, tk, tp)
@@ -637,7 +638,9 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
         bpr = binding.blocks_per_request(w["B"], w["V"], dt) if not filtered else 1
         dom_name = ("KL: lazy_kernel (request queue; rows streamed through warp-private TMA rings up to the first "
                     "rejection; residual pass and draw in the same block" +
-                    (f"; each request split over a cluster of {bpr} blocks" if bpr > 1 else "") + ")")
+                    (f"; each request split over a cluster of {bpr} blocks" if bpr > 1 else "") +
+                    ("; the last requests two blocks each in a chained second launch, timed with the first"
+                     if launches > nk else "") + ")")
         if filtered:
             dom_name += "; each reached row cut in the block (key-offset counts, per-chunk partials)"
         alg = dom_bytes
@@ -653,7 +656,7 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
            "l2": ("L2 flushed before every call (inputs smaller than twice L2)" if flush is not None
                   else "inputs larger than twice L2 (no flush)"),
            "dom_bytes": dom_bytes, "dom_name": dom_name, "alg_bytes": alg, "rows_read": rows_read,
-           "kernels": nk, "clocks": clk, "lazy": lazy, "blocks_per_request": bpr}
+           "kernels": nk, "launches": launches, "clocks": clk, "lazy": lazy, "blocks_per_request": bpr}
     del d, buf
     torch.cuda.empty_cache()
     return out

@@ -26,7 +26,7 @@ EXPORTED = [
     "spec_reject_status_string", "spec_reject_version", "spec_reject_sample_profiled", "spec_reject_num_kernels",
     "spec_reject_sample_noalloc", "spec_reject_metrics_update", "spec_ngram_propose",
     "spec_tree_workspace_size", "spec_tree_verify_greedy", "spec_reject_sample_filtered", "spec_reject_sample_ex",
-    "spec_reject_sample_host_ex", "spec_reject_blocks_per_request",
+    "spec_reject_sample_host_ex", "spec_reject_blocks_per_request", "spec_reject_launches_per_call",
 ]
 
 
@@ -94,6 +94,9 @@ def load():
     lib.spec_reject_sample_ex.argtypes = sample_args + [P]
     lib.spec_reject_blocks_per_request.restype = ctypes.c_int
     lib.spec_reject_blocks_per_request.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32]
+    lib.spec_reject_launches_per_call.restype = ctypes.c_int
+    lib.spec_reject_launches_per_call.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int,
+                                                  ctypes.c_int]
     lib.spec_reject_num_kernels.restype = ctypes.c_int
     lib.spec_reject_num_kernels.argtypes = [ctypes.c_int, ctypes.c_int32, ctypes.c_int, ctypes.c_int]
     _lib = lib
@@ -324,6 +327,13 @@ def num_kernels(B: int, has_draft_probs: bool, has_filters: bool = False, dtype:
 def blocks_per_request(B: int, V: int, dtype: int = BF16) -> int:
     """Blocks (a thread-block cluster) per request of an unfiltered call on the current device."""
     return int(load().spec_reject_blocks_per_request(int(dtype), int(B), int(V)))
+
+
+def launches_per_call(B: int, V: int, has_draft_probs: bool, has_filters: bool = False, dtype: int = BF16) -> int:
+    """Kernel launches of one call on the current device (stages, plus the chained second launch of
+    the first-rejection pass for large batches)."""
+    return int(load().spec_reject_launches_per_call(int(dtype), int(B), int(V), int(bool(has_draft_probs)),
+                                                    int(bool(has_filters))))
 
 
 def reads_to_first_rejection(B: int, has_filters: bool = False, dtype: int = BF16) -> bool:

@@ -98,6 +98,10 @@ struct Params {
     // diagnostics (all may be null)
     float *dbg_pdraft;
     float *dbg_z;
+    // first-rejection pass: the requests [r_begin, r_end) this launch serves, and the index of
+    // its request counter in the error word; wait_prior = 0 for a launch chained after another
+    // pass launch whose results it does not read (it starts as that launch's blocks finish)
+    int32_t r_begin, r_end, qslot, wait_prior;
 };
 
 

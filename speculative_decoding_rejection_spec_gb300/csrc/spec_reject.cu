@@ -1945,8 +1945,10 @@ __global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
 {
     allow_dependents();
     validate_layout(P);
-    if (threadIdx.x == 0)
-        P.err[2] = 0;  // next request to hand out
+    if (threadIdx.x == 0) {
+        P.err[2] = 0;  // next request to hand out (first-rejection pass)
+        P.err[3] = 0;  // the same for a second, chained launch of it
+    }
 }
 
 struct ChunkMassFromShared {  // chunk masses already reduced into shared memory
@@ -2016,10 +2018,15 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     float2 *const lpart = in_block<CS>(spart, 0u);  // the leader's chunk partials
     float *const lrm = in_block<CS>(srm, 0u);       // and residual masses
 
-    wait_for_prerequisite();
+    if (P.wait_prior)
+        wait_for_prerequisite();
+    allow_dependents();  // a chained launch may take SM slots as this launch's blocks finish
     if (P.err[0] & SPEC_DEVERR_LAYOUT) {  // the whole batch is invalid (as K2 reports it)
-        for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < P.B; r += gridDim.x * blockDim.x)
+        for (int r = P.r_begin + (int)(blockIdx.x * blockDim.x + threadIdx.x); r < P.r_end;
+             r += gridDim.x * blockDim.x)
             P.out_acc[r] = -1;
+        if (!P.wait_prior)
+            wait_for_prerequisite();  // end after the launch this one is chained to (see the end)
         return;
     }
     if (threadIdx.x < kLWarps * kLStages)
@@ -2055,13 +2062,13 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
 
     for (;;) {
         if (leader && threadIdx.x == 0) {
-            const int nr = s_abort ? P.B : atomicAdd(P.err + 2, 1);
+            const int nr = s_abort ? P.r_end : P.r_begin + atomicAdd(P.err + P.qslot, 1);
             for (unsigned q = 0; q < (unsigned)CS; ++q)
                 *in_block<CS>(&s_r, q) = nr;
         }
         cluster_barrier<CS>();
         const int r = s_r;
-        if (r >= P.B || (CS == 1 && s_abort))
+        if (r >= P.r_end || (CS == 1 && s_abort))
             break;  // uniform across the cluster
         const int cu0 = P.cu[r];
         const int k = P.cu[r + 1] - cu0;
@@ -2365,6 +2372,10 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     if (lane == 0)
         for (int64_t q2 = qc; q2 < qi; ++q2)
             mbar_wait(&bars[q2 % kLStages], (uint32_t)(q2 / kLStages) & 1, P.err);
+    // a launch chained after another without reading its results still ends after it, so that
+    // work the caller queues after this call on the stream waits for both
+    if (!P.wait_prior)
+        wait_for_prerequisite();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -2845,6 +2856,22 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // that the GPU holds a cluster for every request at once and every warp of a cluster has at
 // least one chunk of each row (a cluster serialises its requests' draws, and its barriers cost
 // more than a small row saves).
+// Requests of a batch that fills the GPU one block per request that are served by a second
+// launch with two blocks per request (see run()): a share of the blocks the first launch holds,
+// for batches of at least three times that many requests whose rows give each warp of a pair a
+// chunk; 0 otherwise.
+#ifndef SPEC_KL_TAIL_PERMILLE
+#define SPEC_KL_TAIL_PERMILLE 300  // tail requests per 1000 blocks of the first launch
+#endif
+int lazy_tail_requests(const DeviceInfo &di, int DT, int32_t B, int nchunks)
+{
+    const int64_t blocks = (int64_t)di.sms * di.blocks_lazy[DT];
+    const int64_t tail = blocks * SPEC_KL_TAIL_PERMILLE / 1000;
+    if (tail < 1 || di.clusters_lazy[DT][1] <= 0 || (kLWarps << 1) > nchunks || (int64_t)B < 3 * tail + blocks)
+        return 0;
+    return (int)tail;
+}
+
 int lazy_cluster_log2(const DeviceInfo &di, int DT, int32_t B, int nchunks)
 {
     if (SPEC_KL_CLUSTER_LOG2 >= 0)
@@ -2979,6 +3006,10 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
         return SPEC_ERR_INVALID_ARG;
     P.counters = reinterpret_cast<unsigned long long *>(counters);
     P.dbg_z = dbg_z;
+    P.r_begin = 0;
+    P.r_end = B;
+    P.qslot = 2;
+    P.wait_prior = 1;
     const bool filtered = top_k || top_p;
     if (filtered) {
         if (!aligned(top_k, 4) || !aligned(top_p, 4) ||
@@ -3057,13 +3088,27 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
                 return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
             }
         }
+        const int tail = rows_in_host ? 0 : lazy_tail_requests(*di, DT, B, pl.nchunks);
+        Params Pm = P;
+        Pm.r_end = B - tail;
         cudaError_t e;
         if (rows_in_host)
-            e = DT ? launch_lazy(lazy_kernel<1, true, false>, gridL, 1, kLSmem, P, pdl, stream)
-                   : launch_lazy(lazy_kernel<0, true, false>, gridL, 1, kLSmem, P, pdl, stream);
+            e = DT ? launch_lazy(lazy_kernel<1, true, false>, gridL, 1, kLSmem, Pm, pdl, stream)
+                   : launch_lazy(lazy_kernel<0, true, false>, gridL, 1, kLSmem, Pm, pdl, stream);
         else
-            e = DT ? launch_lazy(lazy_kernel<1, false, false>, gridL, 1, kLSmem, P, pdl, stream)
-                   : launch_lazy(lazy_kernel<0, false, false>, gridL, 1, kLSmem, P, pdl, stream);
+            e = DT ? launch_lazy(lazy_kernel<1, false, false>, gridL, 1, kLSmem, Pm, pdl, stream)
+                   : launch_lazy(lazy_kernel<0, false, false>, gridL, 1, kLSmem, Pm, pdl, stream);
+        if (e == cudaSuccess && tail > 0) {
+            // the last requests, two blocks each, in a launch chained after the first (it reads
+            // none of the first's results): its clusters take SM slots as the first launch's
+            // blocks run out of requests, and finish their requests twice as fast
+            Params Pt = P;
+            Pt.r_begin = B - tail;
+            Pt.qslot = 3;
+            Pt.wait_prior = 0;
+            const int ncl = (int)clamp_grid(di->clusters_lazy[DT][1], tail);
+            e = DT ? launch_lazy_cluster<1, 2>(Pt, ncl, true, stream) : launch_lazy_cluster<0, 2>(Pt, ncl, true, stream);
+        }
         mark();
         return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
     }
@@ -3553,6 +3598,20 @@ int spec_reject_blocks_per_request(spec_dtype logits_dtype, int32_t B, int32_t V
     if (B < 1 || !make_plan(B, B, V, logits_dtype, 0, &pl) || device_info(&di) != cudaSuccess)
         return 0;
     return 1 << lazy_cluster_log2(*di, logits_dtype == SPEC_BF16 ? 1 : 0, B, pl.nchunks);
+}
+
+int spec_reject_launches_per_call(spec_dtype logits_dtype, int32_t B, int32_t V, int has_draft_probs,
+                                  int has_filters)
+{
+    Plan pl;
+    DeviceInfo *di;
+    const int stages = spec_reject_num_kernels(logits_dtype, B, has_draft_probs, has_filters);
+    if (B < 1 || has_filters || !make_plan(B, B, V, logits_dtype, has_draft_probs, &pl) || device_info(&di) != cudaSuccess)
+        return stages;
+    const int DT = logits_dtype == SPEC_BF16 ? 1 : 0;
+    if (lazy_cluster_log2(*di, DT, B, pl.nchunks) == 0 && lazy_tail_requests(*di, DT, B, pl.nchunks) > 0)
+        return 3;  // the layout check, the first-rejection pass, its chained second launch
+    return stages;
 }
 
 int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_probs, int has_filters)

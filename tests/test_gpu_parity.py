@@ -478,3 +478,23 @@ def test_call_replays_from_a_cuda_graph(name, over):
         assert np.array_equal(buf.out_tokens.cpu().numpy(), ref_tok)
         assert np.array_equal(buf.out_num_accepted.cpu().numpy(), ref_acc)
     assert binding.last_device_error(buf.workspace)[0] == 0
+
+
+def test_launch_shapes():
+    """The launch shape each benchmark workload takes on this GPU (host logic with the device's
+    occupancy): large batches one block per request, with the last requests in a chained second
+    launch of two blocks each; small batches in clusters of blocks."""
+    import torch
+    if torch.cuda.get_device_properties(0).multi_processor_count < 148:
+        pytest.skip("shapes checked on a GB300-sized GPU")
+    shapes = {}
+    for name in ("large-1024", "large-512", "large-128", "probabilistic", "deterministic", "greedy", "tiny"):
+        spec = W.CONFIGS[name]
+        dt = binding.BF16 if spec["dtype"] == "bf16" else binding.F32
+        has_q = spec["draft"] in ("noisy_q", "target_q")
+        shapes[name] = (binding.blocks_per_request(spec["B"], spec["V"], dt),
+                        binding.launches_per_call(spec["B"], spec["V"], has_q, False, dt))
+    assert shapes["large-1024"] == (1, 3), shapes
+    assert shapes["large-512"] == (1, 2) and shapes["deterministic"] == (1, 2), shapes
+    assert shapes["large-128"] == (2, 2) and shapes["probabilistic"] == (4, 2), shapes
+    assert shapes["greedy"] == (1, 2) and shapes["tiny"] == (1, 2), shapes
