@@ -630,11 +630,18 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
     valid = acc >= 0
     rejecting = int((valid & (acc < ks)).sum()) if has_q else 0
     small = 8 * (w["T"] - w["B"]) + 12 * w["T"] + 4 * (2 * w["B"] + 1)
+    # draft-probability bytes a rejection needs: the whole row of q, except with a top-k of at most
+    # 256 tokens, where the residual has mass at the kept tokens only and the cut mode reads q
+    # there alone (a 32-byte sector per kept token)
+    tk_all = None if tk is None else tk.cpu().numpy()
+    q_row_bytes = w["V"] * 4
+    if lazy and filtered and tk_all is not None and (tk_all > 0).all() and int(tk_all.max()) <= 256:
+        q_row_bytes = 32 * int(tk_all.max())
     if lazy:
         rows_read = int((acc[valid] + 1).sum())
         stages = ["layout_check", "rows_to_first_rejection"]
         dom = 1
-        dom_bytes = rows_read * w["V"] * es + rejecting * w["V"] * 4 + small
+        dom_bytes = rows_read * w["V"] * es + rejecting * q_row_bytes + small
         bpr = binding.blocks_per_request(w["B"], w["V"], dt) if not filtered else 1
         dom_name = ("KL: lazy_kernel (request queue; rows streamed through warp-private TMA rings up to the first "
                     "rejection; residual pass and draw in the same block" +

@@ -1401,6 +1401,11 @@ static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot a
 
 constexpr int kCutNarrow = 128;       // largest keys counted per chunk first (one binade of bf16)
 constexpr int kCutNarrowChunks = 64;  // chunks (4096 tokens) a row may have for the per-chunk counts
+constexpr int kCutList = kFKeys - kCutNarrow;  // per warp: window tokens listed by the narrow count
+                                               // (after its counts and a sink per lane)
+constexpr int kKeptMax = 256;         // kept tokens an output row may have for the draw from the list
+static_assert(kCutNarrowChunks <= 8 * kLWarps, "a listed token names its chunk among the warp's in 3 bits");
+static_assert(kUnitBytes / 2 <= 4096, "a listed token's element in its chunk fits 12 bits");
 
 struct CutSmem {
     unsigned hw[kLWarps][kFKeys + 32];                // per warp: tokens per key offset, then a sink per lane
@@ -1409,7 +1414,15 @@ struct CutSmem {
     int hcc_over;
     unsigned bh[kFKeys];                // block totals per key offset
     unsigned long long km[kFKeys];      // fixed-point mass of one token per key offset
-    unsigned long long bm[kFKeys];      // block masses per key offset (tokens x km)
+    union {
+        unsigned long long bm[kFKeys];  // block masses per key offset (tokens x km)
+        struct {                        // the draw from the list: kept tokens, in list order and sorted
+            int idx[kKeptMax];
+            float w[kKeptMax];
+            int sidx[kKeptMax];
+            float sw[kKeptMax];
+        } kp;
+    };
     union {
         unsigned long long kmc[kFKeys + 1];  // km up to the cut offset, then zeros
         unsigned long long rm[256];          // radix: weights per digit
@@ -1425,6 +1438,11 @@ struct CutSmem {
     float tp;
     uint32_t thr;                       // cut key of the latest row (0 = none)
     int abort;                          // a copy of a pass did not land in time
+    int ln[kLWarps];                    // per warp: window tokens its narrow count met (listed up to kCutList)
+    int lok;                            // the latest cut's window tokens are all listed (narrow path)
+    int kc[kLWarps];                    // the draw from the list: kept tokens per warp
+    int zok;                            // and whether its residual has mass
+    int tok;                            // and its token
     int narrow_miss;                    // the block's latest cut lay below the narrow window
     uint64_t bar[kLWarps][2];           // per warp: one mbarrier per half of its ring slot
     uint32_t ph[kLWarps];               // per warp: the parity each of the two is waiting for
@@ -1537,7 +1555,9 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     };
     // A pass over this warp's chunks c = warp, warp + nw, ...: each chunk in two copies of at
     // most 4 KB (TMA, into the two halves of the warp's ring slot, both in flight), then
-    // start(c), fv(w) for each 16-byte vector w of its elements from shared memory and fe(bits)
+    // start(c), fv(st, nv, c, lo) for the nv 16-byte vectors st[] of each copy in shared memory,
+    // elements lo, lo + 1, ... of the row (the warp's lanes take vectors lane, lane + 32, ...:
+    // per_vec) and fe(bits)
     // for the last elements of the row past a multiple of 8 (global memory), then done(c).  Chunks with want(c) false are not
     // read (empty copies keep the barriers' phases in step).  A copy that does not land in time
     // sets C.abort; the pass still returns through every barrier of the block.
@@ -1582,8 +1602,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                     start(c);
                 const uint4 *st = reinterpret_cast<const uint4 *>(P.slot + sl * kCutHalfBytes);
                 const int nv = (hi - lo) >> 3;
-                for (int v = lane; v < nv; v += 32)
-                    fv(st[v]);
+                fv(st, nv, c, lo);
                 for (int i = lo + nv * 8 + lane; i < hi; i += 32)
                     fe((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i));
                 if (sl == 1)
@@ -1598,6 +1617,12 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     };
     auto all = [](int) { return true; };
     auto nop = [](int) {};
+    auto per_vec = [&](auto f) {
+        return [&, f](const uint4 *st, int nv, int, int) {
+            for (int v = lane; v < nv; v += 32)
+                f(st[v]);
+        };
+    };
     auto each8 = [](const uint4 &w, auto fe) {
         fe(w.x & 0xffffu);
         fe(w.x >> 16);
@@ -1688,33 +1713,73 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     // counts by key offset over the w largest keys, one histogram per warp with a sink per lane
     // for the rest (no branch); with `flush`, the counts of each chunk move to C.hcc[c] after
     // the chunk (8 bits each; a larger count sets C.hcc_over)
-    // A narrow window (w <= kCutNarrow) of a row whose maximum is at least 512 keys above +0
-    // counts only the tokens inside it: an integer test on both halves of each word (bits &
-    // 0x7fff plus 0x8000 - lowest carries into bit 15 exactly when the bits are at least the
-    // window's lowest, and bit 15 of the bits is clear for positive logits) marks them, and a
-    // lane counts its marked tokens one by one (usually none): one atomic instruction per vector
-    // where every token would take eight.
+    // A narrow window (w <= kCutNarrow) counts only the tokens inside it, about one in a hundred:
+    // a packed bf16 compare against the window's lowest logit tests two tokens at once (the order
+    // keys follow the logits; -0 and +0 share a key and compare equal; NaN compares false), the
+    // results of four vectors become one 32-bit mask per lane, and each lane then counts the
+    // tokens its mask marks, reading them from the copy in shared memory.  The warp takes as
+    // many turns as its busiest lane has marks, where counting every token would take eight
+    // atomics per vector.
     auto count_pass = [&](int w, bool flush) {
         unsigned *h = C.hw[warp];
         const uint32_t sink = (uint32_t)w + (uint32_t)lane;
-        auto fe = [&](uint32_t b16) { atomicAdd(&h[min(offset(b16), sink)], 1u); };
-        const bool marks = plain && w <= kCutNarrow;
-        const uint32_t add = 0x8000u - (kmax - 0x8000u - (uint32_t)(w - 1));  // plain: kmax - 0x8000 >= kB
-        const uint32_t add2 = add | (add << 16);
-        auto hit = [&](uint32_t x) { return ((x & 0x7fff7fffu) + add2) & ~x & 0x80008000u; };
-        auto vec = [&](const uint4 &v) {
+        bool tail_in = false;  // a token of a row's last elements (past a multiple of 8) lies in the window
+        auto fe = [&](uint32_t b16) {
+            const uint32_t o = offset(b16);
+            tail_in = tail_in || o < (uint32_t)w;
+            atomicAdd(&h[min(o, sink)], 1u);
+        };
+        const bool marks = w <= kCutNarrow;
+        constexpr uint32_t kNegInfKey = 0x80u;  // keys below it are NaNs
+        const uint32_t klo = kmax >= kNegInfKey + (uint32_t)(w - 1) ? kmax - (uint32_t)(w - 1) : kNegInfKey;
+        const uint32_t lo16 = __float_as_uint(x_of<1>(klo)) >> 16;
+        const uint32_t lo2 = lo16 | (lo16 << 16);
+        auto ge = [&](uint32_t x) {  // 0xffff per 16-bit half holding a logit >= the window's lowest
+            uint32_t r;
+            asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(lo2));
+            return r;
+        };
+        auto mask8 = [&](const uint4 &x) -> uint32_t {  // bit e: element e of the vector is in the window
+            const uint32_t f0 = __byte_perm(ge(x.x), ge(x.y), 0x6420) & 0x01010101u;  // elements 0..3, a byte each
+            const uint32_t f1 = __byte_perm(ge(x.z), ge(x.w), 0x6420) & 0x01010101u;  // elements 4..7
+            return ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xf0u);  // bytes to bits
+        };
+        // the window's tokens, in the warp's list (while it has room): (the warp's chunk number
+        // << 28) | (element in the chunk << 16) | bf16 bits
+        uint32_t *list = C.hw[warp] + kCutNarrow + 32;
+        int nl = 0;  // tokens met (every lane)
+        const unsigned lt = (1u << lane) - 1u;
+        auto vec = [&](const uint4 *st, int nv, int c, int lo) {
             if (!marks) {
-                each8(v, fe);
+                for (int v = lane; v < nv; v += 32)
+                    each8(st[v], fe);
                 return;
             }
-            const uint32_t h0 = hit(v.x), h1 = hit(v.y), h2 = hit(v.z), h3 = hit(v.w);
-            uint32_t m = ((h0 >> 15) & 1u) | ((h0 >> 30) & 2u) | ((h1 >> 13) & 4u) | ((h1 >> 28) & 8u) |
-                         ((h2 >> 11) & 16u) | ((h2 >> 26) & 32u) | ((h3 >> 9) & 64u) | ((h3 >> 24) & 128u);
-            while (m) {
-                const int j = __ffs(m) - 1;
-                m &= m - 1;
-                const uint32_t word = j < 4 ? (j < 2 ? v.x : v.y) : (j < 6 ? v.z : v.w);
-                fe((j & 1) ? word >> 16 : word & 0xffffu);
+            const unsigned short *st16 = reinterpret_cast<const unsigned short *>(st);
+            const uint32_t tag = ((uint32_t)((c - warp) / nw) << 28) | ((uint32_t)(lo - c * P.chunk) << 16);
+            for (int g = 0; g * 4 * 32 < nv; ++g) {  // uniform over the warp
+                const int v0 = g * 4 * 32 + lane;
+                uint32_t m = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (v0 + 32 * t < nv)
+                        m |= mask8(st[v0 + 32 * t]) << (8 * t);
+                for (;;) {  // one marked token per lane and turn
+                    const unsigned bal = __ballot_sync(kFull, m != 0u);
+                    if (!bal)
+                        break;
+                    if (m) {
+                        const int b = __ffs(m) - 1;
+                        m &= m - 1;
+                        const int e = (v0 + 32 * (b >> 3)) * 8 + (b & 7);  // element of the copy
+                        const uint32_t b16 = st16[e];
+                        atomicAdd(&h[offset(b16)], 1u);  // inside the window: below w
+                        const int pos = nl + __popc(bal & lt);
+                        if (flush && pos < kCutList)
+                            list[pos] = tag + ((uint32_t)e << 16) + b16;
+                    }
+                    nl += __popc(bal);
+                }
             }
         };
         // a chunk whose maximum lies below the window holds no token of it: not read (its
@@ -1749,6 +1814,12 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             pass(reaches, nop, vec, fe, flush_chunk);
         else
             pass(all, nop, vec, fe, flush_chunk);
+        // the last elements are counted, not listed: a window token among them leaves the list
+        // incomplete (taken as overflowing)
+        if (__any_sync(kFull, tail_in))
+            nl = kCutList + 1;
+        if (flush && lane == 0)
+            C.ln[warp] = nl;
         __syncthreads();
     };
 
@@ -1773,6 +1844,12 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         }
         if (pn >= 0) {  // K1F's one-pass partials
             const uint32_t thr = kmax - (uint32_t)pn;
+            if (threadIdx.x == 0) {
+                int ok = 1;
+                for (int w = 0; w < nw; ++w)
+                    ok &= C.ln[w] <= kCutList;
+                C.lok = ok;  // read after the barrier below
+            }
             for (int c = warp; c < P.nchunks; c += nw) {
                 const float mk = C.cmx[c];
                 float mc = -INFINITY, sc = 0.f;
@@ -1818,7 +1895,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                 spart[c] = make_float2(-INFINITY, 0.f);
         unsigned long long sum = 0;
         auto fe = [&](uint32_t b16) { sum += C.kmc[min(offset(b16), (uint32_t)kB)]; };
-        pass(live, nop, [&](const uint4 &w) { each8(w, fe); }, fe,
+        pass(live, nop, per_vec([&](const uint4 &w) { each8(w, fe); }), fe,
              [&](int c) {
                  const float mc = C.cmx[c];
                  const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
@@ -1861,7 +1938,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                     }
                 }
             };
-            pass(all, nop, [&](const uint4 &w) { each8(w, fe); }, fe, nop);
+            pass(all, nop, per_vec([&](const uint4 &w) { each8(w, fe); }), fe, nop);
             __syncthreads();
             for (int d = threadIdx.x; d < 256; d += blockDim.x) {
                 unsigned long long t = 0;
@@ -1909,7 +1986,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         if (key16(b16) >= thr)
             sum += __float2ull_rn(ex2(fmaf(__uint_as_float(b16 << 16), cs, -Mc)) * kTwo32);
     };
-    pass(live, [&](int c) { Mc = C.cmx[c] * cs; }, [&](const uint4 &w) { each8(w, fe); }, fe,
+    pass(live, [&](int c) { Mc = C.cmx[c] * cs; }, per_vec([&](const uint4 &w) { each8(w, fe); }), fe,
          [&](int c) {
              const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f;
              if (lane == 0)
@@ -1926,12 +2003,144 @@ template <int DT> __device__ __noinline__ void kl_cut_row(const CutDims P, CutSm
     const float tp = C.tp;
     const bool use_k = tk > 0 && tk < P.V;
     const bool use_p = tp > 0.f && tp < 1.f;
+    if (threadIdx.x == 0)
+        C.lok = 0;  // set by a cut whose window tokens are all listed (every other thread reads it
+                    // after the cut's barriers, or after the caller's when there is no cut)
     if (!(use_k || use_p))
         return;  // C.thr stays 0
     const uint32_t thr = kl_cut_key<DT>(P, C, spart, row, cs, tk, tp, use_k);
     if (threadIdx.x == 0)
         C.thr = thr;
     __syncthreads();
+}
+
+// The output token of a cut row from the window tokens its narrow count listed (C.lok): every
+// token the cut keeps (key >= C.thr) is among them, and every other token has no mass, so the
+// draw reads the kept tokens only (and q at those tokens only) instead of the whole row.  The
+// draw is the full path's: the smallest token whose cumulative mass, in token order, exceeds
+// u * Z; the last token with mass when rounding leaves u * Z at or past the total.  Masses:
+//   mode 0 (explicit q):  max(0, p(x) - q(x)), p(x) = 2^(x cs - M) / S (inv_s = 1 / S);
+//   mode 1 (one-hot draft): 2^(x cs - M), none at x* (p without the draft token);
+//   mode 2 (the bonus row): 2^(x cs - M);
+// an empty residual (modes 0 and 1) draws from 2^(x cs - M).  All threads of the block; returns
+// the token, or -1 when more than kKeptMax tokens are kept (the caller takes the full path).
+__device__ __noinline__ int kl_list_draw(CutSmem &C, int chunk, int mode, const float *qrow, float cs, float M,
+                                         float inv_s, int xstar, float u)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = (int)(blockDim.x >> 5);
+    const unsigned lt = (1u << lane) - 1u;
+    const uint32_t thr = C.thr;
+    const uint32_t *list = C.hw[warp] + kCutNarrow + 32;
+    const int n = C.ln[warp];
+    auto key = [](uint32_t b16) {
+        const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
+        return 0x8000u + (((b16 & 0x7fffu) ^ sg) - sg);
+    };
+    int cnt = 0;
+    for (int i = lane; i < n; i += 32)
+        cnt += key(list[i] & 0xffffu) >= thr;
+    cnt = __reduce_add_sync(kFull, cnt);
+    if (lane == 0)
+        C.kc[warp] = cnt;
+    __syncthreads();
+    int off = 0, total = 0;
+    for (int w = 0; w < nw; ++w) {
+        off += w < warp ? C.kc[w] : 0;
+        total += C.kc[w];
+    }
+    if (total > kKeptMax || total == 0)
+        return -1;  // uniform
+    // the kept tokens with 2^(x cs - M), in list order (warp by warp)
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        const uint32_t e = i < n ? list[i] : 0u;
+        const bool keep = i < n && key(e & 0xffffu) >= thr;
+        const unsigned bal = __ballot_sync(kFull, keep);
+        if (keep) {
+            const int pos = off + __popc(bal & lt);
+            C.kp.idx[pos] = (warp + nw * (int)(e >> 28)) * chunk + (int)((e >> 16) & 0xfffu);
+            C.kp.w[pos] = ex2(fmaf(__uint_as_float((e & 0xffffu) << 16), cs, -M));
+        }
+        off += __popc(bal);
+    }
+    __syncthreads();
+    // sorted by token (the kept tokens are distinct; rank = kept tokens before it), with their
+    // masses, or with p's when `with_p`
+    auto sort = [&](bool with_p) {
+        for (int t = threadIdx.x; t < total; t += blockDim.x) {
+            const int x = C.kp.idx[t];
+            const float p = C.kp.w[t];
+            int rank = 0;
+            for (int o = 0; o < total; ++o)
+                rank += C.kp.idx[o] < x;
+            C.kp.sidx[rank] = x;
+            C.kp.sw[rank] = (with_p || mode == 2) ? p
+                            : mode == 0         ? fmaxf(0.f, p * inv_s - __ldg(qrow + x))
+                                                : (x == xstar ? 0.f : p);
+        }
+        __syncthreads();
+    };
+    // warp 0: lane l takes sorted tokens [b0, b1); seg = their mass, inc = the inclusive scan of
+    // the segments, Z = the total
+    const int per = (total + 31) / 32;
+    const int b0 = min(total, lane * per), b1 = min(total, b0 + per);
+    auto scan = [&](float &seg, float &inc) {
+        seg = 0.f;
+        for (int t = b0; t < b1; ++t)
+            seg += C.kp.sw[t];
+        inc = seg;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o)
+                inc += y;
+        }
+        return __shfl_sync(kFull, inc, 31);
+    };
+    sort(false);
+    if (mode != 2) {
+        if (warp == 0) {
+            float seg, inc;
+            const float Z = scan(seg, inc);
+            if (lane == 0)
+                C.zok = Z > 0.f;
+        }
+        __syncthreads();
+        if (!C.zok)  // empty residual: draw from p (uniform)
+            sort(true);
+    }
+    if (warp == 0) {
+        float seg, inc;
+        const float Z = scan(seg, inc);
+        const float th = u * Z;
+        float run = inc - seg;
+        int hit = -1;
+        for (int t = b0; t < b1; ++t) {
+            run += C.kp.sw[t];
+            if (run > th) {
+                hit = t;
+                break;
+            }
+        }
+        const unsigned found = __ballot_sync(kFull, hit >= 0);
+        int t;
+        if (found) {
+            t = __shfl_sync(kFull, hit, __ffs(found) - 1);
+        } else {  // rounding left u * Z at or past the total: the last token with mass
+            int last = -1;
+            for (int q = b0; q < b1; ++q)
+                if (C.kp.sw[q] > 0.f)
+                    last = q;
+            t = (int)__reduce_max_sync(kFull, (unsigned)(last + 1)) - 1;
+        }
+        if (lane == 0)
+            C.tok = t >= 0 ? C.kp.sidx[t] : (total > 0 ? C.kp.sidx[total - 1] : 0);
+    }
+    __syncthreads();
+    const int token = C.tok;
+    __syncthreads();  // C.tok and the kept arrays are rewritten by the next draw
+    return token;
 }
 
 
@@ -2270,8 +2479,20 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         const char *rowj = (HOST && P.lstage) ? P.lstage + (size_t)tj * P.lstride * ES : row_ptr<DT>(P, tj);
         float *qstage_j = (HOST && P.qstage) ? P.qstage + (db + j) * (int64_t)P.V : nullptr;
         int token = -1;
-        const bool residual = !greedy && j < k && P.q;
+        bool residual = !greedy && j < k && P.q;
         const uint32_t thr = CUT ? C.thr : 0u;  // cut key of row t_j
+        bool drawn = false;
+        if constexpr (CUT)
+            if (!greedy && C.lok) {  // uniform: row t_j's kept tokens are all listed
+                const int mode = j == k ? 2 : (P.q ? 0 : 1);
+                // q where it lives (rows in host memory: the device copy is written by the residual
+                // pass, which the list makes unnecessary)
+                const float *qj = mode == 0 ? P.q + (db + j) * P.qstride : nullptr;
+                const int xj = __shfl_sync(kFull, xs, j & 31);
+                token = kl_list_draw(C, P.chunk, mode, qj, cs, s_M, 1.f / s_S, xj, __ldg(P.uni + 2 * tj + 1));
+                drawn = token >= 0;
+                residual = residual && !drawn;
+            }
         if (residual) {  // explicit q: residual chunk masses of row t_j by every warp (K3)
             const float Mj = s_M, Sj = s_S;
             const ResidualMass<DT, CUT> f{rowj, P.q + (db + j) * P.qstride, cs, Mj, 1.f / Sj, thr};
@@ -2286,7 +2507,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
             }
             cluster_barrier<CS>();
         }
-        if (leader) {
+        if (leader && !drawn) {
             // the draw, by the whole block: chunk masses scanned by every warp alike (smem), the
             // chunk searched by all threads at once (block_find: one round trip to memory)
             const float us = greedy ? 0.f : __ldg(P.uni + 2 * tj + 1);
