@@ -1384,16 +1384,18 @@ static_assert(kLThreads * 32 >= kUnitBytes, "a block of KL must cover a whole ch
 //
 // The same cut as K1F, from the row KL has just streamed (its unfiltered chunk partials are in
 // shared memory; the row is read again through the warp's ring slot, mostly from L2):
-//   1. with at most kCutNarrowChunks chunks, the tokens of the kCutNarrow largest keys counted by
-//      order-key offset below the maximum's key, per chunk (only vectors holding such a token
-//      are unpacked); warp 0 finds the k-th largest key, S_k and the top-p key from the totals
-//      (integer sums of count x fixed-point mass, K1F's one-pass rules), and a cut inside this
-//      window takes K1F's one-pass partials from the per-chunk counts;
-//   2. otherwise the same over the kFKeys largest keys (one histogram per warp, a sink per lane
-//      for the rest), and one more pass gives each chunk's partial over the survivors: per
-//      element the mass of its key offset, summed as integers, which is K1F's count x mass sum;
-//   3. a cut below that window is found by a radix select on the 16-bit order key (two passes
-//      of digit histograms per selection), with the partials of K1F's general path.
+//   1. counts of tokens by order-key offset below the row maximum's key over a window of the
+//      largest keys, tried in three widths: kCutNarrow (one binade of bf16; with at most
+//      kCutNarrowChunks chunks, counted per chunk, and its tokens listed for the draw), kCutMid,
+//      then kFKeys.  The first two mark their tokens with packed compares and count only those
+//      (visit_marked); the widest counts every token (one histogram per warp, a sink per lane
+//      for the rest).  Warp 0 finds the k-th largest key, S_k and the top-p key from the totals
+//      (integer sums of count x fixed-point mass, K1F's one-pass rules).  A width is skipped
+//      while the block's latest cut lay deeper (rows of a batch tend to cut alike);
+//   2. partials over the survivors: from the per-chunk counts of the narrow window, else one more
+//      pass adding, per kept token, the fixed-point mass of its key offset (K1F's count x mass sum);
+//   3. a cut below the widest window is found by a radix select on the 16-bit order key (two
+//      passes of digit histograms per selection), with the partials of K1F's general path.
 // Whichever step finds it, the cut key and the partials are K1F's, bit for bit.
 
 constexpr int kCutHalfBytes = kUnitBytes / 2;  // a pass moves each chunk in two copies of this size
@@ -1401,6 +1403,9 @@ static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot a
 
 constexpr int kCutNarrow = 128;       // largest keys counted per chunk first (one binade of bf16)
 constexpr int kCutNarrowChunks = 64;  // chunks (4096 tokens) a row may have for the per-chunk counts
+constexpr int kCutMid = 256;          // then the largest keys counted with marks (two binades)
+static_assert(kCutMid + 32 <= kFKeys + 32 && kCutMid % 32 == 0 && (kCutMid / 32 & (kCutMid / 32 - 1)) == 0,
+              "the middle window fits the per-warp histograms and splits evenly over a warp");
 constexpr int kCutList = kFKeys - kCutNarrow;  // per warp: window tokens listed by the narrow count
                                                // (after its counts and a sink per lane)
 constexpr int kKeptMax = 256;         // kept tokens an output row may have for the draw from the list
@@ -1423,10 +1428,7 @@ struct CutSmem {
             float sw[kKeptMax];
         } kp;
     };
-    union {
-        unsigned long long kmc[kFKeys + 1];  // km up to the cut offset, then zeros
-        unsigned long long rm[256];          // radix: weights per digit
-    };
+    unsigned long long rm[256];         // radix: weights per digit
     float cmx[kLMaxChunks];             // unfiltered chunk maxima
     unsigned long long red[kLWarps];
     double z;                           // normaliser (top-p alone), 2^-32 units
@@ -1444,6 +1446,7 @@ struct CutSmem {
     int zok;                            // and whether its residual has mass
     int tok;                            // and its token
     int narrow_miss;                    // the block's latest cut lay below the narrow window
+    int mid_miss;                       // and below the middle one
     uint64_t bar[kLWarps][2];           // per warp: one mbarrier per half of its ring slot
     uint32_t ph[kLWarps];               // per warp: the parity each of the two is waiting for
 };
@@ -1489,6 +1492,58 @@ __device__ __forceinline__ void warp_digit_crossing(CutSmem &C, unsigned long lo
     if (found && lane == __ffs(found) - 1) {
         C.dsel = pos;
         C.dabove = ab;
+    }
+}
+
+// The bf16 pair holding twice the logit whose order key is `key` (keys under that of -inf,
+// 0x80, are NaNs: a lower key gives -inf).
+__device__ __forceinline__ uint32_t bf16_pair_of_key(uint32_t key)
+{
+    const uint32_t b = __float_as_uint(x_of<1>(key > 0x80u ? key : 0x80u)) >> 16;
+    return b | (b << 16);
+}
+
+// The tokens of one copy in shared memory (nv 16-byte vectors of bf16; lane l takes vectors l,
+// l + 32, ...) whose logits compare >= the pair lo2 (the order keys follow the logits: -0 and +0
+// share a key and compare equal; NaN compares false).  A packed compare tests two tokens; the
+// results of four vectors become a 32-bit mask per lane, and visit(bits, element, ballot) runs
+// once per marked token, one per lane and turn, all lanes in step, so that the warp takes as many
+// turns as its busiest lane has marks; turn(ballot) follows every turn.  Cheap where the marked
+// tokens are few, as above a cut or inside a narrow window.
+template <class Visit, class Turn>
+__device__ __forceinline__ void visit_marked(const uint4 *st, int nv, uint32_t lo2, Visit visit, Turn turn)
+{
+    const int lane = threadIdx.x & 31;
+    auto ge = [&](uint32_t x) {  // 0xffff per 16-bit half holding a logit >= lo2's
+        uint32_t r;
+        asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(lo2));
+        return r;
+    };
+    auto mask8 = [&](const uint4 &x) -> uint32_t {  // bit e: element e of the vector is marked
+        const uint32_t f0 = __byte_perm(ge(x.x), ge(x.y), 0x6420) & 0x01010101u;  // elements 0..3, a byte each
+        const uint32_t f1 = __byte_perm(ge(x.z), ge(x.w), 0x6420) & 0x01010101u;  // elements 4..7
+        return ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xf0u);  // bytes to bits
+    };
+    const unsigned short *st16 = reinterpret_cast<const unsigned short *>(st);
+    for (int g = 0; g * 4 * 32 < nv; ++g) {  // uniform over the warp
+        const int v0 = g * 4 * 32 + lane;
+        uint32_t m = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (v0 + 32 * t < nv)
+                m |= mask8(st[v0 + 32 * t]) << (8 * t);
+        for (;;) {
+            const unsigned bal = __ballot_sync(kFull, m != 0u);
+            if (!bal)
+                break;
+            if (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                const int e = (v0 + 32 * (b >> 3)) * 8 + (b & 7);  // element of the copy
+                visit((uint32_t)st16[e], e, bal);
+            }
+            turn(bal);
+        }
     }
 }
 
@@ -1702,24 +1757,16 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             else
                 ok = use_k;  // top-p alone: the cut lies below the window
         }
-        if (ok && n == kB)  // one token's mass by key offset, zero past the cut (no branch in the pass)
-            for (int o = lane; o <= kB; o += 32)
-                C.kmc[o] = o <= pcut ? C.km[o] : 0ull;
         if (lane == 0)
             C.pos = ok ? pcut : -1;
     }
     };
 
-    // counts by key offset over the w largest keys, one histogram per warp with a sink per lane
-    // for the rest (no branch); with `flush`, the counts of each chunk move to C.hcc[c] after
-    // the chunk (8 bits each; a larger count sets C.hcc_over)
-    // A narrow window (w <= kCutNarrow) counts only the tokens inside it, about one in a hundred:
-    // a packed bf16 compare against the window's lowest logit tests two tokens at once (the order
-    // keys follow the logits; -0 and +0 share a key and compare equal; NaN compares false), the
-    // results of four vectors become one 32-bit mask per lane, and each lane then counts the
-    // tokens its mask marks, reading them from the copy in shared memory.  The warp takes as
-    // many turns as its busiest lane has marks, where counting every token would take eight
-    // atomics per vector.
+    // counts by key offset over the w largest keys in the warp's histogram: windows up to kCutMid
+    // count their marked tokens only (visit_marked: about one token in a hundred for the narrow
+    // window), wider ones every token, with a sink per lane for the tokens below the window (no
+    // branch); with `flush`, the counts of each chunk move to C.hcc[c] after the chunk (8 bits
+    // each; a larger count sets C.hcc_over) and the window's tokens are listed
     auto count_pass = [&](int w, bool flush) {
         unsigned *h = C.hw[warp];
         const uint32_t sink = (uint32_t)w + (uint32_t)lane;
@@ -1729,23 +1776,10 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             tail_in = tail_in || o < (uint32_t)w;
             atomicAdd(&h[min(o, sink)], 1u);
         };
-        const bool marks = w <= kCutNarrow;
-        constexpr uint32_t kNegInfKey = 0x80u;  // keys below it are NaNs
-        const uint32_t klo = kmax >= kNegInfKey + (uint32_t)(w - 1) ? kmax - (uint32_t)(w - 1) : kNegInfKey;
-        const uint32_t lo16 = __float_as_uint(x_of<1>(klo)) >> 16;
-        const uint32_t lo2 = lo16 | (lo16 << 16);
-        auto ge = [&](uint32_t x) {  // 0xffff per 16-bit half holding a logit >= the window's lowest
-            uint32_t r;
-            asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(lo2));
-            return r;
-        };
-        auto mask8 = [&](const uint4 &x) -> uint32_t {  // bit e: element e of the vector is in the window
-            const uint32_t f0 = __byte_perm(ge(x.x), ge(x.y), 0x6420) & 0x01010101u;  // elements 0..3, a byte each
-            const uint32_t f1 = __byte_perm(ge(x.z), ge(x.w), 0x6420) & 0x01010101u;  // elements 4..7
-            return ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xf0u);  // bytes to bits
-        };
-        // the window's tokens, in the warp's list (while it has room): (the warp's chunk number
-        // << 28) | (element in the chunk << 16) | bf16 bits
+        const bool marks = w <= kCutMid;
+        const uint32_t lo2 = bf16_pair_of_key(kmax >= (uint32_t)(w - 1) ? kmax - (uint32_t)(w - 1) : 0u);
+        // with `flush`, the window's tokens also go to the warp's list (while it has room): (the
+        // warp's chunk number << 28) | (element in the chunk << 16) | bf16 bits
         uint32_t *list = C.hw[warp] + kCutNarrow + 32;
         int nl = 0;  // tokens met (every lane)
         const unsigned lt = (1u << lane) - 1u;
@@ -1755,32 +1789,15 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                     each8(st[v], fe);
                 return;
             }
-            const unsigned short *st16 = reinterpret_cast<const unsigned short *>(st);
             const uint32_t tag = ((uint32_t)((c - warp) / nw) << 28) | ((uint32_t)(lo - c * P.chunk) << 16);
-            for (int g = 0; g * 4 * 32 < nv; ++g) {  // uniform over the warp
-                const int v0 = g * 4 * 32 + lane;
-                uint32_t m = 0;
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    if (v0 + 32 * t < nv)
-                        m |= mask8(st[v0 + 32 * t]) << (8 * t);
-                for (;;) {  // one marked token per lane and turn
-                    const unsigned bal = __ballot_sync(kFull, m != 0u);
-                    if (!bal)
-                        break;
-                    if (m) {
-                        const int b = __ffs(m) - 1;
-                        m &= m - 1;
-                        const int e = (v0 + 32 * (b >> 3)) * 8 + (b & 7);  // element of the copy
-                        const uint32_t b16 = st16[e];
-                        atomicAdd(&h[offset(b16)], 1u);  // inside the window: below w
-                        const int pos = nl + __popc(bal & lt);
-                        if (flush && pos < kCutList)
-                            list[pos] = tag + ((uint32_t)e << 16) + b16;
-                    }
-                    nl += __popc(bal);
-                }
-            }
+            visit_marked(st, nv, lo2,
+                         [&](uint32_t b16, int e, unsigned bal) {
+                             atomicAdd(&h[offset(b16)], 1u);  // inside the window: below w
+                             const int pos = nl + __popc(bal & lt);
+                             if (flush && pos < kCutList)
+                                 list[pos] = tag + ((uint32_t)e << 16) + b16;
+                         },
+                         [&](unsigned bal) { nl += __popc(bal); });
         };
         // a chunk whose maximum lies below the window holds no token of it: not read (its
         // per-chunk counts are zeros)
@@ -1873,30 +1890,63 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         __syncthreads();
     }
 
-    // ---- 1. counts over the kFKeys largest keys
-    count_pass(kB, false);
-    totals(kB, [&](int o) {
-        unsigned t = 0;
-        for (int w = 0; w < nw; ++w)
-            t += C.hw[w][o];
-        return t;
-    });
-    select_window(kB);
-    __syncthreads();
-    const int pcut = C.pos;
-    if (threadIdx.x == 0 && pcut >= 0 && pcut < kCutNarrow)
-        C.narrow_miss = 0;  // this cut would have fit the narrow window: try it again next time
+    // ---- 1b. counts over the kCutMid largest keys, with marks (skipped while the block's latest
+    // cut lay deeper), then 1c. over the kFKeys largest keys, every token counted
+    int pcut = -1;
+    if (!C.mid_miss) {
+        count_pass(kCutMid, false);
+        totals(kCutMid, [&](int o) {
+            unsigned t = 0;
+            for (int w = 0; w < nw; ++w)
+                t += C.hw[w][o];
+            return t;
+        });
+        select_window(kCutMid);
+        __syncthreads();
+        pcut = C.pos;
+        if (pcut < 0) {
+            for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
+                (&C.hw[0][0])[i] = 0u;  // sinks of the middle window sit inside the wide one
+            if (threadIdx.x == 0)
+                C.mid_miss = 1;
+            __syncthreads();
+        }
+    }
+    if (pcut < 0) {
+        count_pass(kB, false);
+        totals(kB, [&](int o) {
+            unsigned t = 0;
+            for (int w = 0; w < nw; ++w)
+                t += C.hw[w][o];
+            return t;
+        });
+        select_window(kB);
+        __syncthreads();
+        pcut = C.pos;
+    }
+    if (threadIdx.x == 0 && pcut >= 0) {  // a cut that would have fit a skipped window: try it again
+        if (pcut < kCutNarrow)
+            C.narrow_miss = 0;
+        if (pcut < kCutMid)
+            C.mid_miss = 0;
+    }
     if (pcut >= 0) {
-        // ---- 3. chunk partials over the survivors: masses relative to the row maximum, rescaled
+        // ---- 3. chunk partials over the survivors: per kept token (marked against the cut key)
+        // the fixed-point mass of its key offset, summed as integers, rescaled to the chunk maximum
         const uint32_t thr = kmax - (uint32_t)pcut;
+        const uint32_t thr2 = bf16_pair_of_key(thr);
         auto live = [&](int c) { return C.cmx[c] > -INFINITY && key_of<1>(C.cmx[c]) >= thr; };
         for (int c = warp; c < P.nchunks; c += nw)
             if (lane == 0 && !live(c))
                 spart[c] = make_float2(-INFINITY, 0.f);
         unsigned long long sum = 0;
-        auto fe = [&](uint32_t b16) { sum += C.kmc[min(offset(b16), (uint32_t)kB)]; };
-        pass(live, nop, per_vec([&](const uint4 &w) { each8(w, fe); }), fe,
-             [&](int c) {
+        auto add = [&](uint32_t b16, int, unsigned) { sum += C.km[offset(b16)]; };
+        auto fe = [&](uint32_t b16) {
+            if (offset(b16) <= (uint32_t)pcut)
+                sum += C.km[offset(b16)];
+        };
+        pass(live, nop, [&](const uint4 *st, int nv, int, int) { visit_marked(st, nv, thr2, add, [](unsigned) {}); },
+             fe, [&](int c) {
                  const float mc = C.cmx[c];
                  const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
                  if (lane == 0)
@@ -2248,6 +2298,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
         if (threadIdx.x == 0) {
             C.abort = 0;
             C.narrow_miss = 0;
+            C.mid_miss = 0;
         }
     }
     mbar_fence_init();
