@@ -547,6 +547,17 @@ def main():
         torch.distributed.destroy_process_group()
 
 
+def q_bytes_per_rejection(w, cut_in_first_rejection_pass):
+    """Draft-probability bytes one rejection needs: the whole row of q, except where the
+    first-rejection pass cuts with a top-k of at most 256 tokens on every request: the residual
+    has mass at the kept tokens only, and the pass reads q there alone (a 32-byte sector per kept
+    token; ties at the cut key aside, at most top-k of them)."""
+    tk = w.get("top_k")
+    if cut_in_first_rejection_pass and tk is not None and (tk > 0).all() and int(tk.max()) <= 256:
+        return 32 * int(tk.max())
+    return w["V"] * 4
+
+
 def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_seconds=0.0):
     """One sampler call per step over workload w (inputs resident in HBM).  Times `steps` plain
     calls with CUDA events on the launching stream (at least `min_seconds` of them when that is
@@ -630,13 +641,7 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
     valid = acc >= 0
     rejecting = int((valid & (acc < ks)).sum()) if has_q else 0
     small = 8 * (w["T"] - w["B"]) + 12 * w["T"] + 4 * (2 * w["B"] + 1)
-    # draft-probability bytes a rejection needs: the whole row of q, except with a top-k of at most
-    # 256 tokens, where the residual has mass at the kept tokens only and the cut mode reads q
-    # there alone (a 32-byte sector per kept token)
-    tk_all = None if tk is None else tk.cpu().numpy()
-    q_row_bytes = w["V"] * 4
-    if lazy and filtered and tk_all is not None and (tk_all > 0).all() and int(tk_all.max()) <= 256:
-        q_row_bytes = 32 * int(tk_all.max())
+    q_row_bytes = q_bytes_per_rejection(w, lazy and filtered)
     if lazy:
         rows_read = int((acc[valid] + 1).sum())
         stages = ["layout_check", "rows_to_first_rejection"]
@@ -757,8 +762,10 @@ def e2e(w, dev, args):
         notes.append(f"target logits read in place from pinned memory: {rows} of {w['T']} rows")
     if has_q:
         rejecting = int(((acc >= 0) & (acc < ks)).sum())
-        h2d += rejecting * w["V"] * 4 + 32 * (w["T"] - w["B"])
-        notes.append(f"draft probabilities read in place: {rejecting} rows + {w['T'] - w['B']} gathers")
+        qb = q_bytes_per_rejection(w, logits_in_place and filtered)
+        h2d += rejecting * qb + 32 * (w["T"] - w["B"])
+        what = "rows" if qb == w["V"] * 4 else f"x {qb} bytes at the kept tokens"
+        notes.append(f"draft probabilities read in place: {rejecting} {what} + {w['T'] - w['B']} gathers")
     q_note = "; ".join(notes) if notes else None
     d2h = 4 * (w["T"] + w["B"])
     from speculative_decoding_rejection_spec_gb300 import workloads as W
