@@ -1074,7 +1074,107 @@ __device__ __forceinline__ float warp_residual_chunk(const ResidualMass<DT, F> &
     constexpr int ES = Elem<DT>::kSize;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int64_t tail = lo;
-    if (((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo)) & 15) == 0) {
+    if (STAGE && DT == 1 && (((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo) |
+                               reinterpret_cast<uintptr_t>(qdst + lo)) & 15) == 0)) {
+        // bf16 rows with q in host memory.  Lane l sums the 8 tokens of group g = g0 + l as the
+        // plain path below does (the same order, so the same sums), but q is loaded as two
+        // contiguous 512-byte spans per 256 tokens (q[4l..4l+3] and q[128+4l..]) and handed to
+        // the lanes that need it by shuffles: a 16-byte load per lane at a 32-byte stride would
+        // make each load instruction fetch every line of a 1 KB span over the host link, and the
+        // two instructions fetch them twice.  U groups are loaded before any copy is stored: a
+        // store might alias a later load as far as the compiler knows.
+        const int64_t ng = (hi - lo) / VEC;
+        const int64_t nfull = ng / 32;  // whole 256-token spans
+        const int src0 = (2 * lane) & 31, src1 = (2 * lane + 1) & 31;
+        const bool lo_half = lane < 16;
+        for (int64_t s0 = 0; s0 < nfull; s0 += U) {
+            uint4 rw[U], qa[U], qb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (s0 + u < nfull) {
+                    const int64_t base = lo + (s0 + u) * 256;
+                    rw[u] = ld_stream(f.row + (base + 8 * lane) * ES);
+                    qa[u] = ld_stream(f.qrow + base + 4 * lane);
+                    qb[u] = ld_stream(f.qrow + base + 128 + 4 * lane);
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (s0 + u < nfull) {
+                    const int64_t base = lo + (s0 + u) * 256;
+                    *reinterpret_cast<uint4 *>(qdst + base + 4 * lane) = qa[u];
+                    *reinterpret_cast<uint4 *>(qdst + base + 128 + 4 * lane) = qb[u];
+                    auto pick = [&](uint32_t a, uint32_t b, int src) {
+                        const uint32_t x = __shfl_sync(kFull, a, src), y = __shfl_sync(kFull, b, src);
+                        return __uint_as_float(lo_half ? x : y);
+                    };
+                    const float q8[8] = {pick(qa[u].x, qb[u].x, src0), pick(qa[u].y, qb[u].y, src0),
+                                         pick(qa[u].z, qb[u].z, src0), pick(qa[u].w, qb[u].w, src0),
+                                         pick(qa[u].x, qb[u].x, src1), pick(qa[u].y, qb[u].y, src1),
+                                         pick(qa[u].z, qb[u].z, src1), pick(qa[u].w, qb[u].w, src1)};
+                    float x[VEC];
+                    unpack<DT>(rw[u], x);
+#pragma unroll
+                    for (int h = 0; h < VEC / 4; ++h) {
+                        acc[0] += fmaxf(0.f, f.pm(x[4 * h + 0]) - q8[4 * h + 0]);
+                        acc[1] += fmaxf(0.f, f.pm(x[4 * h + 1]) - q8[4 * h + 1]);
+                        acc[2] += fmaxf(0.f, f.pm(x[4 * h + 2]) - q8[4 * h + 2]);
+                        acc[3] += fmaxf(0.f, f.pm(x[4 * h + 3]) - q8[4 * h + 3]);
+                    }
+                }
+        }
+        // the groups past the last whole span, as the plain path
+        for (int64_t g = nfull * 32 + lane; g < ng; g += 32) {
+            const int64_t v = lo + g * VEC;
+            float x[VEC];
+            unpack<DT>(ld_stream(f.row + v * ES), x);
+#pragma unroll
+            for (int h = 0; h < VEC / 4; ++h) {
+                const uint4 qw = ld_stream(f.qrow + v + 4 * h);
+                *reinterpret_cast<uint4 *>(qdst + v + 4 * h) = qw;
+                acc[0] += fmaxf(0.f, f.pm(x[4 * h + 0]) - __uint_as_float(qw.x));
+                acc[1] += fmaxf(0.f, f.pm(x[4 * h + 1]) - __uint_as_float(qw.y));
+                acc[2] += fmaxf(0.f, f.pm(x[4 * h + 2]) - __uint_as_float(qw.z));
+                acc[3] += fmaxf(0.f, f.pm(x[4 * h + 3]) - __uint_as_float(qw.w));
+            }
+        }
+        tail = lo + ng * VEC;
+    } else if (STAGE && ((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo) |
+                          reinterpret_cast<uintptr_t>(qdst + lo)) & 15) == 0) {
+        // U groups loaded before any is stored (see above); fp32 q loads are contiguous per warp
+        const int64_t ng = (hi - lo) / VEC;
+        for (int64_t g0 = lane; g0 < ng; g0 += 32 * U) {
+            uint4 rw[U], qw[U][VEC / 4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = g0 + 32 * u;
+                if (g < ng) {
+                    const int64_t v = lo + g * VEC;
+                    rw[u] = ld_stream(f.row + v * ES);
+#pragma unroll
+                    for (int h = 0; h < VEC / 4; ++h)
+                        qw[u][h] = ld_stream(f.qrow + v + 4 * h);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = g0 + 32 * u;
+                if (g < ng) {
+                    const int64_t v = lo + g * VEC;
+                    float x[VEC];
+                    unpack<DT>(rw[u], x);
+#pragma unroll
+                    for (int h = 0; h < VEC / 4; ++h) {
+                        *reinterpret_cast<uint4 *>(qdst + v + 4 * h) = qw[u][h];
+                        acc[0] += fmaxf(0.f, f.pm(x[4 * h + 0]) - __uint_as_float(qw[u][h].x));
+                        acc[1] += fmaxf(0.f, f.pm(x[4 * h + 1]) - __uint_as_float(qw[u][h].y));
+                        acc[2] += fmaxf(0.f, f.pm(x[4 * h + 2]) - __uint_as_float(qw[u][h].z));
+                        acc[3] += fmaxf(0.f, f.pm(x[4 * h + 3]) - __uint_as_float(qw[u][h].w));
+                    }
+                }
+            }
+        }
+        tail = lo + ng * VEC;
+    } else if (((reinterpret_cast<uintptr_t>(f.row + lo * ES) | reinterpret_cast<uintptr_t>(f.qrow + lo)) & 15) == 0) {
         const int64_t ng = (hi - lo) / VEC;
 #pragma unroll(U)
         for (int64_t g = lane; g < ng; g += 32) {

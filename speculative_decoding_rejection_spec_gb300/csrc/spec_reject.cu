@@ -1364,7 +1364,7 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass
 #endif
 #ifndef SPEC_KL_HOST_RESIDUAL_UNROLL
-#define SPEC_KL_HOST_RESIDUAL_UNROLL 8  // the same, draft rows read over the host link
+#define SPEC_KL_HOST_RESIDUAL_UNROLL 2  // the same, draft rows read over the host link (groups loaded before the copies are stored)
 #endif
 #ifndef SPEC_KL_MIN_BLOCKS
 #define SPEC_KL_MIN_BLOCKS 2  // blocks per SM
