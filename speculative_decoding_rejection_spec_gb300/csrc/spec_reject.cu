@@ -1398,8 +1398,13 @@ static_assert(kLThreads * 32 >= kUnitBytes, "a block of KL must cover a whole ch
 //      passes of digit histograms per selection), with the partials of K1F's general path.
 // Whichever step finds it, the cut key and the partials are K1F's, bit for bit.
 
-constexpr int kCutHalfBytes = kUnitBytes / 2;  // a pass moves each chunk in two copies of this size
-static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot as two halves");
+#ifndef SPEC_CUT_PARTS
+#define SPEC_CUT_PARTS 2
+#endif
+constexpr int kCutParts = SPEC_CUT_PARTS;                 // a pass moves each chunk in this many copies,
+constexpr int kCutPartBytes = kUnitBytes / kCutParts;     // of this size, all in flight at once
+static_assert(kCutParts >= 2 && kCutParts <= 8 && kUnitBytes % (16 * kCutParts) == 0, "copies of whole vectors");
+static_assert(kLStages == 1, "the passes of a cut use the warp's one ring slot as kCutParts parts");
 
 constexpr int kCutNarrow = 128;       // largest keys counted per chunk first (one binade of bf16)
 constexpr int kCutNarrowChunks = 64;  // chunks (4096 tokens) a row may have for the per-chunk counts
@@ -1447,8 +1452,8 @@ struct CutSmem {
     int tok;                            // and its token
     int narrow_miss;                    // the block's latest cut lay below the narrow window
     int mid_miss;                       // and below the middle one
-    uint64_t bar[kLWarps][2];           // per warp: one mbarrier per half of its ring slot
-    uint32_t ph[kLWarps];               // per warp: the parity each of the two is waiting for
+    uint64_t bar[kLWarps][kCutParts];   // per warp: one mbarrier per part of its ring slot
+    uint32_t ph[kLWarps];               // per warp: the parity each of them is waiting for (a bit each)
 };
 constexpr size_t kLCutSmem = kLSmem + sizeof(CutSmem);
 
@@ -1608,8 +1613,8 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         const uint32_t sg = (uint32_t)((int32_t)(b16 << 16) >> 31);
         return kmax - (0x8000u + (((b16 & 0x7fffu) ^ sg) - sg));
     };
-    // A pass over this warp's chunks c = warp, warp + nw, ...: each chunk in two copies of at
-    // most 4 KB (TMA, into the two halves of the warp's ring slot, both in flight), then
+    // A pass over this warp's chunks c = warp, warp + nw, ...: each chunk in kCutParts copies of
+    // at most kCutPartBytes (TMA, into the parts of the warp's ring slot, all in flight), then
     // start(c), fv(st, nv, c, lo) for the nv 16-byte vectors st[] of each copy in shared memory,
     // elements lo, lo + 1, ... of the row (the warp's lanes take vectors lane, lane + 32, ...:
     // per_vec) and fe(bits)
@@ -1617,34 +1622,34 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     // read (empty copies keep the barriers' phases in step).  A copy that does not land in time
     // sets C.abort; the pass still returns through every barrier of the block.
     auto pass = [&](auto want, auto start, auto fv, auto fe, auto done) {
-        constexpr int kHalf = kCutHalfBytes / 2;  // bf16 elements per copy
+        constexpr int kPart = kCutPartBytes / 2;  // bf16 elements per copy
         const int nmine = warp < P.nchunks ? (P.nchunks - 1 - warp) / nw + 1 : 0;
-        const int n = 2 * nmine;
+        const int n = kCutParts * nmine;
         uint32_t ph = C.ph[warp];
         auto range = [&](int u, int &c, int &lo, int &hi) {
-            c = warp + nw * (u >> 1);
+            c = warp + nw * (u / kCutParts);
             const int c0 = c * P.chunk, c1 = min(P.V, c0 + P.chunk);
-            lo = min(c1, c0 + (u & 1) * kHalf);
-            hi = min(c1, lo + kHalf);
+            lo = min(c1, c0 + (u % kCutParts) * kPart);
+            hi = min(c1, lo + kPart);
         };
         auto issue = [&](int u) {  // lane 0
             int c, lo, hi;
             range(u, c, lo, hi);
             const uint32_t bytes = want(c) ? ((uint32_t)(hi - lo) * 2u) & ~15u : 0u;
-            uint64_t *bar = &C.bar[warp][u & 1];
+            uint64_t *bar = &C.bar[warp][u % kCutParts];
             mbar_arrive_expect_tx(bar, bytes);
             if (bytes)
-                bulk_g2s(P.slot + (u & 1) * kCutHalfBytes, row + (size_t)lo * 2, bytes, bar);
+                bulk_g2s(P.slot + (u % kCutParts) * kCutPartBytes, row + (size_t)lo * 2, bytes, bar);
         };
         if (lane == 0)
-            for (int u = 0; u < 2 && u < n; ++u)
+            for (int u = 0; u < kCutParts && u < n; ++u)
                 issue(u);
         for (int u = 0; u < n; ++u) {
-            const int sl = u & 1;
+            const int sl = u % kCutParts;
             if (!__all_sync(kFull, mbar_wait(&C.bar[warp][sl], (ph >> sl) & 1u, P.err))) {
                 if (lane == 0) {  // let the copies still in flight land before the slot is reused
-                    for (int u2 = u; u2 < u + 2 && u2 < n; ++u2)
-                        mbar_wait(&C.bar[warp][u2 & 1], (ph >> (u2 & 1)) & 1u, P.err);
+                    for (int u2 = u; u2 < u + kCutParts && u2 < n; ++u2)
+                        mbar_wait(&C.bar[warp][u2 % kCutParts], (ph >> (u2 % kCutParts)) & 1u, P.err);
                     C.abort = 1;
                 }
                 break;
@@ -1655,17 +1660,17 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             if (want(c)) {
                 if (sl == 0)
                     start(c);
-                const uint4 *st = reinterpret_cast<const uint4 *>(P.slot + sl * kCutHalfBytes);
+                const uint4 *st = reinterpret_cast<const uint4 *>(P.slot + sl * kCutPartBytes);
                 const int nv = (hi - lo) >> 3;
                 fv(st, nv, c, lo);
                 for (int i = lo + nv * 8 + lane; i < hi; i += 32)
                     fe((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + i));
-                if (sl == 1)
+                if (sl == kCutParts - 1)
                     done(c);
             }
-            __syncwarp();  // the half is consumed: refill it
-            if (lane == 0 && u + 2 < n)
-                issue(u + 2);
+            __syncwarp();  // the part is consumed: refill it
+            if (lane == 0 && u + kCutParts < n)
+                issue(u + kCutParts);
         }
         if (lane == 0)
             C.ph[warp] = ph;
@@ -2291,7 +2296,7 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
     if (threadIdx.x < kLWarps * kLStages)
         mbar_init(&full[threadIdx.x], 1);
     if constexpr (CUT) {
-        if (threadIdx.x < 2 * kLWarps)
+        if (threadIdx.x < kCutParts * kLWarps)
             mbar_init(&C.bar[0][0] + threadIdx.x, 1);
         if (threadIdx.x < kLWarps)
             C.ph[threadIdx.x] = 0;
