@@ -9,7 +9,9 @@ Default workload: the large-batch sweep point B=1024, K=8, V=128256, bf16 target
 logits, explicit fp32 draft probabilities, temperature 0.7 (2.36 GB of logits +
 4.2 GB of draft probabilities per step: larger than L2, so no flush is needed).
 Exactly --steps calls are timed with CUDA events; SM clocks and clock-event reasons are
-read through NVML every 0.5 ms during that region.
+read through NVML every 0.5 ms during that region (`clocks`), and again over half a
+second of the same calls right after it (`clocks_window`: a 20-step region lasts a few
+milliseconds, too few samples to show a throttle).
 
 The JSON line also carries `per_config`: the other workloads of the target's list
 (tiny, greedy, probabilistic, deterministic, large-128, large-512), each timed for
@@ -532,6 +534,7 @@ def main():
             "hbm_gbs_effective": round(m["alg_bytes"] / (ms / 1e3) / 1e9, 1),
             "stage_ms": [round(x, 4) for x in m["stage_ms"]], "stages": m["stages"],
             "roofline": roofline, "gpu_launches": m["launches"] * args.steps, "clocks": m["clocks"],
+            "clocks_window": m["clocks_window"],
             "rows_read_per_step": m["rows_read"], "rows_total": int(w["T"]),
             "blocks_per_request": m["blocks_per_request"]}
 
@@ -622,6 +625,25 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
     clk = clocks.stop()
     if barrier:
         torch.distributed.barrier()
+    clk_window = None
+    if min_seconds <= 0:
+        # a few-step timed region lasts milliseconds, a handful of clock samples: the same call
+        # repeated for half a second right after it, outside the timed region, samples the clocks
+        # the kernels run at (reported beside the timed region's own samples)
+        window = clock_sampler(dev)
+        window.start()
+        t0, n = time.perf_counter(), 0
+        while time.perf_counter() - t0 < 0.5:
+            for _ in range(20):
+                if flush is not None:
+                    flush.zero_()
+                call()
+            n += 20
+            torch.cuda.synchronize()
+        clk_window = window.stop()
+        if clk_window is not None:
+            clk_window["calls"] = n
+            clk_window["seconds"] = round(time.perf_counter() - t0, 3)
     # per-kernel times: the same calls with an event after each kernel
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(min(steps, 200))]
     for row in ev:
@@ -668,7 +690,8 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
            "l2": ("L2 flushed before every call (inputs smaller than twice L2)" if flush is not None
                   else "inputs larger than twice L2 (no flush)"),
            "dom_bytes": dom_bytes, "dom_name": dom_name, "alg_bytes": alg, "rows_read": rows_read,
-           "kernels": nk, "launches": launches, "clocks": clk, "lazy": lazy, "blocks_per_request": bpr}
+           "kernels": nk, "launches": launches, "clocks": clk, "clocks_window": clk_window, "lazy": lazy,
+           "blocks_per_request": bpr}
     del d, buf
     torch.cuda.empty_cache()
     return out
