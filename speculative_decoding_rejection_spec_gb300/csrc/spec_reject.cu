@@ -2965,6 +2965,49 @@ __global__ void __launch_bounds__(kThreads) debug_argmax_kernel(Params P, float 
     }
 }
 
+#ifdef SPEC_KL_CUT_VARIANT
+// ---------------------------------------------------------------------------------------
+// This file compiled a second time (spec_reject_cut16.cu) with kLWarps = 16: the first-
+// rejection pass with cuts, one 16-warp block per SM.  Only its launcher and occupancy query
+// are visible to the other translation unit; everything else here has internal linkage.
+// ---------------------------------------------------------------------------------------
+}  // namespace
+
+// Blocks of the 16-warp pass with cuts that fit on one SM (0: none), after raising its
+// dynamic shared-memory limit.
+cudaError_t lazy_cut16_blocks_per_sm(int *blocks)
+{
+    cudaError_t e = cudaFuncSetAttribute(lazy_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kLCutSmem);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, lazy_kernel<1, false, true>, kLThreads, kLCutSmem);
+}
+
+// Launch of the 16-warp pass with cuts (rows in device memory), with `pdl` as a programmatic
+// dependent launch of the layout check.
+cudaError_t launch_lazy_cut16(const Params &P, int grid, bool pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kLThreads, 1, 1);
+    cfg.dynamicSmemBytes = kLCutSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, lazy_kernel<1, false, true>, P);
+}
+}  // namespace specrej
+#else
+}  // namespace
+// The 16-warp pass with cuts, from the second translation unit of this file.
+cudaError_t lazy_cut16_blocks_per_sm(int *blocks);
+cudaError_t launch_lazy_cut16(const Params &P, int grid, bool pdl, cudaStream_t stream);
+namespace {
+
 // ---------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------
@@ -2976,6 +3019,7 @@ struct DeviceInfo {
     int blocks_wr[2] = {0, 0};
     int blocks_lazy[2] = {0, 0};
     int blocks_lazy_cut = 0;       // KL with cuts (bf16)
+    int blocks_lazy_cut16 = 0;     // the same with 16-warp blocks (spec_reject_cut16.cu)
     int blocks_lazy_cut_host = 0;  // the same, rows in host memory
     int clusters_lazy[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // KL with clusters of 1, 2, 4, 8 blocks
 };
@@ -3092,6 +3136,8 @@ template <int DT> cudaError_t fill_info(DeviceInfo &di)
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_lazy_cut_host, lazy_kernel<1, true, true>,
                                                                kLThreads, kLCutSmem)))
             return e;
+        if ((e = lazy_cut16_blocks_per_sm(&di.blocks_lazy_cut16)))
+            return e;
     }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.blocks_residual[DT], residual_kernel<DT, false>, kThreads, 0);
 }
@@ -3137,6 +3183,10 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // launch with two blocks per request (see run()): a share of the blocks the first launch holds,
 // for batches of at least three times that many requests whose rows give each warp of a pair a
 // chunk; 0 otherwise.
+#ifndef SPEC_KL_CUT16_PER_SM
+#define SPEC_KL_CUT16_PER_SM 4  // requests per SM up to which the pass with cuts runs 16-warp blocks
+#endif
+
 #ifndef SPEC_KL_TAIL_PERMILLE
 #define SPEC_KL_TAIL_PERMILLE 300  // tail requests per 1000 blocks of the first launch
 #endif
@@ -3335,11 +3385,16 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             P.qstage = q ? q_stage : nullptr;
         }
         if (filtered) {
-            const int gridL =
-                (int)clamp_grid((int64_t)di->sms * (rows_in_host ? di->blocks_lazy_cut_host : di->blocks_lazy_cut), B);
-            const cudaError_t e = rows_in_host
-                                      ? launch_lazy(lazy_kernel<1, true, true>, gridL, 1, kLCutSmem, P, pdl, stream)
-                                      : launch_lazy(lazy_kernel<1, false, true>, gridL, 1, kLCutSmem, P, pdl, stream);
+            // batches of at most SPEC_KL_CUT16_PER_SM requests per SM: 16-warp blocks, one per SM,
+            // which cut each reached row twice as fast (the row's cut takes most of its time)
+            const bool w16 = !rows_in_host && di->blocks_lazy_cut16 > 0 &&
+                             (int64_t)B <= (int64_t)di->sms * SPEC_KL_CUT16_PER_SM;
+            const int gridL = (int)clamp_grid(
+                (int64_t)di->sms * (rows_in_host ? di->blocks_lazy_cut_host
+                                                 : (w16 ? di->blocks_lazy_cut16 : di->blocks_lazy_cut)), B);
+            const cudaError_t e = rows_in_host ? launch_lazy(lazy_kernel<1, true, true>, gridL, 1, kLCutSmem, P, pdl, stream)
+                                  : w16        ? launch_lazy_cut16(P, gridL, pdl, stream)
+                                               : launch_lazy(lazy_kernel<1, false, true>, gridL, 1, kLCutSmem, P, pdl, stream);
             mark();
             return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
         }
@@ -3899,3 +3954,5 @@ int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_pr
 }
 
 }  // extern "C"
+
+#endif  // SPEC_KL_CUT_VARIANT
