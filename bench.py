@@ -14,9 +14,11 @@ second of the same calls right after it (`clocks_window`: a 20-step region lasts
 milliseconds, too few samples to show a throttle).
 
 The JSON line also carries `per_config`: the other workloads of the target's list
-(tiny, greedy, probabilistic, deterministic, large-128, large-512), each timed for
-about half a second of calls in the same run (L2 flushed before every call when the
-inputs are smaller than twice L2), with its dominant kernel's roofline fraction.
+(tiny, greedy, probabilistic, deterministic, large-128, large-512) and the cut mode
+(large-1024 and large-512 with top-k 50 / top-p 0.9, large-1024 with top-p 0.9 alone),
+each timed for about half a second of calls in the same run (L2 flushed before every
+call when the inputs are smaller than twice L2), with its dominant kernel's roofline
+fraction.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle instead (a bounded
 sample of the same workload on the host cores).
@@ -708,6 +710,8 @@ def roofline_of(m, peak, peak_kind, workload_key):
 
 
 PER_CONFIG = ["tiny", "greedy", "probabilistic", "deterministic", "large-128", "large-512"]
+# the same measurement with top-k / top-p on the target (every request): (workload, top-k, top-p)
+PER_CONFIG_CUT = [("large-1024", 50, 0.9), ("large-512", 50, 0.9), ("large-1024", None, 0.9)]
 
 
 def per_config(args, dev, peak, peak_kind):
@@ -715,12 +719,23 @@ def per_config(args, dev, peak, peak_kind):
     about half a second of calls): step time, the dominant kernel and its roofline fraction."""
     from speculative_decoding_rejection_spec_gb300 import workloads as W
     out = {}
-    for name in PER_CONFIG:
-        w = W.generate(name)
-        m = measure(w, dev, 20, max(args.warmup, 3), min_seconds=0.5)
+    runs = [(n, n, None, None) for n in PER_CONFIG]
+    runs += [(n + (f"+k{tk}" if tk else "") + (f"+p{tp}" if tp else ""), n, tk, tp) for n, tk, tp in PER_CONFIG_CUT]
+    base = {}
+    for key, name, tk, tp in runs:
+        if name not in base:  # one draw of each workload; the cuts only add their per-request arrays
+            base.clear()
+            base[name] = W.generate(name)
+        w = dict(base[name])
+        B = w["B"]
+        if tk is not None:
+            w["top_k"] = np.full(B, tk, dtype=np.int32)
+        if tp is not None:
+            w["top_p"] = np.full(B, tp, dtype=np.float32)
+        m = measure(w, dev, 20, max(args.warmup, 3), tk_tp=(tk, tp), min_seconds=0.5)
         ms = m["total_ms"] / m["steps"]
-        rf = roofline_of(m, peak, peak_kind, name)
-        out[name] = {"ms_per_step": round(ms, 5), "value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT,
+        rf = roofline_of(m, peak, peak_kind, key)
+        out[key] = {"ms_per_step": round(ms, 5), "value": W.total_drafts(w) / (ms / 1e3), "unit": UNIT,
                      "steps": m["steps"], "kernel": rf["kernel"], "kernel_ms": rf["ms_per_launch"],
                      "algorithmic_bytes": m["dom_bytes"], "achieved_gbs": rf["achieved"], "frac": rf["frac"],
                      "frac_of_nominal_8tbs": rf["frac_of_nominal_8tbs"], "traffic": rf["traffic"],
