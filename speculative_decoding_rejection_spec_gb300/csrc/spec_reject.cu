@@ -25,9 +25,14 @@
 //       the located chunk) and warp 0 writes the outputs.  Batches too small to fill the GPU
 //       one block per request run with thread-block clusters of 2, 4 or 8 blocks per request
 //       (chunks spread over every warp of the cluster, partials gathered in the leader block
-//       through distributed shared memory).  With cuts, each reached row is cut in the block
-//       (kl_cut_row); with rows in host memory, rows are read over the host link with 16-byte
-//       loads and copied to the device for the residual pass and the draw.
+//       through distributed shared memory).  The last requests of a large batch run in a
+//       second launch, two blocks each, chained to the first.  With cuts, each reached row is
+//       cut in the block (kl_cut_row: counts over a window of the largest keys, marked with
+//       packed compares), and the output row's residual and draw read only its listed kept
+//       tokens when they are few (kl_list_draw); batches of at most 4 requests per SM take a
+//       16-warp build of this kernel (spec_reject_cut16.cu compiles this file again).  With
+//       rows in host memory, rows are read over the host link with 16-byte loads and copied to
+//       the device for the residual pass and the draw.
 //   K1  rowstats_wr_kernel / rowstats_kernel, the full pass's row statistics: every chunk of
 //       every row, warp-private TMA rings (register-staged 16-byte loads for misaligned rows);
 //       block 0 checks the layout.
