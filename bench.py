@@ -675,10 +675,12 @@ def measure(w, dev, steps, warmup, tk_tp=(None, None), barrier=False, min_second
         dom_name = ("KL: lazy_kernel (request queue; rows streamed through warp-private TMA rings up to the first "
                     "rejection; residual pass and draw in the same block" +
                     (f"; each request split over a cluster of {bpr} blocks" if bpr > 1 else "") +
-                    ("; the last requests two blocks each in a chained second launch, timed with the first"
+                    (("; the last requests in a chained second launch (" +
+                      ("16-warp blocks" if filtered else "two blocks each") + "), timed with the first")
                      if launches > nk else "") + ")")
         if filtered:
-            dom_name += "; each reached row cut in the block (key-offset counts, per-chunk partials)"
+            dom_name += ("; each reached row cut in the block (key-offset counts of marked tokens), the output row "
+                         "drawn from its kept tokens")
         alg = dom_bytes
     else:
         rows_read = int(w["T"])

@@ -393,11 +393,12 @@ int spec_reject_num_kernels(spec_dtype logits_dtype, int32_t B, int has_draft_pr
 int spec_reject_blocks_per_request(spec_dtype logits_dtype, int32_t B, int32_t V);
 
 /* Kernel launches one call makes on the current device (16-byte-aligned rows in device memory):
- * spec_reject_num_kernels() stages, of which the first-rejection pass of a large batch without
- * top-k / top-p is two launches (most requests one block each, the last ones two blocks each in
- * a second launch chained by programmatic dependent launch, which takes SM slots as the first
- * launch's blocks run out of requests).  The profiled entry records its events per stage.  The
- * pages have no counterpart: this reports the launch shape, for measurements. */
+ * spec_reject_num_kernels() stages, of which the first-rejection pass of a large batch is two
+ * launches (most requests one block each, the last ones in a second launch chained by
+ * programmatic dependent launch, which takes SM slots as the first launch's blocks run out of
+ * requests: without top-k / top-p two blocks per request, with them a 16-warp block per
+ * request).  The profiled entry records its events per stage.  The pages have no counterpart:
+ * this reports the launch shape, for measurements. */
 int spec_reject_launches_per_call(spec_dtype logits_dtype, int32_t B, int32_t V, int has_draft_probs,
                                   int has_filters);
 

@@ -3192,6 +3192,10 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 #define SPEC_KL_CUT16_PER_SM 4  // requests per SM up to which the pass with cuts runs 16-warp blocks
 #endif
 
+#ifndef SPEC_KL_CUT_TAIL_PERMILLE
+#define SPEC_KL_CUT_TAIL_PERMILLE 1000  // requests per 1000 SMs run by the 16-warp build after a large batch's cut pass
+#endif
+
 #ifndef SPEC_KL_TAIL_PERMILLE
 #define SPEC_KL_TAIL_PERMILLE 300  // tail requests per 1000 blocks of the first launch
 #endif
@@ -3202,6 +3206,19 @@ int lazy_tail_requests(const DeviceInfo &di, int DT, int32_t B, int nchunks)
     if (tail < 1 || di.clusters_lazy[DT][1] <= 0 || (kLWarps << 1) > nchunks || (int64_t)B < 3 * tail + blocks)
         return 0;
     return (int)tail;
+}
+
+// Requests of a batch with cuts on device rows that the 16-warp build of the pass takes: all of
+// them for batches of at most SPEC_KL_CUT16_PER_SM requests per SM, else the last
+// SPEC_KL_CUT_TAIL_PERMILLE per 1000 SMs, in a second launch chained to the 8-warp one; 0
+// without that build.
+int64_t lazy_cut16_requests(const DeviceInfo &di, int32_t B)
+{
+    if (di.blocks_lazy_cut16 <= 0)
+        return 0;
+    if ((int64_t)B <= (int64_t)di.sms * SPEC_KL_CUT16_PER_SM)
+        return B;
+    return (int64_t)di.sms * SPEC_KL_CUT_TAIL_PERMILLE / 1000;
 }
 
 int lazy_cluster_log2(const DeviceInfo &di, int DT, int32_t B, int nchunks)
@@ -3390,16 +3407,30 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             P.qstage = q ? q_stage : nullptr;
         }
         if (filtered) {
-            // batches of at most SPEC_KL_CUT16_PER_SM requests per SM: 16-warp blocks, one per SM,
-            // which cut each reached row twice as fast (the row's cut takes most of its time)
-            const bool w16 = !rows_in_host && di->blocks_lazy_cut16 > 0 &&
-                             (int64_t)B <= (int64_t)di->sms * SPEC_KL_CUT16_PER_SM;
+            // small batches: 16-warp blocks, one per SM, which cut each reached row twice as fast
+            // (a row's cut takes most of its time, bound by instruction issue inside the block)
+            const int64_t n16 = rows_in_host ? 0 : lazy_cut16_requests(*di, B);
+            const bool w16 = n16 == (int64_t)B;
             const int gridL = (int)clamp_grid(
                 (int64_t)di->sms * (rows_in_host ? di->blocks_lazy_cut_host
                                                  : (w16 ? di->blocks_lazy_cut16 : di->blocks_lazy_cut)), B);
-            const cudaError_t e = rows_in_host ? launch_lazy(lazy_kernel<1, true, true>, gridL, 1, kLCutSmem, P, pdl, stream)
-                                  : w16        ? launch_lazy_cut16(P, gridL, pdl, stream)
-                                               : launch_lazy(lazy_kernel<1, false, true>, gridL, 1, kLCutSmem, P, pdl, stream);
+            // larger batches: 8-warp blocks (two per SM), except the last requests, which run in a
+            // second launch of the 16-warp build chained to the first: its blocks take SMs as the
+            // first launch's blocks run out of requests, and finish their chains faster
+            const int64_t tail16 = w16 ? 0 : n16;
+            Params Pm = P;
+            Pm.r_end = (int32_t)(B - tail16);
+            cudaError_t e = rows_in_host ? launch_lazy(lazy_kernel<1, true, true>, gridL, 1, kLCutSmem, P, pdl, stream)
+                            : w16        ? launch_lazy_cut16(P, gridL, pdl, stream)
+                                         : launch_lazy(lazy_kernel<1, false, true>, gridL, 1, kLCutSmem, Pm, pdl, stream);
+            if (e == cudaSuccess && tail16 > 0) {
+                Params Pt = P;
+                Pt.r_begin = (int32_t)(B - tail16);
+                Pt.qslot = 3;
+                Pt.wait_prior = 0;
+                e = launch_lazy_cut16(Pt, (int)clamp_grid((int64_t)di->sms * di->blocks_lazy_cut16, tail16), true,
+                                      stream);
+            }
             mark();
             return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
         }
@@ -3943,9 +3974,13 @@ int spec_reject_launches_per_call(spec_dtype logits_dtype, int32_t B, int32_t V,
     Plan pl;
     DeviceInfo *di;
     const int stages = spec_reject_num_kernels(logits_dtype, B, has_draft_probs, has_filters);
-    if (B < 1 || has_filters || !make_plan(B, B, V, logits_dtype, has_draft_probs, &pl) || device_info(&di) != cudaSuccess)
+    if (B < 1 || !make_plan(B, B, V, logits_dtype, has_draft_probs, &pl) || device_info(&di) != cudaSuccess)
         return stages;
     const int DT = logits_dtype == SPEC_BF16 ? 1 : 0;
+    if (has_filters) {  // with cuts: bf16 rows of at least SPEC_KL_MIN_REQUESTS requests take the pass
+        const int64_t n16 = lazy_cut16_requests(*di, B);
+        return stages == 2 && n16 > 0 && n16 < B ? 3 : stages;
+    }
     if (lazy_cluster_log2(*di, DT, B, pl.nchunks) == 0 && lazy_tail_requests(*di, DT, B, pl.nchunks) > 0)
         return 3;  // the layout check, the first-rejection pass, its chained second launch
     return stages;

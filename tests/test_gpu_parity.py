@@ -498,3 +498,9 @@ def test_launch_shapes():
     assert shapes["large-512"] == (1, 2) and shapes["deterministic"] == (1, 2), shapes
     assert shapes["large-128"] == (2, 2) and shapes["probabilistic"] == (4, 2), shapes
     assert shapes["greedy"] == (1, 2) and shapes["tiny"] == (1, 2), shapes
+    # with top-k / top-p: bf16 batches of at least 64 requests take the first-rejection pass, large
+    # ones with their last requests in a chained launch of the 16-warp build; fp32 the full pass
+    cut = {n: binding.launches_per_call(W.CONFIGS[n]["B"], W.CONFIGS[n]["V"], True, True,
+                                        binding.BF16 if W.CONFIGS[n]["dtype"] == "bf16" else binding.F32)
+           for n in ("large-1024", "large-512", "large-128", "probabilistic")}
+    assert cut == {"large-1024": 3, "large-512": 2, "large-128": 2, "probabilistic": 4}, cut
