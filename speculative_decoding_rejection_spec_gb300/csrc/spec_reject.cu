@@ -63,9 +63,17 @@
 
 namespace specrej {
 namespace {
+
+// Programmatic dependent launch: a kernel launched as the dependent of the one before it on the
+// stream may be scheduled while that one still runs (once all its blocks have started and
+// allowed it); it waits here for that kernel's completion and writes before reading anything.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 template <int DT>
 __global__ void __launch_bounds__(kThreads, SPEC_LDG_MIN_BLOCKS) rowstats_kernel(Params P, int force_argmax)
 {
+    allow_dependents();  // the next kernel of the full pass may take SM slots as these blocks finish
     if (blockIdx.x == 0 && force_argmax != kArgmaxKeepErrors)
         validate_layout(P);
     if (P.B == 0)
@@ -114,6 +122,7 @@ constexpr int kWrThreads = kWrWarps * 32;
 template <int DT>
 __global__ void __launch_bounds__(kWrThreads, SPEC_WR_MIN_BLOCKS) rowstats_wr_kernel(Params P, int force_argmax)
 {
+    allow_dependents();  // the next kernel of the full pass may take SM slots as these blocks finish
     constexpr int VEC = Elem<DT>::kVec;
     constexpr int ES = Elem<DT>::kSize;
     extern __shared__ __align__(128) unsigned char ring[];
@@ -461,6 +470,8 @@ __device__ __forceinline__ void find_crossing(FilterShared &S, int nb, unsigned 
 template <int DT>
 __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(Params P, int csize)
 {
+    allow_dependents();
+    wait_for_prerequisite();  // the row statistics
     constexpr int KEY_BITS = DT ? 16 : 32;
     constexpr int ES = Elem<DT>::kSize;
     __shared__ FilterShared S;
@@ -1053,6 +1064,8 @@ __device__ __forceinline__ int warp_combine_argmax(const float2 *pp, int nchunks
 template <int DT, bool F>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 {
+    allow_dependents();
+    wait_for_prerequisite();  // the row statistics (and the cuts)
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (r >= P.B)
@@ -1282,6 +1295,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(Params P)
 template <int DT, bool F>
 __global__ void __launch_bounds__(kThreads, 4) residual_kernel(Params P)
 {
+    wait_for_prerequisite();  // the decisions (and the staged draft rows)
     const int lane = threadIdx.x & 31;
     const int64_t nunits = (int64_t)P.B * P.nchunks;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
@@ -2204,10 +2218,6 @@ __device__ __noinline__ int kl_list_draw(CutSmem &C, int chunk, int mode, const 
 }
 
 
-// Programmatic dependent launch: KL may be scheduled while the layout check still runs; it
-// waits here for that kernel's writes (the error word, the request queue) before reading them.
-__device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Layout check and request-queue reset before KL (one block).
 __global__ void __launch_bounds__(256) lazy_init_kernel(Params P)
@@ -2671,6 +2681,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
 // interleaves those host loads with its own arithmetic and moves half the bandwidth.
 __global__ void __launch_bounds__(kThreads) stage_rows_kernel(Params P, float *stage)
 {
+    allow_dependents();
+    wait_for_prerequisite();  // the decisions
     constexpr int kPiece = 4096;  // floats per unit
     constexpr int kUnroll = 8;
     const int lane = threadIdx.x & 31;
@@ -3069,6 +3081,25 @@ cudaError_t launch_lazy(K kernel, int grid, int cs, size_t smem, const Params &P
     return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
+// Launch of a kernel of the full pass, as a programmatic dependent launch of the kernel before it
+// on the stream when `pdl` (the kernel waits for that one's writes itself).
+template <class... A, class... B>
+cudaError_t launch_dep(void (*kernel)(A...), int grid, int block, size_t smem, bool pdl, cudaStream_t stream,
+                       B... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int DT, int CS> cudaError_t launch_lazy_cluster(const Params &P, int clusters, bool pdl, cudaStream_t stream)
 {
     return launch_lazy(lazy_kernel<DT, false, false, CS>, clusters * CS, CS, kLSmem, P, pdl, stream);
@@ -3287,7 +3318,7 @@ void launch_rowstats(int DT, const Params &P, const DeviceInfo &di, int64_t T, i
 }
 
 // K1F: one cluster per target row (blocks of unfiltered rows exit at once).
-cudaError_t launch_filter(int DT, const Params &P, int64_t T, int nchunks, cudaStream_t stream)
+cudaError_t launch_filter(int DT, const Params &P, int64_t T, int nchunks, cudaStream_t stream, bool pdl)
 {
     const int csize = (nchunks + kFilterMaxChunksPerBlock - 1) / kFilterMaxChunksPerBlock;
     const int cpc = (nchunks + csize - 1) / csize;
@@ -3297,13 +3328,15 @@ cudaError_t launch_filter(int DT, const Params &P, int64_t T, int nchunks, cudaS
     cfg.dynamicSmemBytes = 0;
     (void)cpc;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return DT ? cudaLaunchKernelEx(&cfg, filter_kernel<1>, P, csize) : cudaLaunchKernelEx(&cfg, filter_kernel<0>, P, csize);
 }
 
@@ -3380,8 +3413,10 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     // stage events: [0] before K1, then one after each kernel launched: K1, K1F (filtered
     // calls only), K2, K3 (explicit draft probabilities only)
     int evi = 0;
+    bool marked = false;  // the latest mark() recorded an event (the next launch then is no dependent launch)
     auto mark = [&]() {
-        if (evi < nev && ev[evi])
+        marked = evi < nev && ev[evi];
+        if (marked)
             cudaEventRecord(ev[evi], stream);
         ++evi;
     };
@@ -3482,11 +3517,14 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
     }
     if (rows_in_host)
         return SPEC_ERR_INVALID_ARG;  // only the first-rejection pass reads rows in host memory
+    // the full pass: K1, then K1F / K2 / K3 each as a programmatic dependent launch of the kernel
+    // before it (no stage event between them)
     mark();
     launch_rowstats(DT, P, *di, T, pl.nchunks, logits, lstride, gridA, stream, 0);
     mark();
+    bool chain = true;  // the kernel just launched is one of the pass's (a debug kernel is not)
     if (filtered && T > 0 && B > 0) {
-        if (launch_filter(DT, P, T, pl.nchunks, stream) != cudaSuccess)
+        if (launch_filter(DT, P, T, pl.nchunks, stream, chain && !marked) != cudaSuccess)
             return SPEC_ERR_CUDA;
         mark();
     }
@@ -3496,30 +3534,37 @@ spec_status run(const void *logits, spec_dtype dt, int64_t T, int32_t V, int64_t
             debug_soft_kernel<1><<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s);
         else
             debug_soft_kernel<0><<<g, kThreads, 0, stream>>>(P, dbg_m, dbg_s);
+        chain = false;
     }
     if (B > 0) {
         const bool F = P.thr != nullptr;
-        if (DT)
-            (F ? finalize_kernel<1, true> : finalize_kernel<1, false>)<<<gridB, kThreads, 0, stream>>>(P);
-        else
-            (F ? finalize_kernel<0, true> : finalize_kernel<0, false>)<<<gridB, kThreads, 0, stream>>>(P);
+        cudaError_t e = DT ? launch_dep(F ? finalize_kernel<1, true> : finalize_kernel<1, false>, gridB, kThreads, 0,
+                                        chain && !marked, stream, P)
+                           : launch_dep(F ? finalize_kernel<0, true> : finalize_kernel<0, false>, gridB, kThreads, 0,
+                                        chain && !marked, stream, P);
+        if (e != cudaSuccess)
+            return SPEC_ERR_CUDA;
         mark();
         if (q) {
             Params P3 = P;
             if (q_stage) {  // q in host memory: stage the rows K3 reads into device memory first
                 const int64_t sunits = (int64_t)B * ((V + 4095) / 4096);
                 const int gridS = (int)clamp_grid((int64_t)di->sms * 8, (sunits + kWarps - 1) / kWarps);
-                stage_rows_kernel<<<gridS, kThreads, 0, stream>>>(P, q_stage);
+                if (launch_dep(stage_rows_kernel, gridS, kThreads, 0, !marked, stream, P, q_stage) != cudaSuccess)
+                    return SPEC_ERR_CUDA;
                 P3.q = q_stage;
                 P3.qstride = V;
             }
             const int64_t runits = (int64_t)B * pl.nchunks;
             const int64_t rfull = (int64_t)di->sms * (di->blocks_residual[DT] > 0 ? di->blocks_residual[DT] : 1);
             const int gridC = (int)clamp_grid(rfull, (runits + kWarps - 1) / kWarps);
-            if (DT)
-                (F ? residual_kernel<1, true> : residual_kernel<1, false>)<<<gridC, kThreads, 0, stream>>>(P3);
-            else
-                (F ? residual_kernel<0, true> : residual_kernel<0, false>)<<<gridC, kThreads, 0, stream>>>(P3);
+            const bool pdl3 = q_stage ? true : !marked;  // after the staging kernel, or after K2
+            e = DT ? launch_dep(F ? residual_kernel<1, true> : residual_kernel<1, false>, gridC, kThreads, 0, pdl3,
+                                stream, P3)
+                   : launch_dep(F ? residual_kernel<0, true> : residual_kernel<0, false>, gridC, kThreads, 0, pdl3,
+                                stream, P3);
+            if (e != cudaSuccess)
+                return SPEC_ERR_CUDA;
             mark();
         }
     }
