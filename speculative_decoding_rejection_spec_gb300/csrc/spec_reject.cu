@@ -1380,7 +1380,10 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #define SPEC_KL_MIN_REQUESTS 64  // smaller batches with cuts or host rows: the full pass is faster
 #endif
 #ifndef SPEC_KL_RESIDUAL_UNROLL
-#define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass
+#define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass (fp32 rows)
+#endif
+#ifndef SPEC_KL_RESIDUAL_UNROLL_BF16
+#define SPEC_KL_RESIDUAL_UNROLL_BF16 16  // the same for bf16 rows (measured: 8 -> 16 took 1-2% off large batches)
 #endif
 #ifndef SPEC_KL_HOST_RESIDUAL_UNROLL
 #define SPEC_KL_HOST_RESIDUAL_UNROLL 2  // the same, draft rows read over the host link (groups loaded before the copies are stored)
@@ -2572,7 +2575,9 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 const float z = (HOST && qstage_j)
                                     ? warp_residual_chunk<DT, CUT, SPEC_KL_HOST_RESIDUAL_UNROLL, true>(f, lo, hi, lane,
                                                                                                        qstage_j)
-                                    : warp_residual_chunk<DT, CUT, SPEC_KL_RESIDUAL_UNROLL>(f, lo, hi, lane);
+                                    : warp_residual_chunk<DT, CUT,
+                                                          DT ? SPEC_KL_RESIDUAL_UNROLL_BF16 : SPEC_KL_RESIDUAL_UNROLL>(
+                                          f, lo, hi, lane);
                 if (lane == 0)
                     lrm[c] = z;
             }
