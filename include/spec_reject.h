@@ -311,7 +311,9 @@ spec_status spec_reject_sample_noalloc(const void *target_logits, spec_dtype log
  * count that "投机解码（Speculative Decoding）端到端深挖" §13 divides by:
  *   accept rate   alpha = counters[NUM_ACCEPTED_TOKENS] / counters[NUM_DRAFT_TOKENS]
  *   accept length tau   = (counters[NUM_ACCEPTED_TOKENS] + counters[NUM_VERIFIES]) / counters[NUM_VERIFIES]
- * (the bonus or recovered token counts in tau, not in alpha).
+ * (the bonus or recovered token counts in tau, not in alpha).  The library returns the counters
+ * only; the two divisions are the caller's (the Python binding's accept_rate_and_length does them
+ * as a convenience outside this interface).
  *
  *   cu_num_draft, out_num_accepted  device int32 [B + 1] and [B] of a spec_reject_sample() call
  *   counters                        device int64 [SPEC_METRIC_COUNT], 8-byte aligned
