@@ -1383,7 +1383,8 @@ constexpr int kLMaxChunks = (SPEC_REJECT_MAX_VOCAB * 4 + kUnitBytes - 1) / kUnit
 #define SPEC_KL_RESIDUAL_UNROLL 8  // 16-byte load groups in flight per lane in the residual pass (fp32 rows)
 #endif
 #ifndef SPEC_KL_RESIDUAL_UNROLL_BF16
-#define SPEC_KL_RESIDUAL_UNROLL_BF16 16  // the same for bf16 rows (measured: 8 -> 16 took 1-2% off large batches)
+#define SPEC_KL_RESIDUAL_UNROLL_BF16 16  // the same for bf16 rows without cuts (8 -> 16 took 1-2% off
+                                         // large batches; with cuts 16 measured 2-4% slower)
 #endif
 #ifndef SPEC_KL_HOST_RESIDUAL_UNROLL
 #define SPEC_KL_HOST_RESIDUAL_UNROLL 2  // the same, draft rows read over the host link (groups loaded before the copies are stored)
@@ -1436,6 +1437,7 @@ static_assert(kCutMid + 32 <= kFKeys + 32 && kCutMid % 32 == 0 && (kCutMid / 32 
 constexpr int kCutList = kFKeys - kCutNarrow;  // per warp: window tokens listed by the narrow count
                                                // (after its counts and a sink per lane)
 constexpr int kKeptMax = 256;         // kept tokens an output row may have for the draw from the list
+static_assert(kKeptMax < kCutList, "a warp lists every kept token of a row that keeps at most kKeptMax");
 static_assert(kCutNarrowChunks <= 8 * kLWarps, "a listed token names its chunk among the warp's in 3 bits");
 static_assert(kUnitBytes / 2 <= 4096, "a listed token's element in its chunk fits 12 bits");
 
@@ -1468,9 +1470,11 @@ struct CutSmem {
     uint32_t thr;                       // cut key of the latest row (0 = none)
     int abort;                          // a copy of a pass did not land in time
     int ln[kLWarps];                    // per warp: window tokens its narrow count met (listed up to kCutList)
-    int lok;                            // the latest cut's window tokens are all listed (narrow path)
+    int lok;                            // the latest cut's kept tokens are all listed (and at most kKeptMax)
+    unsigned nkept;                     // the latest cut's kept tokens (from the window totals)
     int kc[kLWarps];                    // the draw from the list: kept tokens per warp
     int zok;                            // and whether its residual has mass
+    int ktail;                          // and its kept tokens among the row's last V mod 8
     int tok;                            // and its token
     int narrow_miss;                    // the block's latest cut lay below the narrow window
     int mid_miss;                       // and below the middle one
@@ -1797,12 +1801,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     auto count_pass = [&](int w, bool flush) {
         unsigned *h = C.hw[warp];
         const uint32_t sink = (uint32_t)w + (uint32_t)lane;
-        bool tail_in = false;  // a token of a row's last elements (past a multiple of 8) lies in the window
-        auto fe = [&](uint32_t b16) {
-            const uint32_t o = offset(b16);
-            tail_in = tail_in || o < (uint32_t)w;
-            atomicAdd(&h[min(o, sink)], 1u);
-        };
+        auto fe = [&](uint32_t b16) { atomicAdd(&h[min(offset(b16), sink)], 1u); };
         const bool marks = w <= kCutMid;
         const uint32_t lo2 = bf16_pair_of_key(kmax >= (uint32_t)(w - 1) ? kmax - (uint32_t)(w - 1) : 0u);
         // with `flush`, the window's tokens also go to the warp's list (while it has room): (the
@@ -1858,11 +1857,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             pass(reaches, nop, vec, fe, flush_chunk);
         else
             pass(all, nop, vec, fe, flush_chunk);
-        // the last elements are counted, not listed: a window token among them leaves the list
-        // incomplete (taken as overflowing)
-        if (__any_sync(kFull, tail_in))
-            nl = kCutList + 1;
-        if (flush && lane == 0)
+        if (flush && lane == 0)  // (the row's last elements past a multiple of 8 are counted, not listed)
             C.ln[warp] = nl;
         __syncthreads();
     };
@@ -1872,6 +1867,24 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     // while the block's latest cut lay deeper: rows of a batch tend to cut alike, and either
     // path gives the same key and partials.  A chunk with more than 255 tokens on one key of
     // the window takes the wide path too.)
+    // Tokens the cut at offset p keeps (keys kmax - p .. kmax), from the latest window's totals.
+    auto kept_count = [&](int p) -> unsigned {
+        if (warp == 0) {
+            unsigned t = 0;
+            for (int o = lane; o <= p; o += 32)
+                t += C.bh[o];
+            t = __reduce_add_sync(kFull, t);
+            if (lane == 0)
+                C.nkept = t;
+        }
+        __syncthreads();
+        return C.nkept;
+    };
+    // The output row's draw reads its kept tokens from a list (kl_list_draw) exactly when the cut
+    // lies inside the widest window (any of the three finds it, by the block's history) and keeps
+    // at most kKeptMax tokens: a property of the row, so the draw's arithmetic does not depend on
+    // which window the block tried.
+    int pcut = -1;
     if (P.nchunks <= kCutNarrowChunks && !C.narrow_miss) {
         count_pass(kCutNarrow, true);
         int pn = -1;
@@ -1886,14 +1899,21 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             __syncthreads();
             pn = C.pos;
         }
-        if (pn >= 0) {  // K1F's one-pass partials
+        bool narrow_done = false;
+        if (pn >= 0) {
+            const bool few = kept_count(pn) <= (unsigned)kKeptMax;
+            bool listed = true;  // every warp's window tokens are in its list
+            for (int w = 0; w < nw; ++w)
+                listed = listed && C.ln[w] <= kCutList;
+            if (few && !listed)
+                pcut = pn;  // the listing pass below (the partials it gives are these, bit for bit)
+            else
+                narrow_done = true;
+            if (threadIdx.x == 0)
+                C.lok = few && listed;  // read after the barrier below
+        }
+        if (narrow_done) {  // K1F's one-pass partials
             const uint32_t thr = kmax - (uint32_t)pn;
-            if (threadIdx.x == 0) {
-                int ok = 1;
-                for (int w = 0; w < nw; ++w)
-                    ok &= C.ln[w] <= kCutList;
-                C.lok = ok;  // read after the barrier below
-            }
             for (int c = warp; c < P.nchunks; c += nw) {
                 const float mk = C.cmx[c];
                 float mc = -INFINITY, sc = 0.f;
@@ -1910,17 +1930,18 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
             __syncthreads();
             return thr;
         }
-        for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
-            (&C.hw[0][0])[i] = 0u;  // sinks of the narrow window sit inside the wide one
-        if (threadIdx.x == 0)
-            C.narrow_miss = 1;
-        __syncthreads();
+        if (pcut < 0) {
+            for (int i = threadIdx.x; i < nw * (kB + 32); i += blockDim.x)
+                (&C.hw[0][0])[i] = 0u;  // sinks of the narrow window sit inside the wide one
+            if (threadIdx.x == 0)
+                C.narrow_miss = 1;
+            __syncthreads();
+        }
     }
 
     // ---- 1b. counts over the kCutMid largest keys, with marks (skipped while the block's latest
     // cut lay deeper), then 1c. over the kFKeys largest keys, every token counted
-    int pcut = -1;
-    if (!C.mid_miss) {
+    if (pcut < 0 && !C.mid_miss) {
         count_pass(kCutMid, false);
         totals(kCutMid, [&](int o) {
             unsigned t = 0;
@@ -1959,20 +1980,39 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
     }
     if (pcut >= 0) {
         // ---- 3. chunk partials over the survivors: per kept token (marked against the cut key)
-        // the fixed-point mass of its key offset, summed as integers, rescaled to the chunk maximum
+        // the fixed-point mass of its key offset, summed as integers, rescaled to the chunk maximum;
+        // with at most kKeptMax kept tokens the pass also lists them for the draw (a warp lists at
+        // most that many, well inside its room)
         const uint32_t thr = kmax - (uint32_t)pcut;
         const uint32_t thr2 = bf16_pair_of_key(thr);
+        const bool listing = kept_count(pcut) <= (unsigned)kKeptMax;
         auto live = [&](int c) { return C.cmx[c] > -INFINITY && key_of<1>(C.cmx[c]) >= thr; };
         for (int c = warp; c < P.nchunks; c += nw)
             if (lane == 0 && !live(c))
                 spart[c] = make_float2(-INFINITY, 0.f);
         unsigned long long sum = 0;
-        auto add = [&](uint32_t b16, int, unsigned) { sum += C.km[offset(b16)]; };
+        uint32_t *list = C.hw[warp] + kCutNarrow + 32;
+        int nl = 0;
+        const unsigned lt = (1u << lane) - 1u;
+        uint32_t tag = 0;
+        auto add = [&](uint32_t b16, int e, unsigned bal) {
+            sum += C.km[offset(b16)];
+            if (listing) {
+                const int pos = nl + __popc(bal & lt);
+                if (pos < kCutList)
+                    list[pos] = tag + ((uint32_t)e << 16) + b16;
+            }
+        };
+        auto turn = [&](unsigned bal) { nl += __popc(bal); };
         auto fe = [&](uint32_t b16) {
             if (offset(b16) <= (uint32_t)pcut)
                 sum += C.km[offset(b16)];
         };
-        pass(live, nop, [&](const uint4 *st, int nv, int, int) { visit_marked(st, nv, thr2, add, [](unsigned) {}); },
+        pass(live, nop,
+             [&](const uint4 *st, int nv, int c, int lo) {
+                 tag = ((uint32_t)((c - warp) / nw) << 28) | ((uint32_t)(lo - c * P.chunk) << 16);
+                 visit_marked(st, nv, thr2, add, turn);
+             },
              fe, [&](int c) {
                  const float mc = C.cmx[c];
                  const float sc = __ull2float_rn(warp_sum_u64(sum)) * kTwoM32f * ex2(M - mc * cs);
@@ -1980,6 +2020,10 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
                      spart[c] = make_float2(mc, sc);
                  sum = 0;
              });
+        if (lane == 0)
+            C.ln[warp] = nl;
+        if (threadIdx.x == 0)
+            C.lok = listing;  // (nl <= kKeptMax < kCutList in every warp)
         __syncthreads();
         return thr;
     }
@@ -2102,7 +2146,7 @@ template <int DT> __device__ __noinline__ void kl_cut_row(const CutDims P, CutSm
 // an empty residual (modes 0 and 1) draws from 2^(x cs - M).  All threads of the block; returns
 // the token, or -1 when more than kKeptMax tokens are kept (the caller takes the full path).
 __device__ __noinline__ int kl_list_draw(CutSmem &C, int chunk, int mode, const float *qrow, float cs, float M,
-                                         float inv_s, int xstar, float u)
+                                         float inv_s, int xstar, float u, const char *row, int V)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = (int)(blockDim.x >> 5);
@@ -2120,12 +2164,27 @@ __device__ __noinline__ int kl_list_draw(CutSmem &C, int chunk, int mode, const 
     cnt = __reduce_add_sync(kFull, cnt);
     if (lane == 0)
         C.kc[warp] = cnt;
+    // the row's last V mod 8 tokens (past a multiple of 8) are counted by the passes, not listed
+    const int ntail = V & 7;
+    const int tail0 = V - ntail;
+    uint32_t tb = 0;
+    bool tkeep = false;
+    if (warp == 0) {
+        if (lane < ntail) {
+            tb = (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + tail0 + lane);
+            tkeep = key(tb) >= thr;
+        }
+        const unsigned tbal = __ballot_sync(kFull, tkeep);
+        if (lane == 0)
+            C.ktail = __popc(tbal);
+    }
     __syncthreads();
-    int off = 0, total = 0;
+    int off = 0, total = C.ktail, listed_total = 0;
     for (int w = 0; w < nw; ++w) {
         off += w < warp ? C.kc[w] : 0;
-        total += C.kc[w];
+        listed_total += C.kc[w];
     }
+    total += listed_total;
     if (total > kKeptMax || total == 0)
         return -1;  // uniform
     // the kept tokens with 2^(x cs - M), in list order (warp by warp)
@@ -2140,6 +2199,14 @@ __device__ __noinline__ int kl_list_draw(CutSmem &C, int chunk, int mode, const 
             C.kp.w[pos] = ex2(fmaf(__uint_as_float((e & 0xffffu) << 16), cs, -M));
         }
         off += __popc(bal);
+    }
+    if (warp == 0) {  // the kept tail tokens after the listed ones
+        const unsigned bal = __ballot_sync(kFull, tkeep);
+        if (tkeep) {
+            const int pos = listed_total + __popc(bal & lt);
+            C.kp.idx[pos] = tail0 + lane;
+            C.kp.w[pos] = ex2(fmaf(__uint_as_float(tb << 16), cs, -M));
+        }
     }
     __syncthreads();
     // sorted by token (the kept tokens are distinct; rank = kept tokens before it), with their
@@ -2563,7 +2630,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                 // pass, which the list makes unnecessary)
                 const float *qj = mode == 0 ? P.q + (db + j) * P.qstride : nullptr;
                 const int xj = __shfl_sync(kFull, xs, j & 31);
-                token = kl_list_draw(C, P.chunk, mode, qj, cs, s_M, 1.f / s_S, xj, __ldg(P.uni + 2 * tj + 1));
+                token = kl_list_draw(C, P.chunk, mode, qj, cs, s_M, 1.f / s_S, xj, __ldg(P.uni + 2 * tj + 1), rowj,
+                                     P.V);
                 drawn = token >= 0;
                 residual = residual && !drawn;
             }
@@ -2576,8 +2644,8 @@ __global__ void __launch_bounds__(kLThreads, SPEC_KL_MIN_BLOCKS) lazy_kernel(Par
                                     ? warp_residual_chunk<DT, CUT, SPEC_KL_HOST_RESIDUAL_UNROLL, true>(f, lo, hi, lane,
                                                                                                        qstage_j)
                                     : warp_residual_chunk<DT, CUT,
-                                                          DT ? SPEC_KL_RESIDUAL_UNROLL_BF16 : SPEC_KL_RESIDUAL_UNROLL>(
-                                          f, lo, hi, lane);
+                                                          (DT && !CUT) ? SPEC_KL_RESIDUAL_UNROLL_BF16
+                                                                       : SPEC_KL_RESIDUAL_UNROLL>(f, lo, hi, lane);
                 if (lane == 0)
                     lrm[c] = z;
             }

@@ -277,3 +277,31 @@ def test_first_rejection_pass_with_filters_low_chunks(tk, tp):
     assert lazy["status"] == 0
     PT.assert_same_unflagged(w, lazy, full)
     PT.assert_parity(w, lazy)
+
+
+@pytest.mark.gpu
+def test_first_rejection_pass_with_filters_is_deterministic():
+    """The same batch gives the same bits on every call, although which of the cut's windows a
+    block tries first depends on the rows it happened to take before (the request queue's order
+    changes from call to call): a row whose cut lies inside the widest window and keeps at most
+    256 tokens always draws from its listed kept tokens, whichever window found the cut.  Per
+    request cuts at several depths make the blocks' window choices differ between calls."""
+    import torch
+    B = 320
+    rng = np.random.default_rng(41)
+    tk = rng.choice([0, 20, 50, 200, 3000], size=B).astype(np.int32)
+    tp = rng.choice([1.0, 0.5, 0.8, 0.9, 0.95], size=B).astype(np.float32)
+    w = W.generate(dict(B=B, K=6, V=32768, dtype="bf16", sigma=2.0, boost=8.0, temperature=0.7, draft="noisy_q",
+                        q_sigma=0.7, q_temperature=1.0, top_k=tk, top_p=tp, seed=43), name="mixed-depth-cuts")
+    d = binding.to_device(w)
+    kt, kp = torch.from_numpy(tk).cuda(), torch.from_numpy(tp).cuda()
+    buf = binding.make_buffers(w["B"], w["T"], w["V"], binding.BF16, True)
+    first = None
+    for _ in range(6):
+        tokens, acc = binding.sample_filtered(**d, top_k=kt, top_p=kp, buffers=buf)
+        got = (tokens.cpu().numpy().copy(), acc.cpu().numpy().copy())
+        if first is None:
+            first = got
+        assert np.array_equal(got[0], first[0]) and np.array_equal(got[1], first[1])
+    lazy = {"tokens": first[0], "acc": first[1], "status": 0}
+    PT.assert_parity(w, lazy)
