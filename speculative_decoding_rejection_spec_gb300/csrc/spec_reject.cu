@@ -1438,7 +1438,11 @@ constexpr int kCutList = kFKeys - kCutNarrow;  // per warp: window tokens listed
                                                // (after its counts and a sink per lane)
 constexpr int kKeptMax = 256;         // kept tokens an output row may have for the draw from the list
 static_assert(kKeptMax < kCutList, "a warp lists every kept token of a row that keeps at most kKeptMax");
-static_assert(kCutNarrowChunks <= 8 * kLWarps, "a listed token names its chunk among the warp's in 3 bits");
+// A listed token names its chunk among its warp's (c = warp + nw * n) by n in bits 28-31: rows of
+// up to kCutListChunks chunks can be listed (the 128-key count lists only rows of at most
+// kCutNarrowChunks chunks).
+constexpr int kCutListChunks = 16 * kLWarps;
+static_assert(kCutNarrowChunks <= kCutListChunks, "the narrow count's rows fit the list format");
 static_assert(kUnitBytes / 2 <= 4096, "a listed token's element in its chunk fits 12 bits");
 
 struct CutSmem {
@@ -1881,9 +1885,9 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         return C.nkept;
     };
     // The output row's draw reads its kept tokens from a list (kl_list_draw) exactly when the cut
-    // lies inside the widest window (any of the three finds it, by the block's history) and keeps
-    // at most kKeptMax tokens: a property of the row, so the draw's arithmetic does not depend on
-    // which window the block tried.
+    // lies inside the widest window (any of the three finds it, by the block's history), keeps at
+    // most kKeptMax tokens and the row has at most kCutListChunks chunks: a property of the row, so
+    // the draw's arithmetic does not depend on which window the block tried.
     int pcut = -1;
     if (P.nchunks <= kCutNarrowChunks && !C.narrow_miss) {
         count_pass(kCutNarrow, true);
@@ -1985,7 +1989,7 @@ __device__ __noinline__ uint32_t kl_cut_key(const CutDims P, CutSmem &C, float2 
         // most that many, well inside its room)
         const uint32_t thr = kmax - (uint32_t)pcut;
         const uint32_t thr2 = bf16_pair_of_key(thr);
-        const bool listing = kept_count(pcut) <= (unsigned)kKeptMax;
+        const bool listing = kept_count(pcut) <= (unsigned)kKeptMax && P.nchunks <= kCutListChunks;
         auto live = [&](int c) { return C.cmx[c] > -INFINITY && key_of<1>(C.cmx[c]) >= thr; };
         for (int c = warp; c < P.nchunks; c += nw)
             if (lane == 0 && !live(c))

@@ -305,3 +305,17 @@ def test_first_rejection_pass_with_filters_is_deterministic():
         assert np.array_equal(got[0], first[0]) and np.array_equal(got[1], first[1])
     lazy = {"tokens": first[0], "acc": first[1], "status": 0}
     PT.assert_parity(w, lazy)
+
+
+@pytest.mark.gpu
+def test_first_rejection_pass_with_filters_largest_vocab():
+    """Cuts on rows of 530000 bf16 tokens (130 chunks: past what a kept-token list can name, so
+    the output rows draw from the whole row) and of 262143 tokens (64 chunks, the most the
+    128-key count takes per chunk), with top-k small enough for the kept-token draw elsewhere."""
+    for V, seed in ((530000, 51), (262143, 52)):
+        w = W.generate(dict(B=64, K=2, V=V, dtype="bf16", sigma=2.0, boost=8.0, temperature=0.7, draft="noisy_q",
+                            q_sigma=0.7, q_temperature=1.0, top_k=20, top_p=0.9, seed=seed), name=f"cut-V{V}")
+        assert binding.reads_to_first_rejection(w["B"], True)
+        lazy = PT.run_gpu(w)
+        assert lazy["status"] == 0
+        PT.assert_parity(w, lazy)
