@@ -134,7 +134,9 @@ spec_status spec_reject_sample(const void *target_logits, spec_dtype logits_dtyp
  * either may be NULL.  bf16 calls of 64 or more requests on 16-byte-aligned rows (without
  * diagnostics) cut each row the first-rejection pass reaches, in the block that reads it;
  * otherwise every row is cut by one thread-block cluster, at most 8 blocks of at most 20
- * chunks of 8 KB.  Both give the same cut and the same outputs.  The cluster limits V
+ * chunks of 8 KB.  Both give the same cut and decisions; their draws sum the masses in
+ * different orders, so an output token can differ only where the draw falls within fp32
+ * rounding of a boundary between two tokens.  Each is deterministic.  The cluster limits V
  * (V <= 655360 bf16 or 327680 fp32; SPEC_ERR_UNSUPPORTED beyond, for every call with
  * filters).  row_sum and p_draft are
  * optional diagnostic outputs (device fp32 [T] and [T - B]): the restricted normaliser
